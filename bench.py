@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark of layer-major batched int8 prefill on GB300.
+
+One step = one prefill of the whole prompt through every layer (all kernels
+of the path) with weights resident in HBM, last-position logits produced.
+Default workload: Llama-3-8B-shaped int8 decoder, 4096-token prompt, chunks
+of 512 (synthetic, seeded weights and tokens). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 8b|...]
+
+Multi-GPU (torchrun, N > 1): independent replicas, one prompt per rank, no
+collective on the data path ("scaling": "weak").
+`--impl reference` times the CPU oracle (test infrastructure, plain C) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill tok/s (int8 8B-shape, 4096-tok prompt); % of int8-TC/HBM roofline"
+NORTH_HBM_GBS = 8000.0  # the 8 TB/s of the roofline definition
+SMS = 152
+FP32_LANES = 128
+
+
+# ----------------------------------------------------------------------------- accounting
+def layer_weight_bytes(c) -> int:
+    """int8 weights + f32 row scales of one layer (what its GEMMs read)."""
+    return c.layer_bytes() + 4 * (c.qkv_rows + c.dim + 2 * c.ffn + c.dim)
+
+
+def weight_bytes_read(c, prompt: int, chunk: int) -> int:
+    """Layer weights once per chunk plus the output projection once per call
+    ("Batched Prefill", "The arithmetic": the per-token path reads the model
+    once per token; chunking reads it once per chunk)."""
+    n_chunks = -(-prompt // chunk)
+    return layer_weight_bytes(c) * c.n_layers * n_chunks + c.vocab * c.dim + 4 * c.vocab
+
+
+def macs_per_weight_byte(prompt: int, chunk: int) -> float:
+    """Work per weight byte fetched ("Batched Prefill", "The Solution" table): 1 for GEMV, chunk for GEMM."""
+    return prompt / -(-prompt // chunk)
+
+
+def tok_per_s(prompt: int, seconds: float) -> float:
+    return prompt / seconds
+
+
+def algorithmic_work(c, prompt: int, chunk: int) -> dict:
+    """Algorithmic work of one step, per kernel class (flops or bytes)."""
+    D, H, Hkv, hd, F, V, L = c.dim, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn, c.vocab, c.n_layers
+    QD, QKV = H * hd, (H + 2 * Hkv) * hd
+    gemm_flops = 2 * prompt * c.layer_bytes() * L
+    pairs = prompt * (prompt + 1) // 2  # causal (query, key) pairs at start_pos 0
+    attn_flops = 4 * hd * H * pairs * L  # q.k and p.v, 2 flops per multiply-add each
+    # HBM bytes each row kernel must move per token and layer (f32 in, int8 out, plus the row scale)
+    nq_bytes = L * prompt * ((4 + 1) * (2 * D + QD + F) + 4 * 4) + (4 + 1) * D
+    rope_bytes = L * prompt * (4 * QKV + 4 * QD + 4 * 2 * Hkv * hd)
+    lm_head_bytes = V * D + 4 * V + 4 * V
+    embed_bytes = 2 * 4 * prompt * D
+    # attention must read each K/V row of its head group once per chunk and write o
+    n_chunks = -(-prompt // chunk)
+    kv_reads = sum(min(prompt, (i + 1) * chunk) for i in range(n_chunks))
+    attn_bytes = L * (kv_reads * 2 * Hkv * hd * 4 + prompt * 2 * QD * 4)
+    return {
+        "gemm": {"bound": "tensor", "work": gemm_flops, "unit": "TFLOP/s"},
+        "attention": {"bound": "alu", "work": attn_flops, "unit": "TFLOP/s", "bytes": attn_bytes},
+        "norm_quant": {"bound": "hbm", "work": nq_bytes, "unit": "GB/s"},
+        "rope_kv": {"bound": "hbm", "work": rope_bytes, "unit": "GB/s"},
+        "lm_head": {"bound": "hbm", "work": lm_head_bytes, "unit": "GB/s"},
+        "embed": {"bound": "hbm", "work": embed_bytes, "unit": "GB/s"},
+    }
+
+
+def step_bytes(c, prompt: int, chunk: int) -> int:
+    """HBM bytes of one step for the prefill roofline: weights once per chunk,
+    the K/V cache written once and read once per chunk, embeddings, activations."""
+    w = algorithmic_work(c, prompt, chunk)
+    return weight_bytes_read(c, prompt, chunk) + w["attention"]["bytes"] + w["norm_quant"]["work"] + \
+        w["rope_kv"]["work"] + w["embed"]["work"]
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+def peak_for(bound: str, peaks: dict) -> tuple[float, str]:
+    if bound == "tensor":
+        # the exact-integer GEMMs run at f16 operand rate; bf16 and f16 dense rates are equal
+        return float(peaks["bf16_tflops_sustained"]), f"bf16/f16 dense sustained ({peaks['source']})"
+    if bound == "alu":
+        clk = float(peaks.get("sm_max_mhz", 2070.0))
+        return SMS * FP32_LANES * 2 * clk * 1e6 / 1e12, f"FP32 FMA: {SMS} SMs x {FP32_LANES} lanes x 2 x {clk:.0f} MHz"
+    return float(peaks["hbm_gbs"]), f"HBM copy ({peaks['source']})"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.device)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float) -> float:
+    if pg is None:
+        return value
+    import torch
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(model, cfg, sample_tokens: int, toks) -> tuple[float, int, float]:
+    """Time the oracle (as it stands) prefilling the first `sample_tokens`
+    tokens of the prompt in one chunk, one thread per host core."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    om = oracle.OracleModel(model, max_seq=sample_tokens, n_threads=cores)
+    t0 = time.perf_counter()
+    om.prefill(toks[:sample_tokens], 0, sample_tokens)
+    dt = time.perf_counter() - t0
+    om.close()
+    return sample_tokens / dt, cores, dt
+
+
+def run_reference(args, cfg, world, rank, pg):
+    """--impl reference: the oracle on the host cores, bounded sample per step."""
+    if rank != 0:
+        return 0
+    import synth
+
+    model = synth.make_model(cfg)
+    toks = synth.prompt(cfg, cfg.prompt_len)
+    sample = args.ref_sample_tokens
+    for _ in range(args.warmup):
+        oracle_sample(model, cfg, sample, toks)
+    times = []
+    cores = os.cpu_count() or 1
+    for _ in range(args.steps):
+        _, cores, dt = oracle_sample(model, cfg, sample, toks)
+        times.append(dt)
+    total = sum(times)
+    value = sample * args.steps / total
+    desc = (f"oracle prefill of the first {sample} tokens of the {cfg.prompt_len}-token prompt, one chunk, "
+            f"{cores} threads, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": workload_config(cfg, args),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg, args) -> dict:
+    names = {"8b": "Llama-3-8B-shaped int8 decoder, weights resident in HBM",
+             "350m": "350M-class int8 decoder", "1b": "1B-class int8 decoder", "tiny": "tiny int8 decoder"}
+    return {"workload": f"{names.get(cfg.name, cfg.name)}: {cfg.prompt_len}-token prompt, chunk {args.chunk}, "
+                        f"start_pos 0, last-position logits",
+            "dim": cfg.dim, "layers": cfg.n_layers, "heads": cfg.n_heads, "kv_heads": cfg.n_kv_heads,
+            "head_dim": cfg.head_dim, "ffn": cfg.ffn, "vocab": cfg.vocab, "prompt_tokens": cfg.prompt_len,
+            "chunk": args.chunk, "weights": "resident",
+            "l2": "inputs larger than L2 (every step reads all layer weights, %.2f GB int8)" % (
+                cfg.layer_bytes() * cfg.n_layers / 1e9),
+            "parallelism": "replicas" if int(os.environ.get("WORLD_SIZE", "1")) > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, cfg, world, rank, local, pg):
+    import torch
+
+    import prompt_prefill_gb300 as pp
+    import synth
+
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    P, chunk = cfg.prompt_len, args.chunk
+    model = synth.make_model(cfg)
+    toks = synth.prompt(cfg, P, seed=cfg.seed + rank)
+    g = pp.PrefillModel(cfg, model, max_seq=max(cfg.max_seq, P), max_chunk=chunk, gemm_engine=args.engine)
+    stream = torch.cuda.current_stream()
+    d_tok = torch.from_numpy(toks).cuda()
+    d_logits = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+
+    def step():
+        g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)
+
+    # warm-up, then one profiled step per kernel class to find the dominant one
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert g.device_status() == pp.PP_OK
+    class_ms = {}
+    for cls, name in pp.KERNEL_NAMES.items():
+        g.set_profile_kernel(cls)
+        g.reset_stats()
+        step()
+        s = g.stats()
+        class_ms[name] = s["prof_ms"]
+    dominant = max(class_ms, key=class_ms.get)
+    dom_cls = {v: k for k, v in pp.KERNEL_NAMES.items()}[dominant]
+    g.set_profile_kernel(dom_cls)
+    g.reset_stats()
+
+    # timed region: K steps, device-resident inputs
+    clocks = ClockSampler(local).start()
+    barrier(pg)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(pg, ms)
+    stats = g.stats()
+    launches = stats["kernel_launches"]
+    logits = d_logits.cpu().numpy()
+    assert np.all(np.isfinite(logits)), "non-finite logits"
+
+    # e2e: the host C-ABI call (token ids host->device, logits device->host inside)
+    g.set_profile_kernel(pp.PP_KERNEL_NONE)
+    barrier(pg)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        host_logits = g.prefill(toks, 0, chunk)
+    t_e2e = time.perf_counter() - t0
+    t_e2e = max_over_ranks(pg, t_e2e)
+    assert np.array_equal(host_logits.view(np.uint32), logits.view(np.uint32)), "host and device paths differ"
+
+    value = world * P * args.steps / (ms_max / 1000.0)
+    e2e_value = world * P * args.steps / t_e2e
+    work = algorithmic_work(cfg, P, chunk)[dominant]
+    achieved_ms = stats["prof_ms"] / max(1, stats["prof_launches"])
+    per_launch = work["work"] / max(1, stats["prof_launches"] // args.steps)
+    scale = 1e12 if work["unit"] == "TFLOP/s" else 1e9
+    achieved = per_launch / (achieved_ms / 1000.0) / scale
+    peak, peak_src = peak_for(work["bound"], peaks)
+
+    # prefill roofline of the metric: max(GEMM ops / tensor peak, bytes / 8 TB/s)
+    gemm_ops = work_total = algorithmic_work(cfg, P, chunk)["gemm"]["work"]
+    bytes_step = step_bytes(cfg, P, chunk)
+    t_tc = gemm_ops / (peak_for("tensor", peaks)[0] * 1e12)
+    t_roof = max(t_tc, bytes_step / (NORTH_HBM_GBS * 1e9))
+    t_roof_meas = max(t_tc, bytes_step / (float(peaks["hbm_gbs"]) * 1e9))
+    step_s = ms_max / 1000.0 / args.steps
+    del work_total
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded N(0,0.02) int8 per-row weights, uniform ids)",
+        "config": workload_config(cfg, args),
+        "gemm_engine": {pp.PP_GEMM_MMA: "mma.sync s8", pp.PP_GEMM_TC: "tcgen05 exact-integer f16"}.get(g.gemm_engine),
+        "prefill_roofline": {"t_roof_ms": 1000 * t_roof, "frac": t_roof / step_s, "tensor_peak_tflops": peak_for(
+            "tensor", peaks)[0], "hbm_gbs": NORTH_HBM_GBS, "frac_vs_measured_hbm": t_roof_meas / step_s,
+            "gemm_tops": gemm_ops / 1e12, "bytes_gb": bytes_step / 1e9},
+        "roofline": {"kernel": dominant, "bound": work["bound"], "achieved": achieved, "peak": peak,
+                     "unit": work["unit"], "frac": achieved / peak, "traffic": None, "peak_source": peak_src},
+        "kernel_ms_per_step": {k: v for k, v in class_ms.items()},
+        "weight_bytes_read_per_step": weight_bytes_read(cfg, P, chunk),
+        "weight_bytes_naive_per_step": layer_weight_bytes(cfg) * cfg.n_layers * P + cfg.vocab * cfg.dim + 4 * cfg.vocab,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4 * P, "d2h_bytes_per_step": 4 * cfg.vocab},
+        "gpu_launches": launches,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, dt = oracle_sample(model, cfg, args.cpu_sample_tokens, toks)
+        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": f"oracle prefill of the first {args.cpu_sample_tokens} tokens of the prompt "
+                                          f"in one chunk ({dt:.1f} s)"}
+    g.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="8b")
+    ap.add_argument("--chunk", type=int, default=None)
+    ap.add_argument("--prompt", type=int, default=None)
+    ap.add_argument("--engine", type=int, default=0, help="0 auto, 1 mma.sync, 2 tcgen05")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--ref-sample-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least 3 warm-up steps
+    import synth
+
+    cfg = synth.CONFIGS[args.workload]
+    if args.prompt:
+        cfg.prompt_len = args.prompt
+    args.chunk = args.chunk or cfg.chunk
+    world, rank, local, pg = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, cfg, world, rank, pg)
+        return run_ours(args, cfg, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,256 @@
+/*
+ * pp.h -- C ABI of the GB300 layer-major batched int8 prefill library (libpp.so).
+ *
+ * What the library computes (sources are web pages on prompt prefill):
+ *  - "Single-pass prefill" (SipLLM), section "The fix: batch over positions,
+ *    stream each layer once": prefill(tokens, n, start_pos) inverts the loop
+ *    nesting -- for each layer, read its weights once and sweep every prompt
+ *    position through it; the causal K/V history kv[layer][0..i] is written
+ *    position by position; only the last position's logits are produced,
+ *    after a final RMSNorm and the output projection.
+ *  - "Batched Prefill" (cellm), sections "The Solution", "What Stays
+ *    Sequential", "Correctness": the projections become int8 GEMMs over a
+ *    chunk of positions (weights read once per chunk), activations are
+ *    quantised once per chunk and reused by every output row, attention is
+ *    causal per position, and the chunked result equals the per-token path.
+ *  - "Predictive prefetch" (SipLLM), section "The fix: an async double-buffer
+ *    ring": in streamed mode layer L+1 is copied into the other ring slot
+ *    while layer L computes; prefetch hits and misses are counted.
+ *
+ * Model: decoder-only transformer with RMSNorm, RoPE, grouped KV heads,
+ * SwiGLU FFN, int8 per-output-row weights with f32 row scales, f32
+ * embeddings, untied int8 output projection.
+ *
+ * Conventions for every entry point:
+ *  - Return value: PP_OK (0) or a negative PP_ERR_* code. pp_last_error()
+ *    gives a one-line description of the most recent failure on the calling
+ *    thread.
+ *  - "host" pointers are ordinary CPU memory; "device" pointers are CUDA
+ *    global memory on the model's device. The caller owns every buffer it
+ *    passes; the library never frees or retains them past the call, except
+ *    where a function says otherwise.
+ *  - A pp_model is used by one host thread at a time.
+ *  - Nothing here falls back to the CPU: without a CUDA device every compute
+ *    entry point fails with PP_ERR_CUDA.
+ */
+#ifndef PP_H
+#define PP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define PP_OK 0
+#define PP_ERR_ARG -1             /* null pointer, non-positive size, bad token id, unsupported shape */
+#define PP_ERR_CAPACITY -2        /* start_pos + n exceeds the KV capacity max_seq */
+#define PP_ERR_OOM -3             /* device or pinned-host allocation failed */
+#define PP_ERR_CUDA -4            /* a CUDA runtime call failed (no device, launch error, ...) */
+#define PP_ERR_DEVICE_TIMEOUT -5  /* a bounded device-side wait gave up; the kernel exited early */
+#define PP_ERR_UNSUPPORTED -6     /* requested engine or mode is not available on this device */
+
+/* ------------------------------------------------------------- constants */
+#define PP_MODE_RESIDENT 0  /* every layer resident in HBM */
+#define PP_MODE_STREAMED 1  /* layers in pinned host memory, streamed into a device ring */
+
+#define PP_GEMM_AUTO 0      /* fastest engine that passed its self-check on this device */
+#define PP_GEMM_MMA 1       /* warp-level mma.sync s8 x s8 -> s32 */
+#define PP_GEMM_TC 2        /* tcgen05 exact-integer GEMM (fp16 operands, f32 TMEM, int32 drain) */
+
+/* Kernel classes that pp_config.profile_kernel can time with CUDA events. */
+#define PP_KERNEL_NONE -1
+#define PP_KERNEL_GEMM 0        /* all projection GEMMs */
+#define PP_KERNEL_ATTENTION 1
+#define PP_KERNEL_NORM_QUANT 2  /* RMSNorm + quantise and plain quantise */
+#define PP_KERNEL_ROPE_KV 3
+#define PP_KERNEL_LM_HEAD 4
+#define PP_KERNEL_EMBED 5
+#define PP_KERNEL_COUNT 6
+
+/* Epilogues of pp_op_gemm (out is f32 [m][n] row-major, ldo = n unless stated). */
+#define PP_EPI_STORE 0   /* out[t][r] = (float(acc) * w_scale[r]) * a_scale[t] */
+#define PP_EPI_RESID 1   /* out[t][r] = out[t][r] + (float(acc) * w_scale[r]) * a_scale[t] */
+#define PP_EPI_SWIGLU 2  /* rows interleaved in blocks of 16 (gate 16, up 16, ...):
+                            out[t][16b+i] = silu(g) * u, out is [m][n/2] */
+
+/* ------------------------------------------------------------------ model */
+typedef struct pp_config {
+  int32_t dim;          /* model width D */
+  int32_t n_layers;
+  int32_t n_heads;      /* query heads H */
+  int32_t n_kv_heads;   /* KV heads Hkv, divides H */
+  int32_t head_dim;     /* hd: 64 or 128 */
+  int32_t ffn;          /* SwiGLU hidden width F, multiple of 16 */
+  int32_t vocab;        /* V */
+  float rms_eps;
+  float rope_theta;
+  int32_t max_seq;      /* KV capacity (positions); start_pos + n must not exceed it */
+  int32_t max_chunk;    /* largest chunk any prefill call uses; sizes the activation scratch */
+  int32_t mode;         /* PP_MODE_RESIDENT or PP_MODE_STREAMED */
+  int32_t ring_slots;   /* streamed mode: 2 = double-buffer prefetch ring, 1 = synchronous single buffer */
+  int32_t gemm_engine;  /* PP_GEMM_* */
+  int32_t use_graphs;   /* resident mode: replay each chunk length's layer loop as a CUDA graph */
+  int32_t profile_kernel; /* PP_KERNEL_* class to time with events around each launch, or PP_KERNEL_NONE */
+} pp_config;
+
+/* Host weights (the pages' WeightSource seam: the math sees only these).
+ * All matrices are int8 row-major [out][in] with one f32 scale per output row.
+ * Per layer, in this order: wq [H*hd][D], wk [Hkv*hd][D], wv [Hkv*hd][D],
+ * wo [D][H*hd], wg [F][D], wu [F][D], wd [D][F].
+ * Read during pp_model_load only: in resident mode they are copied to the
+ * device, in streamed mode into library-owned pinned host memory. */
+typedef struct pp_weights {
+  const float* tok_emb;          /* [vocab][D] f32 */
+  const int8_t* const* w;        /* [n_layers * 7] matrices as above */
+  const float* const* w_scale;   /* [n_layers * 7] row scales */
+  const float* const* attn_norm; /* [n_layers] -> [D] RMSNorm gain before attention */
+  const float* const* ffn_norm;  /* [n_layers] -> [D] RMSNorm gain before the FFN */
+  const float* final_norm;       /* [D] */
+  const int8_t* w_out;           /* [vocab][D] output projection */
+  const float* w_out_scale;      /* [vocab] */
+} pp_weights;
+
+typedef struct pp_stats {
+  int64_t calls;              /* prefill calls that completed */
+  int64_t chunks;             /* chunks processed */
+  int64_t tokens;             /* prompt positions processed */
+  int64_t weight_bytes_read;  /* int8 weight + scale bytes the kernels fetch by design: every layer once
+                                 per chunk, the output projection once per call ("Streamed" bytes) */
+  int64_t h2d_bytes;          /* host-to-device bytes: token ids, and layer copies in streamed mode */
+  int64_t prefetch_hits;      /* streamed mode: layer copy finished before the compute stream needed it */
+  int64_t prefetch_misses;    /* streamed mode: compute waited on the copy (includes each call's first layer) */
+  int64_t kernel_launches;    /* kernels this library launched (graph replays count their kernels) */
+  int64_t prof_launches;      /* launches of the profiled kernel class */
+  double prof_ms;             /* summed event-timed duration of those launches */
+} pp_stats;
+
+typedef struct pp_model pp_model;
+
+/* Create a model on the current CUDA device: validates cfg, repacks and
+ * uploads (or pins) the weights, allocates the K/V cache for max_seq
+ * positions, the activation scratch for max_chunk positions and the RoPE
+ * table. On failure *out is NULL and nothing is leaked.
+ * Errors: PP_ERR_ARG (bad cfg or null pointers), PP_ERR_OOM, PP_ERR_CUDA,
+ * PP_ERR_UNSUPPORTED (gemm_engine not available). */
+int pp_model_load(const pp_config* cfg, const pp_weights* w, pp_model** out);
+
+/* Release all device and host memory of the model. NULL is a no-op. */
+void pp_model_free(pp_model* m);
+
+/* Layer-major prefill of host tokens[0..n) at positions start_pos ..
+ * start_pos+n-1, `chunk` positions at a time (the last chunk may be ragged),
+ * writing the last position's logits to host logits_out [vocab] f32.
+ * Positions < start_pos must hold K/V from earlier calls (or be unused).
+ * Synchronous: returns after logits_out is written.
+ * Errors: PP_ERR_ARG (null, n <= 0, chunk <= 0 or > max_chunk, start_pos < 0,
+ * token id outside [0, vocab)), PP_ERR_CAPACITY (start_pos + n > max_seq),
+ * PP_ERR_CUDA, PP_ERR_DEVICE_TIMEOUT. On error logits_out is untouched and
+ * K/V rows at positions >= start_pos are undefined. */
+int pp_prefill(pp_model* m, const int32_t* tokens, int32_t n, int32_t start_pos, int32_t chunk,
+               float* logits_out);
+
+/* Same computation with device-resident ids d_tokens [n] and device output
+ * d_logits [vocab], enqueued on `stream` (a cudaStream_t; NULL selects the
+ * model's own stream) without host synchronisation. Ids are checked on the
+ * device: an id outside [0, vocab) gives a zero embedding row and records
+ * PP_ERR_ARG in the model's device status, read by pp_device_status(). */
+int pp_prefill_device(pp_model* m, const int32_t* d_tokens, int32_t n, int32_t start_pos, int32_t chunk,
+                      float* d_logits, void* stream);
+
+/* The per-token path: pp_prefill(m, &token, 1, pos, 1, logits_out). */
+int pp_forward_one(pp_model* m, int32_t token, int32_t pos, float* logits_out);
+
+/* Synchronise the model's streams and return (and clear) the device status
+ * word: PP_OK, PP_ERR_ARG (bad id seen by pp_prefill_device) or
+ * PP_ERR_DEVICE_TIMEOUT. */
+int pp_device_status(pp_model* m);
+
+/* Zero the whole K/V cache. */
+int pp_kv_reset(pp_model* m);
+
+/* Copy K (which = 0) or V (which = 1) rows [pos0, pos0+n_pos) of one layer to
+ * host out [n_pos][n_kv_heads][head_dim] f32. */
+int pp_kv_read(pp_model* m, int32_t layer, int32_t which, int32_t pos0, int32_t n_pos, float* out);
+
+int pp_get_stats(const pp_model* m, pp_stats* out);
+int pp_reset_stats(pp_model* m);
+
+/* Select the kernel class (PP_KERNEL_*, or PP_KERNEL_NONE) whose launches are
+ * bracketed by CUDA events on the launching stream from now on; their count
+ * and summed duration appear in pp_stats (prof_launches, prof_ms). */
+int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
+
+/* The GEMM engine the model resolved to (PP_GEMM_MMA or PP_GEMM_TC). */
+int pp_model_gemm_engine(const pp_model* m);
+
+/* Static text for a status code. */
+const char* pp_status_str(int status);
+/* Description of the last failure on this thread ("" if none). */
+const char* pp_last_error(void);
+
+/* ------------------------------------------------- single steps (device) */
+/* Each step of the hot path as its own entry point, on device pointers,
+ * enqueued on `stream` (cudaStream_t; NULL = legacy default stream). They
+ * run the same kernels, with the same launch shapes, as the model. Sizes
+ * are checked on the host (PP_ERR_ARG); launch failures give PP_ERR_CUDA. */
+
+/* Per-token absmax quantiser ("Batched Prefill", "The Solution": activations
+ * quantised once per chunk). For each row t of x [rows][k] f32:
+ * amax = max|x|, a_scale[t] = amax/127, q = clamp(rint_even(x * (127/amax)),
+ * -127, 127) in f32; amax == 0 gives q = 0, a_scale = 0. Writes q8 [rows][k]
+ * int8 and, if q16 is not NULL, the same codes as fp16 [rows][k]. */
+int pp_op_quantize(const float* x, int32_t rows, int32_t k, int8_t* q8, uint16_t* q16, float* a_scale,
+                   void* stream);
+
+/* RMSNorm then quantise: y = x / sqrt(mean(x^2) + eps) * g (f32), then as
+ * pp_op_quantize. If y_out is not NULL the normalised rows are written too. */
+int pp_op_rmsnorm_quantize(const float* x, const float* g, int32_t rows, int32_t k, float eps, float* y_out,
+                           int8_t* q8, uint16_t* q16, float* a_scale, void* stream);
+
+/* Exact int8 GEMM: acc[t][r] = sum_i a[t][i] * w[r][i] as int32.
+ * a8 [m][k] int8 (used by PP_GEMM_MMA), a16 [m][k] fp16 holding the same
+ * integer codes (used by PP_GEMM_TC), w [n][k] int8. Needs k % 64 == 0 and
+ * n % 32 == 0 (PP_GEMM_TC: n % 128 == 0). */
+int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m,
+                   int32_t n, int32_t k, int32_t* acc, void* stream);
+
+/* The same GEMM with its dequantising epilogue PP_EPI_* (f32, in the fixed
+ * order (float(acc) * w_scale[r]) * a_scale[t]); out is f32 with leading
+ * dimension ldo. */
+int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_t* a16, const int8_t* w,
+               const float* w_scale, const float* a_scale, int32_t m, int32_t n, int32_t k, float* out,
+               int32_t ldo, void* stream);
+
+/* RoPE + K/V write for `rows` positions start_pos..: qkv [rows][(H+2Hkv)*hd]
+ * f32 (q heads, then k heads, then v heads) -> q_out [rows][H][hd] rotated,
+ * k rotated into k_cache[start_pos+i], v copied into v_cache[start_pos+i]
+ * (caches [*][Hkv][hd] f32). Pairs (j, j+hd/2) turn by pos*theta^(-2j/hd).
+ * rope_table [max_pos][hd/2][2] (cos, sin) comes from pp_op_rope_table. */
+int pp_op_rope_kv(const float* qkv, int32_t rows, int32_t start_pos, int32_t n_heads, int32_t n_kv_heads,
+                  int32_t head_dim, const float* rope_table, float* q_out, float* k_cache, float* v_cache,
+                  void* stream);
+
+/* Fill rope_table [max_pos][hd/2][2] with cos/sin of pos*theta^(-2j/hd)
+ * (angles in double, rounded to f32). */
+int pp_op_rope_table(int32_t max_pos, int32_t head_dim, float theta, float* rope_table, void* stream);
+
+/* Causal attention ("Single-pass prefill": position i attends over
+ * kv[0..i]): q [rows][H][hd] at positions start_pos+i, k/v caches
+ * [*][Hkv][hd]; o [rows][H][hd] = softmax((q.k_j)/sqrt(hd), j <= pos) v.
+ * Query head h reads KV head h / (H / Hkv). f32 on CUDA cores; every
+ * query's reduction order depends only on its absolute position. */
+int pp_op_attention(const float* q, const float* k_cache, const float* v_cache, int32_t rows, int32_t start_pos,
+                    int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float* o, void* stream);
+
+/* Output projection of one quantised row: logits[v] = (float(sum_i q8[i] *
+ * w_out[v][i]) * w_scale[v]) * a_scale[0], for v < vocab. */
+int pp_op_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w_out, const float* w_scale,
+                  int32_t vocab, int32_t dim, float* logits, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PP_H */

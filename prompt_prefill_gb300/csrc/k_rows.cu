@@ -1,0 +1,249 @@
+// Row-wise kernels of the prefill path: embedding gather, RMSNorm + per-token
+// int8 quantiser, RoPE table and RoPE + K/V write, and the last-position
+// output projection. All are HBM/L2-bound; each keeps every per-row reduction
+// in one fixed order so that a row's result never depends on which other rows
+// share its launch (the chunk size).
+#include "pp_internal.cuh"
+
+namespace pp {
+namespace {
+
+constexpr int kRowThreads = 256;
+
+// Embedding gather ("Single-pass prefill": prefill runs the prompt through the
+// model): x[i] = emb[tok[i]]. Ids outside [0, vocab) give a zero row and set
+// the device status word.
+__global__ void __launch_bounds__(kRowThreads) k_embed(const int32_t* __restrict__ tok, const float* __restrict__ emb,
+                                                     int vocab, int dim, float* __restrict__ x, int* status) {
+  const int i = blockIdx.x;
+  const int t = tok[i];
+  const bool ok = t >= 0 && t < vocab;
+  if (!ok && threadIdx.x == 0 && status) atomicCAS(status, DEV_OK, DEV_BAD_TOKEN);
+  const float4* src = reinterpret_cast<const float4*>(emb + (size_t)(ok ? t : 0) * dim);
+  float4* dst = reinterpret_cast<float4*>(x + (size_t)i * dim);
+  for (int c = threadIdx.x; c < dim / 4; c += kRowThreads) dst[c] = ok ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Fixed-order block reductions: per-thread partials, xor butterfly within a
+// warp, then warp 0 folds the 8 warp results in index order.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.f;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRowThreads / 32; ++i) s += red[i];
+    red[kRowThreads / 32] = s;
+  }
+  __syncthreads();
+  return red[kRowThreads / 32];
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    for (int i = 0; i < kRowThreads / 32; ++i) m = fmaxf(m, red[i]);
+    red[kRowThreads / 32] = m;
+  }
+  __syncthreads();
+  return red[kRowThreads / 32];
+}
+
+// RMSNorm (optional) then the per-token absmax quantiser ("Batched Prefill",
+// "The Solution": quantise each token once per chunk; every output row reuses
+// the codes). One CTA per row:
+//   r = 1 / sqrt(sum(x^2)/k + eps), y = (x * r) * g            (NORM only)
+//   amax = max|y|, inv = 127/amax, q = clamp(rint_even(y*inv), +-127), a_scale = amax/127
+// All f32 with IEEE division and square root; amax == 0 gives q = 0, a_scale = 0.
+template <bool NORM>
+__global__ void __launch_bounds__(kRowThreads)
+    k_norm_quant(const float* __restrict__ x, int ldx, const float* __restrict__ g, int k, float eps,
+                 float* __restrict__ y_out, int8_t* __restrict__ q8, __half* __restrict__ q16,
+                 float* __restrict__ a_scale) {
+  __shared__ float red[kRowThreads / 32 + 1];
+  const int row = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  const int k4 = k >> 2;
+  float r = 1.f;
+  if (NORM) {
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < k4; c += kRowThreads) {
+      const float4 v = xr[c];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+    ss = block_sum(ss, red);
+    r = 1.0f / sqrtf(ss / (float)k + eps);
+  }
+  auto yval = [&](float xv, float gv) { return NORM ? __fmul_rn(__fmul_rn(xv, r), gv) : xv; };
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < k4; c += kRowThreads) {
+    const float4 v = xr[c];
+    const float4 gg = NORM ? g4[c] : make_float4(1.f, 1.f, 1.f, 1.f);
+    amax = fmaxf(amax, fabsf(yval(v.x, gg.x)));
+    amax = fmaxf(amax, fabsf(yval(v.y, gg.y)));
+    amax = fmaxf(amax, fabsf(yval(v.z, gg.z)));
+    amax = fmaxf(amax, fabsf(yval(v.w, gg.w)));
+  }
+  amax = block_max(amax, red);
+  const bool zero = amax == 0.f;
+  const float inv = zero ? 0.f : 127.0f / amax;
+  for (int c = threadIdx.x; c < k4; c += kRowThreads) {
+    const float4 v = xr[c];
+    const float4 gg = NORM ? g4[c] : make_float4(1.f, 1.f, 1.f, 1.f);
+    float y[4] = {yval(v.x, gg.x), yval(v.y, gg.y), yval(v.z, gg.z), yval(v.w, gg.w)};
+    int qi[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int q = zero ? 0 : __float2int_rn(__fmul_rn(y[e], inv));
+      qi[e] = q > 127 ? 127 : (q < -127 ? -127 : q);
+    }
+    const size_t base = (size_t)row * k + 4 * (size_t)c;
+    char4 p = make_char4((signed char)qi[0], (signed char)qi[1], (signed char)qi[2], (signed char)qi[3]);
+    *reinterpret_cast<char4*>(q8 + base) = p;
+    if (q16) {
+      __half2 h01 = __halves2half2(__int2half_rn(qi[0]), __int2half_rn(qi[1]));
+      __half2 h23 = __halves2half2(__int2half_rn(qi[2]), __int2half_rn(qi[3]));
+      reinterpret_cast<__half2*>(q16 + base)[0] = h01;
+      reinterpret_cast<__half2*>(q16 + base)[1] = h23;
+    }
+    if (y_out) reinterpret_cast<float4*>(y_out + base)[0] = make_float4(y[0], y[1], y[2], y[3]);
+  }
+  if (threadIdx.x == 0) a_scale[row] = zero ? 0.f : amax / 127.0f;
+}
+
+// RoPE table: table[pos][j] = (cos, sin)(pos * theta^(-2j/hd)), angles in double.
+__global__ void k_rope_table(int max_pos, int hd, double theta, float2* __restrict__ table) {
+  const int half = hd / 2;
+  const long long n = (long long)max_pos * half;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+    const int pos = (int)(e / half), j = (int)(e % half);
+    const double freq = pow(theta, -2.0 * (double)j / (double)hd);
+    double s, c;
+    sincos((double)pos * freq, &s, &c);
+    table[e] = make_float2((float)c, (float)s);
+  }
+}
+
+// RoPE + K/V write ("Single-pass prefill": K/V history written position by
+// position). qkv row = [q heads | k heads | v heads]; pairs (j, j + hd/2).
+__global__ void __launch_bounds__(kRowThreads)
+    k_rope_kv(const float* __restrict__ qkv, int start_pos, int H, int Hkv, int hd, const float2* __restrict__ table,
+              float* __restrict__ q_out, float* __restrict__ k_cache, float* __restrict__ v_cache) {
+  const int i = blockIdx.x;
+  const int pos = start_pos + i;
+  const int half = hd / 2;
+  const int ld = (H + 2 * Hkv) * hd;
+  const float* row = qkv + (size_t)i * ld;
+  const float2* tab = table + (size_t)pos * half;
+  const int n_rot = (H + Hkv) * half;
+  for (int e = threadIdx.x; e < n_rot; e += kRowThreads) {
+    const int head = e / half, j = e % half;
+    const float2 cs = tab[j];
+    const float a = row[head * hd + j], b = row[head * hd + j + half];
+    const float ra = a * cs.x - b * cs.y;
+    const float rb = a * cs.y + b * cs.x;
+    if (head < H) {
+      float* dst = q_out + ((size_t)i * H + head) * hd;
+      dst[j] = ra;
+      dst[j + half] = rb;
+    } else {
+      float* dst = k_cache + ((size_t)pos * Hkv + (head - H)) * hd;
+      dst[j] = ra;
+      dst[j + half] = rb;
+    }
+  }
+  const float* vrow = row + (size_t)(H + Hkv) * hd;
+  float* vdst = v_cache + (size_t)pos * Hkv * hd;
+  for (int e = threadIdx.x; e < Hkv * hd; e += kRowThreads) vdst[e] = vrow[e];
+}
+
+// Output projection of the last position ("Single-pass prefill": logits for
+// the last position only). One warp per vocabulary row; the int32 dot product
+// is exact, so the lane split does not matter.
+__global__ void __launch_bounds__(kRowThreads)
+    k_lm_head(const int8_t* __restrict__ q8, const float* __restrict__ a_scale, const int8_t* __restrict__ w,
+              const float* __restrict__ ws, int vocab, int dim, float* __restrict__ logits) {
+  extern __shared__ int4 qs[];
+  const int n16 = dim / 16;
+  for (int c = threadIdx.x; c < n16; c += kRowThreads) qs[c] = reinterpret_cast<const int4*>(q8)[c];
+  __syncthreads();
+  const float as = a_scale[0];
+  const int lane = threadIdx.x & 31;
+  const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
+  const int n_warps = (gridDim.x * kRowThreads) >> 5;
+  for (int v = warp; v < vocab; v += n_warps) {
+    const int4* wr = reinterpret_cast<const int4*>(w + (size_t)v * dim);
+    int acc = 0;
+#pragma unroll 4
+    for (int c = lane; c < n16; c += 32) {
+      const int4 a = __ldg(wr + c);
+      const int4 b = qs[c];
+      acc = __dp4a(a.x, b.x, acc);
+      acc = __dp4a(a.y, b.y, acc);
+      acc = __dp4a(a.z, b.z, acc);
+      acc = __dp4a(a.w, b.w, acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) logits[v] = ppdev::dequant(acc, ws[v], as);
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab, int dim, float* x, int* status,
+                         cudaStream_t s) {
+  k_embed<<<n, kRowThreads, 0, s>>>(tok, emb, vocab, dim, x, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
+                              int8_t* q8, __half* q16, float* a_scale, cudaStream_t s) {
+  if (g)
+    k_norm_quant<true><<<rows, kRowThreads, 0, s>>>(x, ldx, g, k, eps, y, q8, q16, a_scale);
+  else
+    k_norm_quant<false><<<rows, kRowThreads, 0, s>>>(x, ldx, g, k, eps, y, q8, q16, a_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s) {
+  k_rope_table<<<sm_count() * 4, 256, 0, s>>>(max_pos, hd, (double)theta, reinterpret_cast<float2*>(table));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
+                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s) {
+  k_rope_kv<<<rows, kRowThreads, 0, s>>>(qkv, start_pos, H, Hkv, hd, reinterpret_cast<const float2*>(table), q_out,
+                                         k_cache, v_cache);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,
+                           int dim, float* logits, cudaStream_t s) {
+  const int blocks = sm_count() * 4;
+  k_lm_head<<<blocks, kRowThreads, dim, s>>>(q8, a_scale, w, ws, vocab, dim, logits);
+  return cudaGetLastError();
+}
+
+}  // namespace pp

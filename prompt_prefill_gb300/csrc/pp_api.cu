@@ -1,0 +1,761 @@
+// Host runtime behind the C ABI of include/pp.h: model load and repack, the
+// layer-major prefill loop, the streamed-mode prefetch ring, statistics and
+// the single-step entry points. Every step of the computation runs in this
+// library's kernels; the host only validates, sequences and copies.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pp_internal.cuh"
+
+using namespace pp;
+
+namespace {
+
+thread_local std::string g_err;
+
+void set_err(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+}
+
+#define PP_CUDA(call)                                                                           \
+  do {                                                                                          \
+    cudaError_t e_ = (call);                                                                    \
+    if (e_ != cudaSuccess) {                                                                    \
+      set_err("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__);      \
+      return e_ == cudaErrorMemoryAllocation ? PP_ERR_OOM : PP_ERR_CUDA;                        \
+    }                                                                                           \
+  } while (0)
+
+#define PP_TRY(expr)         \
+  do {                       \
+    int rc_ = (expr);        \
+    if (rc_ != PP_OK) return rc_; \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Byte offsets of one layer's tensors in its packed block (identical on the
+// host, in the resident device copy and in every ring slot).
+struct LayerLayout {
+  size_t wqkv, wo, wgu, wd, sqkv, so, sgu, sd, attn_norm, ffn_norm, bytes;
+  size_t weight_bytes;  // int8 weights + f32 scales (what the GEMMs read)
+};
+
+LayerLayout make_layout(const pp_config& c) {
+  const size_t D = c.dim, QD = (size_t)c.n_heads * c.head_dim, QKV = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim,
+               F = c.ffn;
+  LayerLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.wqkv = take(QKV * D);
+  L.wo = take(D * QD);
+  L.wgu = take(2 * F * D);
+  L.wd = take(D * F);
+  L.sqkv = take(QKV * 4);
+  L.so = take(D * 4);
+  L.sgu = take(2 * F * 4);
+  L.sd = take(D * 4);
+  L.attn_norm = take(D * 4);
+  L.ffn_norm = take(D * 4);
+  L.bytes = off;
+  L.weight_bytes = (QKV * D + D * QD + 2 * F * D + D * F) + 4 * (QKV + D + 2 * F + D);
+  return L;
+}
+
+// Repack layer `l` of the caller's weights into `dst` (host memory):
+// wq|wk|wv rows fused into one QKV matrix; gate and up rows interleaved in
+// blocks of 16 (16 gate rows, then the same 16 up rows) so that one GEMM tile
+// holds both operands of SwiGLU.
+void pack_layer(const pp_config& c, const LayerLayout& lay, const pp_weights& w, int l, uint8_t* dst) {
+  const size_t D = c.dim, hd = c.head_dim, F = c.ffn;
+  const size_t qr = c.n_heads * hd, kr = c.n_kv_heads * hd;
+  const int8_t* const* W = w.w + 7 * l;
+  const float* const* S = w.w_scale + 7 * l;
+  uint8_t* p = dst + lay.wqkv;
+  memcpy(p, W[0], qr * D);
+  memcpy(p + qr * D, W[1], kr * D);
+  memcpy(p + (qr + kr) * D, W[2], kr * D);
+  float* s = reinterpret_cast<float*>(dst + lay.sqkv);
+  memcpy(s, S[0], qr * 4);
+  memcpy(s + qr, S[1], kr * 4);
+  memcpy(s + qr + kr, S[2], kr * 4);
+  memcpy(dst + lay.wo, W[3], D * qr);
+  memcpy(dst + lay.so, S[3], D * 4);
+  const size_t B = kSwiGluBlock;
+  int8_t* gu = reinterpret_cast<int8_t*>(dst + lay.wgu);
+  float* sgu = reinterpret_cast<float*>(dst + lay.sgu);
+  for (size_t b = 0; b < F / B; ++b) {
+    memcpy(gu + (2 * b) * B * D, W[4] + b * B * D, B * D);
+    memcpy(gu + (2 * b + 1) * B * D, W[5] + b * B * D, B * D);
+    memcpy(sgu + 2 * b * B, S[4] + b * B, B * 4);
+    memcpy(sgu + (2 * b + 1) * B, S[5] + b * B, B * 4);
+  }
+  memcpy(dst + lay.wd, W[6], D * F);
+  memcpy(dst + lay.sd, S[6], D * 4);
+  memcpy(dst + lay.attn_norm, w.attn_norm[l], D * 4);
+  memcpy(dst + lay.ffn_norm, w.ffn_norm[l], D * 4);
+}
+
+struct LayerPtrs {
+  const int8_t *wqkv, *wo, *wgu, *wd;
+  const float *sqkv, *so, *sgu, *sd, *attn_norm, *ffn_norm;
+};
+
+LayerPtrs layer_ptrs(const LayerLayout& lay, const uint8_t* base) {
+  LayerPtrs p;
+  p.wqkv = reinterpret_cast<const int8_t*>(base + lay.wqkv);
+  p.wo = reinterpret_cast<const int8_t*>(base + lay.wo);
+  p.wgu = reinterpret_cast<const int8_t*>(base + lay.wgu);
+  p.wd = reinterpret_cast<const int8_t*>(base + lay.wd);
+  p.sqkv = reinterpret_cast<const float*>(base + lay.sqkv);
+  p.so = reinterpret_cast<const float*>(base + lay.so);
+  p.sgu = reinterpret_cast<const float*>(base + lay.sgu);
+  p.sd = reinterpret_cast<const float*>(base + lay.sd);
+  p.attn_norm = reinterpret_cast<const float*>(base + lay.attn_norm);
+  p.ffn_norm = reinterpret_cast<const float*>(base + lay.ffn_norm);
+  return p;
+}
+
+struct EventPair {
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct pp_model {
+  pp_config cfg{};
+  int device = 0;
+  int engine = PP_GEMM_MMA;
+  LayerLayout lay{};
+  cudaStream_t stream = nullptr;       // compute stream (owned)
+  cudaStream_t copy_stream = nullptr;  // streamed mode: layer copies
+  // weights
+  uint8_t* d_layers = nullptr;  // resident: n_layers packed blocks
+  uint8_t* h_layers = nullptr;  // streamed: pinned host packed blocks
+  uint8_t* ring[2] = {nullptr, nullptr};
+  cudaEvent_t ring_ready[2] = {nullptr, nullptr};
+  cudaEvent_t ring_free[2] = {nullptr, nullptr};
+  float* emb = nullptr;
+  float* final_norm = nullptr;
+  int8_t* w_out = nullptr;
+  float* s_out = nullptr;
+  float* rope = nullptr;
+  float* kc = nullptr;
+  float* vc = nullptr;
+  // scratch
+  float *x = nullptr, *qkv = nullptr, *qr = nullptr, *o = nullptr, *h = nullptr, *as = nullptr, *logits = nullptr;
+  int8_t* a8 = nullptr;
+  __half* a16 = nullptr;
+  int32_t* tok = nullptr;
+  int* status = nullptr;
+  // stats and timing
+  pp_stats stats{};
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<EventPair> prof_pending;                 // profiled kernel launches
+  std::vector<EventPair> prefetch_pending;             // (copy_done, needed) per layer visit
+  std::vector<void*> allocations;
+};
+
+namespace {
+
+int ev_get(pp_model* m, cudaEvent_t* e) {
+  if (!m->ev_pool.empty()) {
+    *e = m->ev_pool.back();
+    m->ev_pool.pop_back();
+    return PP_OK;
+  }
+  PP_CUDA(cudaEventCreate(e));
+  return PP_OK;
+}
+
+// Fold finished event pairs into the statistics (the stream must be idle).
+int collect(pp_model* m) {
+  for (auto& p : m->prof_pending) {
+    float ms = 0.f;
+    PP_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
+    m->stats.prof_ms += ms;
+    m->stats.prof_launches += 1;
+    m->ev_pool.push_back(p.a);
+    m->ev_pool.push_back(p.b);
+  }
+  m->prof_pending.clear();
+  for (auto& p : m->prefetch_pending) {
+    float ms = 0.f;  // time from the copy's completion to the moment compute needed it
+    PP_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
+    if (ms >= 0.f)
+      m->stats.prefetch_hits += 1;
+    else
+      m->stats.prefetch_misses += 1;
+    m->ev_pool.push_back(p.a);
+    m->ev_pool.push_back(p.b);
+  }
+  m->prefetch_pending.clear();
+  return PP_OK;
+}
+
+template <class F>
+int launch(pp_model* m, int cls, cudaStream_t st, F&& fn) {
+  const bool prof = m->cfg.profile_kernel == cls;
+  EventPair p{};
+  if (prof) {
+    PP_TRY(ev_get(m, &p.a));
+    PP_TRY(ev_get(m, &p.b));
+    PP_CUDA(cudaEventRecord(p.a, st));
+  }
+  cudaError_t e = fn();
+  if (e != cudaSuccess) {
+    set_err("kernel launch (class %d) failed: %s", cls, cudaGetErrorString(e));
+    return PP_ERR_CUDA;
+  }
+  m->stats.kernel_launches += 1;
+  if (prof) {
+    PP_CUDA(cudaEventRecord(p.b, st));
+    m->prof_pending.push_back(p);
+  }
+  return PP_OK;
+}
+
+int gemm(pp_model* m, cudaStream_t st, int epi, const float* ws, const int8_t* w, int M, int N, int K, float* out,
+         int ldo) {
+  return launch(m, PP_KERNEL_GEMM, st, [&] {
+    return launch_gemm_mma(epi, m->a8, w, ws, m->as, M, N, K, out, ldo, nullptr, st);
+  });
+}
+
+template <class T>
+int dalloc(pp_model* m, T** p, size_t n) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, std::max<size_t>(n * sizeof(T), 256));
+  if (e != cudaSuccess) {
+    set_err("cudaMalloc(%zu) failed: %s", n * sizeof(T), cudaGetErrorString(e));
+    return e == cudaErrorMemoryAllocation ? PP_ERR_OOM : PP_ERR_CUDA;
+  }
+  m->allocations.push_back(v);
+  *p = static_cast<T*>(v);
+  return PP_OK;
+}
+
+int validate_cfg(const pp_config* c) {
+  if (!c) return PP_ERR_ARG;
+  const bool ok = c->dim > 0 && c->dim % 64 == 0 && c->n_layers > 0 && c->n_heads > 0 && c->n_kv_heads > 0 &&
+                  c->n_heads % c->n_kv_heads == 0 && (c->head_dim == 64 || c->head_dim == 128) &&
+                  64 % (c->n_heads / c->n_kv_heads) == 0 && (c->n_heads * c->head_dim) % 64 == 0 && c->ffn > 0 &&
+                  c->ffn % 64 == 0 && c->vocab > 0 && c->max_seq > 0 && c->max_chunk > 0 &&
+                  (c->mode == PP_MODE_RESIDENT || c->mode == PP_MODE_STREAMED) &&
+                  (c->mode == PP_MODE_RESIDENT || c->ring_slots == 1 || c->ring_slots == 2) && c->rms_eps >= 0.f &&
+                  c->rope_theta > 0.f && c->profile_kernel >= PP_KERNEL_NONE && c->profile_kernel < PP_KERNEL_COUNT;
+  if (!ok) {
+    set_err("invalid pp_config (dim%%64, head_dim in {64,128}, 64 %% (H/Hkv), ffn%%64, sizes > 0, mode, ring_slots)");
+    return PP_ERR_ARG;
+  }
+  return PP_OK;
+}
+
+int load_impl(pp_model* m, const pp_weights* w) {
+  const pp_config& c = m->cfg;
+  PP_CUDA(cudaGetDevice(&m->device));
+  m->engine = (c.gemm_engine == PP_GEMM_AUTO || c.gemm_engine == PP_GEMM_MMA) ? PP_GEMM_MMA : -1;
+  if (m->engine < 0) {
+    set_err("gemm_engine %d is not available in this build", c.gemm_engine);
+    return PP_ERR_UNSUPPORTED;
+  }
+  PP_CUDA(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
+  m->lay = make_layout(c);
+  const size_t D = c.dim, V = c.vocab, QD = (size_t)c.n_heads * c.head_dim,
+               QKV = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn, MC = c.max_chunk;
+  const size_t KVE = (size_t)c.n_layers * c.max_seq * c.n_kv_heads * c.head_dim;
+
+  // global tensors
+  PP_TRY(dalloc(m, &m->emb, V * D));
+  PP_TRY(dalloc(m, &m->final_norm, D));
+  PP_TRY(dalloc(m, &m->w_out, V * D));
+  PP_TRY(dalloc(m, &m->s_out, V));
+  PP_TRY(dalloc(m, &m->rope, (size_t)c.max_seq * c.head_dim));
+  PP_TRY(dalloc(m, &m->kc, KVE));
+  PP_TRY(dalloc(m, &m->vc, KVE));
+  PP_CUDA(cudaMemcpy(m->emb, w->tok_emb, V * D * 4, cudaMemcpyHostToDevice));
+  PP_CUDA(cudaMemcpy(m->final_norm, w->final_norm, D * 4, cudaMemcpyHostToDevice));
+  PP_CUDA(cudaMemcpy(m->w_out, w->w_out, V * D, cudaMemcpyHostToDevice));
+  PP_CUDA(cudaMemcpy(m->s_out, w->w_out_scale, V * 4, cudaMemcpyHostToDevice));
+  PP_CUDA(cudaMemsetAsync(m->kc, 0, KVE * 4, m->stream));
+  PP_CUDA(cudaMemsetAsync(m->vc, 0, KVE * 4, m->stream));
+  PP_CUDA(launch_rope_table(c.max_seq, c.head_dim, c.rope_theta, m->rope, m->stream));
+
+  // scratch
+  const size_t KMAX = std::max(std::max(D, QD), F);
+  PP_TRY(dalloc(m, &m->x, MC * D));
+  PP_TRY(dalloc(m, &m->qkv, MC * QKV));
+  PP_TRY(dalloc(m, &m->qr, MC * QD));
+  PP_TRY(dalloc(m, &m->o, MC * QD));
+  PP_TRY(dalloc(m, &m->h, MC * F));
+  PP_TRY(dalloc(m, &m->a8, MC * KMAX));
+  PP_TRY(dalloc(m, &m->a16, MC * KMAX));
+  PP_TRY(dalloc(m, &m->as, MC));
+  PP_TRY(dalloc(m, &m->logits, V));
+  PP_TRY(dalloc(m, &m->tok, (size_t)c.max_seq));
+  PP_TRY(dalloc(m, &m->status, 1));
+  PP_CUDA(cudaMemsetAsync(m->status, 0, sizeof(int), m->stream));
+
+  // layers
+  const size_t stride = m->lay.bytes;
+  if (c.mode == PP_MODE_RESIDENT) {
+    PP_TRY(dalloc(m, &m->d_layers, stride * c.n_layers));
+    uint8_t* stage = nullptr;
+    PP_CUDA(cudaMallocHost(&stage, stride));
+    for (int l = 0; l < c.n_layers; ++l) {
+      pack_layer(c, m->lay, *w, l, stage);
+      cudaError_t e = cudaMemcpy(m->d_layers + stride * l, stage, stride, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        cudaFreeHost(stage);
+        set_err("layer upload failed: %s", cudaGetErrorString(e));
+        return PP_ERR_CUDA;
+      }
+    }
+    cudaFreeHost(stage);
+  } else {
+    cudaError_t e = cudaHostAlloc(&m->h_layers, stride * c.n_layers, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      m->h_layers = nullptr;
+      set_err("cudaHostAlloc(%zu) failed: %s", stride * c.n_layers, cudaGetErrorString(e));
+      return PP_ERR_OOM;
+    }
+    for (int l = 0; l < c.n_layers; ++l) pack_layer(c, m->lay, *w, l, m->h_layers + stride * l);
+    PP_CUDA(cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking));
+    for (int s = 0; s < c.ring_slots; ++s) {
+      PP_TRY(dalloc(m, &m->ring[s], stride));
+      PP_CUDA(cudaEventCreateWithFlags(&m->ring_ready[s], cudaEventDisableTiming));
+      PP_CUDA(cudaEventCreateWithFlags(&m->ring_free[s], cudaEventDisableTiming));
+      PP_CUDA(cudaEventRecord(m->ring_free[s], m->stream));
+    }
+  }
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  return PP_OK;
+}
+
+void free_impl(pp_model* m) {
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  if (m->copy_stream) cudaStreamSynchronize(m->copy_stream);
+  for (auto& p : m->prof_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  for (auto& p : m->prefetch_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  for (auto e : m->ev_pool) cudaEventDestroy(e);
+  for (int s = 0; s < 2; ++s) {
+    if (m->ring_ready[s]) cudaEventDestroy(m->ring_ready[s]);
+    if (m->ring_free[s]) cudaEventDestroy(m->ring_free[s]);
+  }
+  for (void* p : m->allocations) cudaFree(p);
+  if (m->h_layers) cudaFreeHost(m->h_layers);
+  if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
+  if (m->stream) cudaStreamDestroy(m->stream);
+  delete m;
+}
+
+int check_prefill_args(pp_model* m, int n, int start_pos, int chunk) {
+  if (!m) { set_err("null model"); return PP_ERR_ARG; }
+  if (n <= 0 || chunk <= 0 || start_pos < 0 || chunk > m->cfg.max_chunk) {
+    set_err("bad prefill arguments: n=%d start_pos=%d chunk=%d (max_chunk %d)", n, start_pos, chunk, m->cfg.max_chunk);
+    return PP_ERR_ARG;
+  }
+  if ((int64_t)start_pos + n > m->cfg.max_seq) {
+    set_err("start_pos + n = %lld exceeds max_seq %d", (long long)start_pos + n, m->cfg.max_seq);
+    return PP_ERR_CAPACITY;
+  }
+  return PP_OK;
+}
+
+// Streamed mode, before layer visit `v` of this call: make sure the copy of
+// visit v is issued, issue the prefetch of visit v+1 into the other slot when
+// the ring has two slots ("Predictive prefetch": the worker materialises block
+// L+1 while block L computes), and make the compute stream wait for slot v.
+int stream_layer(pp_model* m, cudaStream_t st, int v, int n_visits, const uint8_t** base) {
+  const pp_config& c = m->cfg;
+  const int S = c.ring_slots;
+  const size_t stride = m->lay.bytes;
+  auto issue_copy = [&](int visit) -> int {
+    const int slot = visit % S;
+    const int layer = visit % c.n_layers;
+    PP_CUDA(cudaStreamWaitEvent(m->copy_stream, m->ring_free[slot], 0));
+    PP_CUDA(cudaMemcpyAsync(m->ring[slot], m->h_layers + stride * layer, stride, cudaMemcpyHostToDevice,
+                            m->copy_stream));
+    PP_CUDA(cudaEventRecord(m->ring_ready[slot], m->copy_stream));
+    m->stats.h2d_bytes += (int64_t)stride;
+    return PP_OK;
+  };
+  EventPair hp{};
+  PP_TRY(ev_get(m, &hp.a));
+  PP_TRY(ev_get(m, &hp.b));
+  if (v == 0 || S == 1) PP_TRY(issue_copy(v));
+  // The copy of visit v is now the newest work on the copy stream (with two
+  // slots it was issued at visit v-1 and the copy of v+1 is issued below).
+  PP_CUDA(cudaEventRecord(hp.a, m->copy_stream));  // copy of visit v done
+  PP_CUDA(cudaEventRecord(hp.b, st));              // the compute stream reached layer v
+  const int slot = v % S;
+  PP_CUDA(cudaStreamWaitEvent(st, m->ring_ready[slot], 0));
+  if (S == 2 && v + 1 < n_visits) PP_TRY(issue_copy(v + 1));
+  m->prefetch_pending.push_back(hp);
+  *base = m->ring[slot];
+  return PP_OK;
+}
+
+int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
+                 cudaStream_t st) {
+  const pp_config& c = m->cfg;
+  const int D = c.dim, H = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim, F = c.ffn;
+  const int QD = H * hd, QKV = (H + 2 * Hkv) * hd;
+  const size_t kvl = (size_t)c.max_seq * Hkv * hd;
+  const int n_chunks = (n + chunk - 1) / chunk;
+  const int n_visits = n_chunks * c.n_layers;
+  int visit = 0;
+  if (c.mode == PP_MODE_STREAMED && st != m->stream) {
+    // keep the ring's events on one compute stream
+    cudaEvent_t e;
+    PP_TRY(ev_get(m, &e));
+    PP_CUDA(cudaEventRecord(e, st));
+    PP_CUDA(cudaStreamWaitEvent(m->stream, e, 0));
+    m->ev_pool.push_back(e);
+  }
+  cudaStream_t cs = c.mode == PP_MODE_STREAMED ? m->stream : st;
+  for (int c0 = 0; c0 < n; c0 += chunk) {
+    const int C = std::min(chunk, n - c0);
+    const int pos0 = start_pos + c0;
+    PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, cs); }));
+    for (int l = 0; l < c.n_layers; ++l, ++visit) {
+      const uint8_t* base;
+      if (c.mode == PP_MODE_STREAMED) {
+        PP_TRY(stream_layer(m, cs, visit, n_visits, &base));
+      } else {
+        base = m->d_layers + m->lay.bytes * l;
+      }
+      const LayerPtrs L = layer_ptrs(m->lay, base);
+      float* kcl = m->kc + kvl * l;
+      float* vcl = m->vc + kvl * l;
+      // attention block
+      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+        return launch_norm_quant(m->x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, nullptr, m->as, cs);
+      }));
+      PP_TRY(gemm(m, cs, EPI_STORE, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
+      PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
+        return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
+      }));
+      PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
+        return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, cs);
+      }));
+      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+        return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, nullptr, m->as, cs);
+      }));
+      PP_TRY(gemm(m, cs, EPI_RESID, L.so, L.wo, C, D, QD, m->x, D));
+      // FFN block
+      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+        return launch_norm_quant(m->x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, nullptr, m->as, cs);
+      }));
+      PP_TRY(gemm(m, cs, EPI_SWIGLU, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
+      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+        return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, nullptr, m->as, cs);
+      }));
+      PP_TRY(gemm(m, cs, EPI_RESID, L.sd, L.wd, C, D, F, m->x, D));
+      if (c.mode == PP_MODE_STREAMED) PP_CUDA(cudaEventRecord(m->ring_free[visit % c.ring_slots], cs));
+    }
+    if (c0 + C == n) {
+      // last position only: final RMSNorm -> quantise -> output projection
+      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+        return launch_norm_quant(m->x + (size_t)(C - 1) * D, D, m->final_norm, 1, D, c.rms_eps, nullptr, m->a8,
+                                 nullptr, m->as, cs);
+      }));
+      PP_TRY(launch(m, PP_KERNEL_LM_HEAD, cs, [&] {
+        return launch_lm_head(m->a8, m->as, m->w_out, m->s_out, c.vocab, D, d_logits, cs);
+      }));
+    }
+  }
+  if (c.mode == PP_MODE_STREAMED && st != m->stream) {
+    cudaEvent_t e;
+    PP_TRY(ev_get(m, &e));
+    PP_CUDA(cudaEventRecord(e, m->stream));
+    PP_CUDA(cudaStreamWaitEvent(st, e, 0));
+    m->ev_pool.push_back(e);
+  }
+  m->stats.calls += 1;
+  m->stats.chunks += n_chunks;
+  m->stats.tokens += n;
+  m->stats.weight_bytes_read += (int64_t)m->lay.weight_bytes * c.n_layers * n_chunks + (int64_t)c.vocab * D +
+                                (int64_t)c.vocab * 4;
+  return PP_OK;
+}
+
+}  // namespace
+
+// =====================================================================  C ABI
+extern "C" {
+
+const char* pp_status_str(int s) {
+  switch (s) {
+    case PP_OK: return "ok";
+    case PP_ERR_ARG: return "invalid argument";
+    case PP_ERR_CAPACITY: return "KV capacity exceeded";
+    case PP_ERR_OOM: return "out of memory";
+    case PP_ERR_CUDA: return "CUDA error";
+    case PP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case PP_ERR_UNSUPPORTED: return "unsupported";
+    default: return "unknown status";
+  }
+}
+
+const char* pp_last_error(void) { return g_err.c_str(); }
+
+int pp_model_load(const pp_config* cfg, const pp_weights* w, pp_model** out) {
+  if (!out) { set_err("null out"); return PP_ERR_ARG; }
+  *out = nullptr;
+  PP_TRY(validate_cfg(cfg));
+  if (!w || !w->tok_emb || !w->w || !w->w_scale || !w->attn_norm || !w->ffn_norm || !w->final_norm || !w->w_out ||
+      !w->w_out_scale) {
+    set_err("null weight pointer");
+    return PP_ERR_ARG;
+  }
+  for (int i = 0; i < 7 * cfg->n_layers; ++i)
+    if (!w->w[i] || !w->w_scale[i]) { set_err("null layer matrix %d", i); return PP_ERR_ARG; }
+  for (int l = 0; l < cfg->n_layers; ++l)
+    if (!w->attn_norm[l] || !w->ffn_norm[l]) { set_err("null norm gain %d", l); return PP_ERR_ARG; }
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess || ndev == 0) {
+    set_err("no CUDA device: %s", cudaGetErrorString(e));
+    return PP_ERR_CUDA;
+  }
+  pp_model* m = new pp_model();
+  m->cfg = *cfg;
+  int rc = load_impl(m, w);
+  if (rc != PP_OK) {
+    std::string keep = g_err;
+    free_impl(m);
+    g_err = keep;
+    return rc;
+  }
+  *out = m;
+  return PP_OK;
+}
+
+void pp_model_free(pp_model* m) {
+  if (m) free_impl(m);
+}
+
+int pp_prefill_device(pp_model* m, const int32_t* d_tokens, int32_t n, int32_t start_pos, int32_t chunk,
+                      float* d_logits, void* stream) {
+  PP_TRY(check_prefill_args(m, n, start_pos, chunk));
+  if (!d_tokens || !d_logits) { set_err("null device pointer"); return PP_ERR_ARG; }
+  cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : m->stream;
+  return prefill_impl(m, d_tokens, n, start_pos, chunk, d_logits, st);
+}
+
+int pp_prefill(pp_model* m, const int32_t* tokens, int32_t n, int32_t start_pos, int32_t chunk, float* logits_out) {
+  PP_TRY(check_prefill_args(m, n, start_pos, chunk));
+  if (!tokens || !logits_out) { set_err("null host pointer"); return PP_ERR_ARG; }
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= m->cfg.vocab) {
+      set_err("token %d at index %d outside [0, %d)", tokens[i], i, m->cfg.vocab);
+      return PP_ERR_ARG;
+    }
+  PP_CUDA(cudaMemcpyAsync(m->tok, tokens, sizeof(int32_t) * n, cudaMemcpyHostToDevice, m->stream));
+  m->stats.h2d_bytes += (int64_t)sizeof(int32_t) * n;
+  PP_TRY(prefill_impl(m, m->tok, n, start_pos, chunk, m->logits, m->stream));
+  PP_CUDA(cudaMemcpyAsync(logits_out, m->logits, sizeof(float) * m->cfg.vocab, cudaMemcpyDeviceToHost, m->stream));
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  PP_TRY(collect(m));
+  return pp_device_status(m);
+}
+
+int pp_forward_one(pp_model* m, int32_t token, int32_t pos, float* logits_out) {
+  return pp_prefill(m, &token, 1, pos, 1, logits_out);
+}
+
+int pp_device_status(pp_model* m) {
+  if (!m) return PP_ERR_ARG;
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  int s = 0;
+  PP_CUDA(cudaMemcpy(&s, m->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (s != DEV_OK) PP_CUDA(cudaMemset(m->status, 0, sizeof(int)));
+  if (s == DEV_BAD_TOKEN) { set_err("a token id outside [0, vocab) reached the device"); return PP_ERR_ARG; }
+  if (s == DEV_TIMEOUT) { set_err("a bounded device wait gave up"); return PP_ERR_DEVICE_TIMEOUT; }
+  return PP_OK;
+}
+
+int pp_kv_reset(pp_model* m) {
+  if (!m) return PP_ERR_ARG;
+  const pp_config& c = m->cfg;
+  const size_t KVE = (size_t)c.n_layers * c.max_seq * c.n_kv_heads * c.head_dim;
+  PP_CUDA(cudaMemsetAsync(m->kc, 0, KVE * 4, m->stream));
+  PP_CUDA(cudaMemsetAsync(m->vc, 0, KVE * 4, m->stream));
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  return PP_OK;
+}
+
+int pp_kv_read(pp_model* m, int32_t layer, int32_t which, int32_t pos0, int32_t n_pos, float* out) {
+  if (!m || !out || layer < 0 || layer >= m->cfg.n_layers || (which != 0 && which != 1) || pos0 < 0 || n_pos <= 0 ||
+      (int64_t)pos0 + n_pos > m->cfg.max_seq) {
+    set_err("bad pp_kv_read arguments");
+    return PP_ERR_ARG;
+  }
+  const pp_config& c = m->cfg;
+  const size_t row = (size_t)c.n_kv_heads * c.head_dim;
+  const float* src = (which ? m->vc : m->kc) + (size_t)layer * c.max_seq * row + (size_t)pos0 * row;
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  PP_CUDA(cudaMemcpy(out, src, sizeof(float) * row * n_pos, cudaMemcpyDeviceToHost));
+  return PP_OK;
+}
+
+int pp_get_stats(const pp_model* cm, pp_stats* out) {
+  if (!cm || !out) return PP_ERR_ARG;
+  pp_model* m = const_cast<pp_model*>(cm);
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  PP_TRY(collect(m));
+  *out = m->stats;
+  return PP_OK;
+}
+
+int pp_reset_stats(pp_model* m) {
+  if (!m) return PP_ERR_ARG;
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  PP_TRY(collect(m));
+  m->stats = pp_stats{};
+  return PP_OK;
+}
+
+int pp_model_gemm_engine(const pp_model* m) { return m ? m->engine : PP_ERR_ARG; }
+
+int pp_set_profile_kernel(pp_model* m, int32_t kernel_class) {
+  if (!m || kernel_class < PP_KERNEL_NONE || kernel_class >= PP_KERNEL_COUNT) {
+    set_err("bad pp_set_profile_kernel arguments");
+    return PP_ERR_ARG;
+  }
+  m->cfg.profile_kernel = kernel_class;
+  return PP_OK;
+}
+
+// ---------------------------------------------------------------- single steps
+static int ok_launch(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    set_err("%s: %s", what, cudaGetErrorString(e));
+    return PP_ERR_CUDA;
+  }
+  return PP_OK;
+}
+
+int pp_op_quantize(const float* x, int32_t rows, int32_t k, int8_t* q8, uint16_t* q16, float* a_scale, void* stream) {
+  if (!x || !q8 || !a_scale || rows <= 0 || k <= 0 || k % 4) { set_err("bad pp_op_quantize arguments"); return PP_ERR_ARG; }
+  return ok_launch(launch_norm_quant(x, k, nullptr, rows, k, 0.f, nullptr, q8, reinterpret_cast<__half*>(q16), a_scale,
+                                     static_cast<cudaStream_t>(stream)),
+                   "quantize");
+}
+
+int pp_op_rmsnorm_quantize(const float* x, const float* g, int32_t rows, int32_t k, float eps, float* y_out, int8_t* q8,
+                           uint16_t* q16, float* a_scale, void* stream) {
+  if (!x || !g || !q8 || !a_scale || rows <= 0 || k <= 0 || k % 4 || eps < 0.f) {
+    set_err("bad pp_op_rmsnorm_quantize arguments");
+    return PP_ERR_ARG;
+  }
+  return ok_launch(launch_norm_quant(x, k, g, rows, k, eps, y_out, q8, reinterpret_cast<__half*>(q16), a_scale,
+                                     static_cast<cudaStream_t>(stream)),
+                   "rmsnorm_quantize");
+}
+
+static int check_gemm(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
+                      int32_t k) {
+  if (!w || m <= 0 || n <= 0 || k <= 0 || k % 64 || n % 32) {
+    set_err("bad GEMM shape m=%d n=%d k=%d (k%%64, n%%32)", m, n, k);
+    return PP_ERR_ARG;
+  }
+  if (engine == PP_GEMM_MMA || engine == PP_GEMM_AUTO) {
+    if (!a8) { set_err("engine needs the int8 activations"); return PP_ERR_ARG; }
+    return PP_OK;
+  }
+  (void)a16;
+  set_err("gemm engine %d is not available in this build", engine);
+  return PP_ERR_UNSUPPORTED;
+}
+
+int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
+                   int32_t k, int32_t* acc, void* stream) {
+  PP_TRY(check_gemm(engine, a8, a16, w, m, n, k));
+  if (!acc) { set_err("null acc"); return PP_ERR_ARG; }
+  return ok_launch(launch_gemm_mma(EPI_ACC, a8, w, nullptr, nullptr, m, n, k, nullptr, 0, acc,
+                                   static_cast<cudaStream_t>(stream)),
+                   "gemm_acc");
+}
+
+int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_t* a16, const int8_t* w,
+               const float* w_scale, const float* a_scale, int32_t m, int32_t n, int32_t k, float* out, int32_t ldo,
+               void* stream) {
+  PP_TRY(check_gemm(engine, a8, a16, w, m, n, k));
+  const int out_cols = epilogue == PP_EPI_SWIGLU ? n / 2 : n;
+  if (!w_scale || !a_scale || !out || ldo < out_cols || (epilogue < PP_EPI_STORE || epilogue > PP_EPI_SWIGLU) ||
+      ldo % 2) {
+    set_err("bad pp_op_gemm arguments");
+    return PP_ERR_ARG;
+  }
+  return ok_launch(launch_gemm_mma(epilogue, a8, w, w_scale, a_scale, m, n, k, out, ldo, nullptr,
+                                   static_cast<cudaStream_t>(stream)),
+                   "gemm");
+}
+
+int pp_op_rope_table(int32_t max_pos, int32_t head_dim, float theta, float* rope_table, void* stream) {
+  if (max_pos <= 0 || head_dim <= 0 || head_dim % 2 || theta <= 0.f || !rope_table) {
+    set_err("bad pp_op_rope_table arguments");
+    return PP_ERR_ARG;
+  }
+  return ok_launch(launch_rope_table(max_pos, head_dim, theta, rope_table, static_cast<cudaStream_t>(stream)),
+                   "rope_table");
+}
+
+int pp_op_rope_kv(const float* qkv, int32_t rows, int32_t start_pos, int32_t n_heads, int32_t n_kv_heads,
+                  int32_t head_dim, const float* rope_table, float* q_out, float* k_cache, float* v_cache,
+                  void* stream) {
+  if (!qkv || !rope_table || !q_out || !k_cache || !v_cache || rows <= 0 || start_pos < 0 || n_heads <= 0 ||
+      n_kv_heads <= 0 || head_dim <= 0 || head_dim % 2) {
+    set_err("bad pp_op_rope_kv arguments");
+    return PP_ERR_ARG;
+  }
+  return ok_launch(launch_rope_kv(qkv, rows, start_pos, n_heads, n_kv_heads, head_dim, rope_table, q_out, k_cache,
+                                  v_cache, static_cast<cudaStream_t>(stream)),
+                   "rope_kv");
+}
+
+int pp_op_attention(const float* q, const float* k_cache, const float* v_cache, int32_t rows, int32_t start_pos,
+                    int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float* o, void* stream) {
+  if (!q || !k_cache || !v_cache || !o || rows <= 0 || start_pos < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+      n_heads % n_kv_heads || 64 % (n_heads / n_kv_heads) || (head_dim != 64 && head_dim != 128)) {
+    set_err("bad pp_op_attention arguments");
+    return PP_ERR_ARG;
+  }
+  return ok_launch(launch_attention(q, k_cache, v_cache, rows, start_pos, n_heads, n_kv_heads, head_dim, o,
+                                    static_cast<cudaStream_t>(stream)),
+                   "attention");
+}
+
+int pp_op_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w_out, const float* w_scale, int32_t vocab,
+                  int32_t dim, float* logits, void* stream) {
+  if (!q8 || !a_scale || !w_out || !w_scale || !logits || vocab <= 0 || dim <= 0 || dim % 16 ||
+      (reinterpret_cast<uintptr_t>(q8) & 15) || (reinterpret_cast<uintptr_t>(w_out) & 15)) {
+    set_err("bad pp_op_lm_head arguments (dim%%16, 16-byte aligned int8 buffers)");
+    return PP_ERR_ARG;
+  }
+  return ok_launch(launch_lm_head(q8, a_scale, w_out, w_scale, vocab, dim, logits, static_cast<cudaStream_t>(stream)),
+                   "lm_head");
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pp.h"
+
+namespace pp {
+
+// Epilogue selector of the GEMM kernels (PP_EPI_* plus the raw int32 form).
+enum Epi : int { EPI_STORE = PP_EPI_STORE, EPI_RESID = PP_EPI_RESID, EPI_SWIGLU = PP_EPI_SWIGLU, EPI_ACC = 3 };
+
+// Device status word values (written by kernels, read by pp_device_status).
+enum : int { DEV_OK = 0, DEV_BAD_TOKEN = 1, DEV_TIMEOUT = 2 };
+
+// ---- elementwise / row kernels (k_rows.cu)
+cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab, int dim, float* x, int* status,
+                         cudaStream_t s);
+cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
+                              int8_t* q8, __half* q16, float* a_scale, cudaStream_t s);
+cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s);
+cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
+                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s);
+cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,
+                           int dim, float* logits, cudaStream_t s);
+
+// ---- GEMMs
+// mma.sync engine (k_gemm_mma.cu): a8 [m][k] int8, w [n][k] int8.
+cudaError_t launch_gemm_mma(int epi, const int8_t* a8, const int8_t* w, const float* ws, const float* as, int m,
+                            int n, int k, float* out, int ldo, int32_t* acc, cudaStream_t s);
+
+// ---- attention (k_attention.cu)
+cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,
+                             int Hkv, int hd, float* o, cudaStream_t s);
+
+// Rows of the interleaved gate/up matrix: blocks of 16 gate rows then 16 up rows.
+constexpr int kSwiGluBlock = 16;
+
+}  // namespace pp
+
+// ---------------------------------------------------------------- PTX helpers
+namespace ppdev {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared copy; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+// D = A(16x32 s8, row) * B(32x8 s8, col) + D, int32 accumulate (exact).
+__device__ __forceinline__ void mma_s8_16832(int32_t (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// The dequantising epilogue in its fixed order: (float(acc) * w_scale) * a_scale,
+// each product rounded to nearest (no contraction).
+__device__ __forceinline__ float dequant(int32_t acc, float ws, float as) {
+  return __fmul_rn(__fmul_rn(__int2float_rn(acc), ws), as);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+}  // namespace ppdev

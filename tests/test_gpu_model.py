@@ -1,0 +1,216 @@
+"""End-to-end parity of the GPU prefill with the oracle, and the invariants
+the pages state, through the C ABI.
+
+Criteria: final-position logits within 1e-2 x std(oracle logits) and the
+same top-1 token; the GPU's chunked path bit-identical to its own chunk = 1
+path ("Batched Prefill", "Correctness": byte-identical output); continuation
+and causality bit-identical ("Single-pass prefill": per-position results do
+not change).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import prompt_prefill_gb300 as pp
+import synth
+from tests.gpu_util import bits, load, logits_close, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    torch_cuda()
+    m = synth.make_model(synth.CONFIGS["tiny"])
+    g = load(m, max_seq=64, max_chunk=64)
+    yield m, g
+    g.close()
+
+
+def _assert_e2e(gpu, ref, label=""):
+    ok, rel, top_ok, gap = logits_close(gpu, ref)
+    assert ok, f"{label}: max|d| = {rel:.3g} x std"
+    if gap > 1e-2:  # top-1 is well conditioned
+        assert top_ok, f"{label}: top-1 differs (oracle top-2 gap {gap:.3g} x std)"
+
+
+def test_tiny_matches_oracle(tiny):
+    m, g = tiny
+    toks = synth.prompt(m.cfg)
+    g.kv_reset()
+    got = g.prefill(toks, 0, 8)
+    ref = oracle.OracleModel(m).prefill(toks, 0, 8)
+    _assert_e2e(got, ref, "tiny")
+
+
+def test_tiny_kv_cache_matches_oracle(tiny):
+    m, g = tiny
+    toks = synth.prompt(m.cfg)
+    g.kv_reset()
+    g.prefill(toks, 0, 8)
+    om = oracle.OracleModel(m)
+    om.prefill(toks, 0, 8)
+    for L in range(m.cfg.n_layers):
+        for which in (0, 1):
+            a = g.kv(L, which, 0, 32)
+            b = om.kv(L, which)[:32]
+            assert np.abs(a - b).max() <= 1e-2 * b.std(), (L, which)
+
+
+@pytest.mark.parametrize("chunk", [3, 8, 32, 64])
+def test_tiny_chunked_equals_per_token(tiny, chunk):
+    m, g = tiny
+    toks = synth.prompt(m.cfg)
+    g.kv_reset()
+    ref = g.prefill(toks, 0, 1)
+    kref = g.kv(3, 0, 0, 32)
+    g.kv_reset()
+    got = g.prefill(toks, 0, chunk)
+    assert np.array_equal(bits(got), bits(ref))
+    assert np.array_equal(bits(g.kv(3, 0, 0, 32)), bits(kref))
+
+
+def test_tiny_forward_one_loop(tiny):
+    m, g = tiny
+    toks = synth.prompt(m.cfg, 12)
+    g.kv_reset()
+    for i, t in enumerate(toks):
+        last = g.forward_one(int(t), i)
+    g.kv_reset()
+    assert np.array_equal(bits(last), bits(g.prefill(toks, 0, 5)))
+
+
+def test_tiny_continuation_and_causality(tiny):
+    m, g = tiny
+    toks = synth.prompt(m.cfg, 40)
+    g.kv_reset()
+    whole = g.prefill(toks, 0, 8)
+    k_whole = g.kv(2, 1, 0, 40)
+    g.kv_reset()
+    first = g.prefill(toks[:23], 0, 8)
+    k_first = g.kv(2, 1, 0, 23)
+    cont = g.prefill(toks[23:], 23, 8)
+    assert np.array_equal(bits(whole), bits(cont))
+    assert np.array_equal(bits(k_whole[:23]), bits(k_first))  # later tokens never touch earlier rows
+    g.kv_reset()
+    assert np.array_equal(bits(g.prefill(toks[:23], 0, 6)), bits(first))
+
+
+def test_tiny_max_capacity_and_ragged(tiny):
+    m, g = tiny
+    toks = synth.tokens(77, 64, m.cfg.vocab)
+    g.kv_reset()
+    got = g.prefill(toks, 0, 9)  # 64 = 7 x 9 + 1: ragged last chunk, exactly max_seq
+    ref = oracle.OracleModel(m).prefill(toks, 0, 9)
+    _assert_e2e(got, ref, "tiny max_seq")
+
+
+def test_stats_weight_bytes_once_per_chunk(tiny):
+    m, g = tiny
+    c = m.cfg
+    g.kv_reset()
+    g.reset_stats()
+    g.prefill(synth.prompt(c), 0, 8)  # 32 tokens -> 4 chunks
+    s = g.stats()
+    layer_w = c.layer_bytes() + 4 * (c.qkv_rows + c.dim + 2 * c.ffn + c.dim)
+    head = c.vocab * c.dim + 4 * c.vocab
+    assert s["chunks"] == 4 and s["tokens"] == 32 and s["calls"] == 1
+    assert s["weight_bytes_read"] == 4 * c.n_layers * layer_w + head
+    assert s["h2d_bytes"] == 32 * 4
+    g.reset_stats()
+    g.prefill(synth.prompt(c), 0, 1)  # per-token path reads the model once per token
+    assert g.stats()["weight_bytes_read"] == 32 * c.n_layers * layer_w + head
+
+
+def test_argument_errors(tiny):
+    m, g = tiny
+    V = m.cfg.vocab
+    assert pp.pp_prefill_rc(g.h, np.zeros(0, np.int32), 0, 8, V) == pp.PP_ERR_ARG
+    assert pp.pp_prefill_rc(g.h, np.ones(4, np.int32), 0, 0, V) == pp.PP_ERR_ARG
+    assert pp.pp_prefill_rc(g.h, np.ones(4, np.int32), 0, 65, V) == pp.PP_ERR_ARG  # chunk > max_chunk
+    assert pp.pp_prefill_rc(g.h, np.ones(4, np.int32), -1, 8, V) == pp.PP_ERR_ARG
+    assert pp.pp_prefill_rc(g.h, np.array([1, V], np.int32), 0, 8, V) == pp.PP_ERR_ARG
+    assert pp.pp_prefill_rc(g.h, np.ones(65, np.int32), 0, 8, V) == pp.PP_ERR_CAPACITY
+    assert pp.pp_prefill_rc(g.h, np.ones(2, np.int32), 63, 8, V) == pp.PP_ERR_CAPACITY
+
+
+def test_device_path_flags_bad_token(tiny):
+    torch = torch_cuda()
+    m, g = tiny
+    d_tok = torch.tensor([1, 2, m.cfg.vocab + 5], dtype=torch.int32, device="cuda")
+    d_logits = torch.empty(m.cfg.vocab, dtype=torch.float32, device="cuda")
+    g.kv_reset()
+    g.prefill_device(d_tok, 3, 0, 8, d_logits)
+    assert g.device_status() == pp.PP_ERR_ARG
+    assert g.device_status() == pp.PP_OK  # cleared after being read
+
+
+def test_device_path_equals_host_path(tiny):
+    torch = torch_cuda()
+    m, g = tiny
+    toks = synth.prompt(m.cfg)
+    g.kv_reset()
+    ref = g.prefill(toks, 0, 8)
+    g.kv_reset()
+    d_logits = torch.empty(m.cfg.vocab, dtype=torch.float32, device="cuda")
+    g.prefill_device(torch.from_numpy(toks).cuda(), len(toks), 0, 8, d_logits)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(d_logits.cpu().numpy()), bits(ref))
+
+
+# ------------------------------------------------------------------ 350M class
+def test_350m_matches_oracle():
+    torch_cuda()
+    c = synth.CONFIGS["350m"]
+    m = synth.make_model(c)
+    toks = synth.prompt(c)  # 747 tokens, chunk 32 -> 23 full chunks + 1 of 11
+    g = load(m, max_seq=c.max_seq, max_chunk=32)
+    got = g.prefill(toks, 0, 32)
+    s = g.stats()
+    g.close()
+    ref = oracle.OracleModel(m, max_seq=747).prefill(toks, 0, 32)
+    _assert_e2e(got, ref, "350m")
+    layer_w = c.layer_bytes() + 4 * (c.qkv_rows + c.dim + 2 * c.ffn + c.dim)
+    assert s["weight_bytes_read"] == 24 * c.n_layers * layer_w + c.vocab * c.dim + 4 * c.vocab
+
+
+# ------------------------------------------------------------------ 1B class
+@pytest.fixture(scope="module")
+def one_b():
+    torch_cuda()
+    c = synth.CONFIGS["1b"]
+    m = synth.make_model(c)
+    g = load(m, max_seq=4096, max_chunk=2048)
+    yield m, g
+    g.close()
+
+
+def test_1b_chunk_sweep_bit_identical(one_b):
+    m, g = one_b
+    toks = synth.prompt(m.cfg, 2048)
+    outs = {}
+    for chunk in (32, 128, 512, 2048):
+        g.kv_reset()
+        outs[chunk] = g.prefill(toks, 0, chunk)
+    for chunk in (128, 512, 2048):
+        assert np.array_equal(bits(outs[chunk]), bits(outs[32])), chunk
+
+
+def test_1b_second_call_continues_cache(one_b):
+    m, g = one_b
+    toks = synth.prompt(m.cfg, 4096)
+    g.kv_reset()
+    g.prefill(toks[:2048], 0, 512)
+    second = g.prefill(toks[2048:], 2048, 512)
+    g.kv_reset()
+    whole = g.prefill(toks, 0, 512)
+    assert np.array_equal(bits(second), bits(whole))
+
+
+def test_1b_prefix_and_continuation_match_oracle(one_b):
+    m, g = one_b
+    toks = synth.prompt(m.cfg, 96)
+    om = oracle.OracleModel(m, max_seq=96)
+    g.kv_reset()
+    _assert_e2e(g.prefill(toks[:64], 0, 32), om.prefill(toks[:64], 0, 32), "1b prefix")
+    _assert_e2e(g.prefill(toks[64:], 64, 32), om.prefill(toks[64:], 64, 32), "1b continuation")
