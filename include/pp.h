@@ -183,6 +183,15 @@ int pp_reset_stats(pp_model* m);
  * and summed duration appear in pp_stats (prof_launches, prof_ms). */
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
+/* Record the residual stream at every layer boundary: while set, each
+ * prefill call copies the rows of positions p (start_pos <= p < start_pos+n)
+ * entering layer l to d_trace[l][p][0..dim) and the rows leaving the last
+ * layer to d_trace[n_layers][p]. d_trace is a device buffer of
+ * (n_layers + 1) * max_pos * dim f32 owned by the caller, who keeps it alive
+ * while it is set; NULL switches tracing off. Calls whose positions exceed
+ * max_pos fail with PP_ERR_CAPACITY while tracing is on. */
+int pp_set_trace(pp_model* m, float* d_trace, int32_t max_pos);
+
 /* The GEMM engine the model resolved to (PP_GEMM_MMA or PP_GEMM_TC). */
 int pp_model_gemm_engine(const pp_model* m);
 
@@ -223,6 +232,12 @@ int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const 
 int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_t* a16, const int8_t* w,
                const float* w_scale, const float* a_scale, int32_t m, int32_t n, int32_t k, float* out,
                int32_t ldo, void* stream);
+
+/* K-extent of one exact f32 accumulation segment of the tcgen05 engine
+ * (process-wide; default and maximum 1024, multiple of 64). Partial sums of
+ * up to 1024 products of int8 values stay below 2^24 and are exact in f32;
+ * shorter segments only add drains. Errors: PP_ERR_ARG out of range. */
+int pp_set_exact_segment(int32_t seg_k);
 
 /* RoPE + K/V write for `rows` positions start_pos..: qkv [rows][(H+2Hkv)*hd]
  * f32 (q heads, then k heads, then v heads) -> q_out [rows][H][hd] rotated,

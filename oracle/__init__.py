@@ -73,6 +73,8 @@ def lib():
                 "orc_rope_rows": ([vp, i32, i32, i32, i32, ctypes.c_float], None),
                 "orc_silu_mul": ([ctypes.c_float, ctypes.c_float], ctypes.c_float),
                 "orc_attention": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, i32], None),
+                "orc_layer": ([vp, i32, vp, i32, i32], i32),
+                "orc_final_logits": ([vp, vp, vp], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -219,6 +221,22 @@ class OracleModel:
         rc = lib().orc_forward_one(self.h, int(token), pos, _p(logits))
         if rc != ORC_OK:
             raise RuntimeError(f"orc_forward_one failed: {rc}")
+        return logits
+
+    def layer(self, layer: int, x, start_pos: int = 0) -> np.ndarray:
+        """Layer `layer` alone over rows x [n, dim] (one chunk at start_pos); returns the output rows."""
+        y = np.array(x, dtype=np.float32, order="C", copy=True)
+        rc = lib().orc_layer(self.h, layer, _p(y), y.shape[0], start_pos)
+        if rc != ORC_OK:
+            raise RuntimeError(f"orc_layer failed: {rc}")
+        return y
+
+    def final_logits(self, x_row) -> np.ndarray:
+        x = np.ascontiguousarray(x_row, dtype=np.float32)
+        logits = np.empty((self.model.cfg.vocab,), np.float32)
+        rc = lib().orc_final_logits(self.h, _p(x), _p(logits))
+        if rc != ORC_OK:
+            raise RuntimeError(f"orc_final_logits failed: {rc}")
         return logits
 
     def kv(self, layer: int, which: int) -> np.ndarray:

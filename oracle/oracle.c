@@ -283,15 +283,144 @@ static void orc_dequant_block(const int32_t* acc, const float* w_scale, const fl
     for (int r = 0; r < n; ++r) out[(size_t)t * n + r] = orc_dequant(acc[(size_t)t * n + r], w_scale[r], a_scale[t]);
 }
 
+/* Scratch for one chunk of up to `cm` positions. */
+typedef struct {
+  float *y, *as, *qf, *kf, *vf, *o, *hb, *proj;
+  int8_t* qa;
+  int32_t *acc, *acc2;
+} orc_work;
+
+static void orc_work_free(orc_work* w) {
+  free(w->y); free(w->as); free(w->qf); free(w->kf); free(w->vf); free(w->o); free(w->hb); free(w->proj);
+  free(w->qa); free(w->acc); free(w->acc2);
+}
+
+static int orc_work_alloc(const orc_config* c, int cm, orc_work* w) {
+  const size_t QD = (size_t)c->n_heads * c->head_dim, KVD = (size_t)c->n_kv_heads * c->head_dim;
+  size_t kmax = (size_t)c->dim;
+  if (QD > kmax) kmax = QD;
+  if ((size_t)c->ffn > kmax) kmax = (size_t)c->ffn;
+  memset(w, 0, sizeof *w);
+  w->y = (float*)malloc(sizeof(float) * cm * kmax);
+  w->as = (float*)malloc(sizeof(float) * cm);
+  w->qf = (float*)malloc(sizeof(float) * cm * QD);
+  w->kf = (float*)malloc(sizeof(float) * cm * KVD);
+  w->vf = (float*)malloc(sizeof(float) * cm * KVD);
+  w->o = (float*)malloc(sizeof(float) * cm * QD);
+  w->hb = (float*)malloc(sizeof(float) * cm * c->ffn);
+  w->proj = (float*)malloc(sizeof(float) * cm * kmax);
+  w->qa = (int8_t*)malloc((size_t)cm * kmax);
+  w->acc = (int32_t*)malloc(sizeof(int32_t) * cm * kmax);
+  w->acc2 = (int32_t*)malloc(sizeof(int32_t) * cm * c->ffn);
+  if (!w->y || !w->as || !w->qf || !w->kf || !w->vf || !w->o || !w->hb || !w->proj || !w->qa || !w->acc ||
+      !w->acc2) {
+    orc_work_free(w);
+    return ORC_ERR_OOM;
+  }
+  return ORC_OK;
+}
+
+/*
+ * One decoder layer over one chunk of C positions pos0 .. pos0+C-1, in place
+ * on the residual rows x [C][dim]. "Batched Prefill", "The Solution": the
+ * chunk is quantised once per projection input and every output row reuses
+ * it; "What Stays Sequential": attention runs per position, after the
+ * chunk's K/V rows are written (each K/V row depends only on its own
+ * position, so writing the chunk's rows first changes no position's history).
+ */
+static void orc_layer_chunk(orc_model* m, orc_work* w, int L, float* x, int C, int pos0) {
+  const orc_config* c = &m->cfg;
+  const int D = c->dim, H = c->n_heads, HKV = c->n_kv_heads, HD = c->head_dim, F = c->ffn;
+  const int QD = H * HD, KVD = HKV * HD;
+  const size_t kvl = orc_kv_layer_elems(c);
+  const int8_t* const* W = m->w.w + 7 * L;
+  const float* const* S = m->w.w_scale + 7 * L;
+  float* Kc = m->kcache + kvl * L;
+  float* Vc = m->vcache + kvl * L;
+
+  /* attention block: norm -> quantise once -> Q, K, V projections */
+  orc_rmsnorm_rows(x, m->w.attn_norm[L], C, D, c->rms_eps, w->y);
+  orc_quantize_rows(w->y, C, D, w->qa, w->as);
+  orc_gemm_i8(w->qa, W[0], C, QD, D, w->acc, m->n_threads);
+  orc_dequant_block(w->acc, S[0], w->as, C, QD, w->qf);
+  orc_gemm_i8(w->qa, W[1], C, KVD, D, w->acc, m->n_threads);
+  orc_dequant_block(w->acc, S[1], w->as, C, KVD, w->kf);
+  orc_gemm_i8(w->qa, W[2], C, KVD, D, w->acc, m->n_threads);
+  orc_dequant_block(w->acc, S[2], w->as, C, KVD, w->vf);
+
+  /* RoPE at absolute positions, then write the chunk's K/V rows */
+  orc_rope_rows(w->qf, C, H, HD, pos0, c->rope_theta);
+  orc_rope_rows(w->kf, C, HKV, HD, pos0, c->rope_theta);
+  for (int i = 0; i < C; ++i) {
+    memcpy(Kc + (size_t)(pos0 + i) * KVD, w->kf + (size_t)i * KVD, sizeof(float) * KVD);
+    memcpy(Vc + (size_t)(pos0 + i) * KVD, w->vf + (size_t)i * KVD, sizeof(float) * KVD);
+  }
+
+  /* causal attention per position over kv[0 .. pos] */
+  orc_attention(w->qf, Kc, Vc, C, pos0, H, HKV, HD, w->o, m->n_threads);
+
+  /* O projection + residual */
+  orc_quantize_rows(w->o, C, QD, w->qa, w->as);
+  orc_gemm_i8(w->qa, W[3], C, D, QD, w->acc, m->n_threads);
+  orc_dequant_block(w->acc, S[3], w->as, C, D, w->proj);
+  for (size_t e = 0; e < (size_t)C * D; ++e) x[e] = x[e] + w->proj[e];
+
+  /* FFN: norm -> quantise -> gate, up -> SwiGLU -> quantise -> down + residual */
+  orc_rmsnorm_rows(x, m->w.ffn_norm[L], C, D, c->rms_eps, w->y);
+  orc_quantize_rows(w->y, C, D, w->qa, w->as);
+  orc_gemm_i8(w->qa, W[4], C, F, D, w->acc, m->n_threads);
+  orc_gemm_i8(w->qa, W[5], C, F, D, w->acc2, m->n_threads);
+  for (int i = 0; i < C; ++i)
+    for (int j = 0; j < F; ++j) {
+      size_t e = (size_t)i * F + j;
+      float g = orc_dequant(w->acc[e], S[4][j], w->as[i]);
+      float u = orc_dequant(w->acc2[e], S[5][j], w->as[i]);
+      w->hb[e] = orc_silu_mul(g, u);
+    }
+  orc_quantize_rows(w->hb, C, F, w->qa, w->as);
+  orc_gemm_i8(w->qa, W[6], C, D, F, w->acc, m->n_threads);
+  orc_dequant_block(w->acc, S[6], w->as, C, D, w->proj);
+  for (size_t e = 0; e < (size_t)C * D; ++e) x[e] = x[e] + w->proj[e];
+}
+
+/* "Single-pass prefill": final RMSNorm + output projection of one row. */
+int orc_final_logits(const orc_model* m, const float* x_row, float* logits) {
+  if (!m || !x_row || !logits) return ORC_ERR_ARG;
+  const orc_config* c = &m->cfg;
+  float* y = (float*)malloc(sizeof(float) * c->dim);
+  int8_t* q = (int8_t*)malloc((size_t)c->dim);
+  int32_t* acc = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->vocab);
+  if (!y || !q || !acc) {
+    free(y); free(q); free(acc);
+    return ORC_ERR_OOM;
+  }
+  float as;
+  orc_rmsnorm_row(x_row, m->w.final_norm, c->dim, c->rms_eps, y);
+  orc_quantize_row(y, c->dim, q, &as);
+  orc_gemm_i8(q, m->w.w_out, 1, c->vocab, c->dim, acc, m->n_threads);
+  for (int v = 0; v < c->vocab; ++v) logits[v] = orc_dequant(acc[v], m->w.w_out_scale[v], as);
+  free(y); free(q); free(acc);
+  return ORC_OK;
+}
+
+/* Layer L alone over rows x [n][dim] at positions start_pos .. (one chunk),
+ * in place; K/V rows of positions < start_pos come from the cache. */
+int orc_layer(orc_model* m, int layer, float* x, int n, int start_pos) {
+  if (!m || !x || n <= 0 || start_pos < 0 || layer < 0 || layer >= m->cfg.n_layers) return ORC_ERR_ARG;
+  if ((int64_t)start_pos + n > m->cfg.max_seq) return ORC_ERR_CAPACITY;
+  orc_work w;
+  if (orc_work_alloc(&m->cfg, n, &w) != ORC_OK) return ORC_ERR_OOM;
+  orc_layer_chunk(m, &w, layer, x, n, start_pos);
+  orc_work_free(&w);
+  return ORC_OK;
+}
+
 /*
  * Layer-major prefill. "Single-pass prefill", section "The fix": for each
  * layer the weights are read once and every prompt position is swept
  * through it; "Batched Prefill", section "The Solution": positions are
- * processed in chunks (the weights are read once per chunk), the
- * projections are int8 GEMMs over the chunk, and attention runs per
- * position in order, after the chunk's K/V rows are written (each K/V row
- * depends only on its own position, so writing the chunk's rows first does
- * not change any position's history).
+ * processed in chunks (the weights are read once per chunk). Only the last
+ * position's logits are produced.
  */
 int orc_prefill(orc_model* m, const int32_t* tokens, int n, int start_pos, int chunk, float* logits,
                 float* hidden) {
@@ -301,107 +430,29 @@ int orc_prefill(orc_model* m, const int32_t* tokens, int n, int start_pos, int c
   for (int i = 0; i < n; ++i)
     if (tokens[i] < 0 || tokens[i] >= c->vocab) return ORC_ERR_ARG;
 
-  const int D = c->dim, H = c->n_heads, HKV = c->n_kv_heads, HD = c->head_dim, F = c->ffn;
-  const int QD = H * HD, KVD = HKV * HD;
+  const int D = c->dim;
   const int CM = chunk < n ? chunk : n;
-  const int KMAX = F > QD ? (F > D ? F : D) : (QD > D ? QD : D);
-  const int NMAX = F > QD ? (F > D ? F : D) : (QD > D ? QD : D);
-  const size_t kvl = orc_kv_layer_elems(c);
-
+  orc_work w;
+  if (orc_work_alloc(c, CM, &w) != ORC_OK) return ORC_ERR_OOM;
   float* x = (float*)malloc(sizeof(float) * (size_t)CM * D);
-  float* y = (float*)malloc(sizeof(float) * (size_t)CM * KMAX);
-  int8_t* qa = (int8_t*)malloc((size_t)CM * KMAX);
-  float* as = (float*)malloc(sizeof(float) * (size_t)CM);
-  int32_t* acc = (int32_t*)malloc(sizeof(int32_t) * (size_t)CM * NMAX);
-  int32_t* acc2 = (int32_t*)malloc(sizeof(int32_t) * (size_t)CM * F);
-  float* qf = (float*)malloc(sizeof(float) * (size_t)CM * QD);
-  float* kf = (float*)malloc(sizeof(float) * (size_t)CM * KVD);
-  float* vf = (float*)malloc(sizeof(float) * (size_t)CM * KVD);
-  float* o = (float*)malloc(sizeof(float) * (size_t)CM * QD);
-  float* hb = (float*)malloc(sizeof(float) * (size_t)CM * F);
-  float* proj = (float*)malloc(sizeof(float) * (size_t)CM * NMAX);
   float* xlast = (float*)malloc(sizeof(float) * (size_t)D);
   int rc = ORC_OK;
-  if (!x || !y || !qa || !as || !acc || !acc2 || !qf || !kf || !vf || !o || !hb || !proj || !xlast) {
+  if (!x || !xlast) {
     rc = ORC_ERR_OOM;
     goto done;
   }
-
   for (int c0 = 0; c0 < n; c0 += chunk) {
     const int C = (n - c0) < chunk ? (n - c0) : chunk;
     for (int i = 0; i < C; ++i) memcpy(x + (size_t)i * D, m->w.tok_emb + (size_t)tokens[c0 + i] * D, sizeof(float) * D);
-
-    for (int L = 0; L < c->n_layers; ++L) {
-      const int8_t* const* W = m->w.w + 7 * L;
-      const float* const* S = m->w.w_scale + 7 * L;
-      float* Kc = m->kcache + kvl * L;
-      float* Vc = m->vcache + kvl * L;
-      const int pos0 = start_pos + c0;
-
-      /* attention block: norm -> quantise once -> Q, K, V projections */
-      orc_rmsnorm_rows(x, m->w.attn_norm[L], C, D, c->rms_eps, y);
-      orc_quantize_rows(y, C, D, qa, as);
-      orc_gemm_i8(qa, W[0], C, QD, D, acc, m->n_threads);
-      orc_dequant_block(acc, S[0], as, C, QD, qf);
-      orc_gemm_i8(qa, W[1], C, KVD, D, acc, m->n_threads);
-      orc_dequant_block(acc, S[1], as, C, KVD, kf);
-      orc_gemm_i8(qa, W[2], C, KVD, D, acc, m->n_threads);
-      orc_dequant_block(acc, S[2], as, C, KVD, vf);
-
-      /* RoPE at absolute positions, then write K/V rows of this chunk */
-      orc_rope_rows(qf, C, H, HD, pos0, c->rope_theta);
-      orc_rope_rows(kf, C, HKV, HD, pos0, c->rope_theta);
-      for (int i = 0; i < C; ++i) {
-        memcpy(Kc + (size_t)(pos0 + i) * KVD, kf + (size_t)i * KVD, sizeof(float) * KVD);
-        memcpy(Vc + (size_t)(pos0 + i) * KVD, vf + (size_t)i * KVD, sizeof(float) * KVD);
-      }
-
-      /* causal attention per position over kv[0 .. pos] */
-      orc_attention(qf, Kc, Vc, C, pos0, H, HKV, HD, o, m->n_threads);
-
-      /* O projection + residual */
-      orc_quantize_rows(o, C, QD, qa, as);
-      orc_gemm_i8(qa, W[3], C, D, QD, acc, m->n_threads);
-      orc_dequant_block(acc, S[3], as, C, D, proj);
-      for (size_t e = 0; e < (size_t)C * D; ++e) x[e] = x[e] + proj[e];
-
-      /* FFN: norm -> quantise -> gate, up -> SwiGLU -> quantise -> down + residual */
-      orc_rmsnorm_rows(x, m->w.ffn_norm[L], C, D, c->rms_eps, y);
-      orc_quantize_rows(y, C, D, qa, as);
-      orc_gemm_i8(qa, W[4], C, F, D, acc, m->n_threads);
-      orc_gemm_i8(qa, W[5], C, F, D, acc2, m->n_threads);
-      for (int i = 0; i < C; ++i)
-        for (int j = 0; j < F; ++j) {
-          size_t e = (size_t)i * F + j;
-          float g = orc_dequant(acc[e], S[4][j], as[i]);
-          float u = orc_dequant(acc2[e], S[5][j], as[i]);
-          hb[e] = orc_silu_mul(g, u);
-        }
-      orc_quantize_rows(hb, C, F, qa, as);
-      orc_gemm_i8(qa, W[6], C, D, F, acc, m->n_threads);
-      orc_dequant_block(acc, S[6], as, C, D, proj);
-      for (size_t e = 0; e < (size_t)C * D; ++e) x[e] = x[e] + proj[e];
-    }
+    for (int L = 0; L < c->n_layers; ++L) orc_layer_chunk(m, &w, L, x, C, start_pos + c0);
     if (c0 + C == n) memcpy(xlast, x + (size_t)(C - 1) * D, sizeof(float) * D);
   }
-
-  /* last position only: final RMSNorm -> quantise -> int8 output projection */
-  {
-    int32_t* lacc = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->vocab);
-    if (!lacc) {
-      rc = ORC_ERR_OOM;
-      goto done;
-    }
-    if (hidden) memcpy(hidden, xlast, sizeof(float) * D);
-    orc_rmsnorm_row(xlast, m->w.final_norm, D, c->rms_eps, y);
-    orc_quantize_row(y, D, qa, as);
-    orc_gemm_i8(qa, m->w.w_out, 1, c->vocab, D, lacc, m->n_threads);
-    for (int v = 0; v < c->vocab; ++v) logits[v] = orc_dequant(lacc[v], m->w.w_out_scale[v], as[0]);
-    free(lacc);
-  }
+  if (hidden) memcpy(hidden, xlast, sizeof(float) * D);
+  rc = orc_final_logits(m, xlast, logits);
 done:
-  free(x); free(y); free(qa); free(as); free(acc); free(acc2); free(qf); free(kf); free(vf); free(o); free(hb);
-  free(proj); free(xlast);
+  orc_work_free(&w);
+  free(x);
+  free(xlast);
   return rc;
 }
 

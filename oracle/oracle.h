@@ -69,6 +69,11 @@ void orc_destroy(orc_model* m);
  * The K/V cache persists across calls. */
 int orc_prefill(orc_model* m, const int32_t* tokens, int n, int start_pos, int chunk, float* logits,
                 float* hidden);
+/* One layer alone over rows x [n][dim] at positions start_pos .. start_pos+n-1
+ * (as one chunk), in place; K/V rows of earlier positions come from the cache. */
+int orc_layer(orc_model* m, int layer, float* x, int n, int start_pos);
+/* Final RMSNorm + quantise + output projection of one residual row [dim]. */
+int orc_final_logits(const orc_model* m, const float* x_row, float* logits);
 /* Per-token reference: prefill of one token at `pos`. */
 int orc_forward_one(orc_model* m, int32_t token, int pos, float* logits);
 /* K (which = 0) or V (which = 1) cache of a layer: [max_seq][n_kv_heads][head_dim]. */

@@ -74,12 +74,14 @@ SIGNATURES = {
     "pp_reset_stats": ([_vp], ctypes.c_int),
     "pp_model_gemm_engine": ([_vp], ctypes.c_int),
     "pp_set_profile_kernel": ([_vp, _i32], ctypes.c_int),
+    "pp_set_trace": ([_vp, _vp, _i32], ctypes.c_int),
     "pp_status_str": ([ctypes.c_int], ctypes.c_char_p),
     "pp_last_error": ([], ctypes.c_char_p),
     "pp_op_quantize": ([_vp, _i32, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
     "pp_op_rmsnorm_quantize": ([_vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "pp_op_gemm_acc": ([_i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp], ctypes.c_int),
     "pp_op_gemm": ([_i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp], ctypes.c_int),
+    "pp_set_exact_segment": ([_i32], ctypes.c_int),
     "pp_op_rope_kv": ([_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "pp_op_rope_table": ([_i32, _i32, _f32, _vp, _vp], ctypes.c_int),
     "pp_op_attention": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp], ctypes.c_int),
@@ -233,6 +235,10 @@ def pp_set_profile_kernel(h: int, kernel_class: int):
     _check(lib().pp_set_profile_kernel(h, kernel_class), "pp_set_profile_kernel")
 
 
+def pp_set_trace(h: int, d_trace, max_pos: int):
+    _check(lib().pp_set_trace(h, _ptr(d_trace), max_pos), "pp_set_trace")
+
+
 def pp_model_gemm_engine(h: int) -> int:
     return int(lib().pp_model_gemm_engine(h))
 
@@ -256,6 +262,10 @@ def pp_op_gemm_acc(engine, a8, a16, w, m, n, k, acc, stream=None):
 def pp_op_gemm(engine, epilogue, a8, a16, w, w_scale, a_scale, m, n, k, out, ldo, stream=None):
     _check(lib().pp_op_gemm(engine, epilogue, _ptr(a8), _ptr(a16), _ptr(w), _ptr(w_scale), _ptr(a_scale), m, n, k,
                             _ptr(out), ldo, _stream(stream)), "pp_op_gemm")
+
+
+def pp_set_exact_segment(seg_k: int):
+    _check(lib().pp_set_exact_segment(seg_k), "pp_set_exact_segment")
 
 
 def pp_op_rope_table(max_pos, head_dim, theta, table, stream=None):
@@ -342,6 +352,9 @@ class PrefillModel:
 
     def set_profile_kernel(self, kernel_class):
         pp_set_profile_kernel(self.h, kernel_class)
+
+    def set_trace(self, d_trace, max_pos):
+        pp_set_trace(self.h, d_trace, max_pos)
 
     def device_status(self):
         return pp_device_status(self.h)

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -164,6 +165,13 @@ struct pp_model {
   __half* a16 = nullptr;
   int32_t* tok = nullptr;
   int* status = nullptr;
+  float* trace = nullptr;  // optional residual-stream trace [(n_layers+1)][trace_pos][dim]
+  int trace_pos = 0;
+  // tcgen05 engine: tensor maps of every weight matrix (per layer, or per ring
+  // slot in streamed mode: qkv, o, gate/up, down) and of the fp16 activation
+  // buffer viewed with each GEMM's k (dim, n_heads*head_dim, ffn)
+  std::vector<CUtensorMap> wmap;
+  CUtensorMap amap_d{}, amap_qd{}, amap_f{};
   // stats and timing
   pp_stats stats{};
   std::vector<cudaEvent_t> ev_pool;
@@ -231,11 +239,37 @@ int launch(pp_model* m, int cls, cudaStream_t st, F&& fn) {
   return PP_OK;
 }
 
-int gemm(pp_model* m, cudaStream_t st, int epi, const float* ws, const int8_t* w, int M, int N, int K, float* out,
-         int ldo) {
+// K-extent of one exact f32 segment of the tcgen05 engine (pp_set_exact_segment).
+std::atomic<int> g_tc_seg{kTcSegK};
+int tc_segment() { return g_tc_seg.load(); }
+
+// One projection GEMM of the layer whose weight block sits at map group `mg`
+// (matrix `which`: 0 qkv, 1 o, 2 gate/up, 3 down).
+int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* ws, const int8_t* w, int M, int N,
+         int K, float* out, int ldo) {
+  if (m->engine == PP_GEMM_TC) {
+    const CUtensorMap& wm = m->wmap[(size_t)mg * 4 + which];
+    const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
+    return launch(m, PP_KERNEL_GEMM, st, [&] {
+      return launch_gemm_tc(epi, am, wm, ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, st);
+    });
+  }
   return launch(m, PP_KERNEL_GEMM, st, [&] {
     return launch_gemm_mma(epi, m->a8, w, ws, m->as, M, N, K, out, ldo, nullptr, st);
   });
+}
+
+int make_weight_maps(pp_model* m, const uint8_t* block) {
+  const pp_config& c = m->cfg;
+  const LayerPtrs L = layer_ptrs(m->lay, block);
+  const int D = c.dim, QD = c.n_heads * c.head_dim, QKV = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn;
+  CUtensorMap t[4];
+  PP_CUDA(make_tmap_w(&t[0], L.wqkv, QKV, D));
+  PP_CUDA(make_tmap_w(&t[1], L.wo, D, QD));
+  PP_CUDA(make_tmap_w(&t[2], L.wgu, 2 * F, D));
+  PP_CUDA(make_tmap_w(&t[3], L.wd, D, F));
+  for (auto& x : t) m->wmap.push_back(x);
+  return PP_OK;
 }
 
 template <class T>
@@ -270,11 +304,16 @@ int validate_cfg(const pp_config* c) {
 int load_impl(pp_model* m, const pp_weights* w) {
   const pp_config& c = m->cfg;
   PP_CUDA(cudaGetDevice(&m->device));
-  m->engine = (c.gemm_engine == PP_GEMM_AUTO || c.gemm_engine == PP_GEMM_MMA) ? PP_GEMM_MMA : -1;
-  if (m->engine < 0) {
-    set_err("gemm_engine %d is not available in this build", c.gemm_engine);
+  const bool tc = tc_available();
+  if (c.gemm_engine == PP_GEMM_TC && !tc) {
+    set_err("the tcgen05 engine needs an sm_103 device");
     return PP_ERR_UNSUPPORTED;
   }
+  if (c.gemm_engine != PP_GEMM_AUTO && c.gemm_engine != PP_GEMM_MMA && c.gemm_engine != PP_GEMM_TC) {
+    set_err("unknown gemm_engine %d", c.gemm_engine);
+    return PP_ERR_ARG;
+  }
+  m->engine = c.gemm_engine == PP_GEMM_MMA ? PP_GEMM_MMA : (tc ? PP_GEMM_TC : PP_GEMM_MMA);
   PP_CUDA(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
   m->lay = make_layout(c);
   const size_t D = c.dim, V = c.vocab, QD = (size_t)c.n_heads * c.head_dim,
@@ -311,6 +350,12 @@ int load_impl(pp_model* m, const pp_weights* w) {
   PP_TRY(dalloc(m, &m->tok, (size_t)c.max_seq));
   PP_TRY(dalloc(m, &m->status, 1));
   PP_CUDA(cudaMemsetAsync(m->status, 0, sizeof(int), m->stream));
+  PP_CUDA(cudaMemsetAsync(m->a16, 0, MC * KMAX * sizeof(__half), m->stream));
+  if (m->engine == PP_GEMM_TC) {
+    PP_CUDA(make_tmap_a(&m->amap_d, m->a16, (int)MC, (int)D));
+    PP_CUDA(make_tmap_a(&m->amap_qd, m->a16, (int)MC, (int)QD));
+    PP_CUDA(make_tmap_a(&m->amap_f, m->a16, (int)MC, (int)F));
+  }
 
   // layers
   const size_t stride = m->lay.bytes;
@@ -328,6 +373,8 @@ int load_impl(pp_model* m, const pp_weights* w) {
       }
     }
     cudaFreeHost(stage);
+    if (m->engine == PP_GEMM_TC)
+      for (int l = 0; l < c.n_layers; ++l) PP_TRY(make_weight_maps(m, m->d_layers + stride * l));
   } else {
     cudaError_t e = cudaHostAlloc(&m->h_layers, stride * c.n_layers, cudaHostAllocDefault);
     if (e != cudaSuccess) {
@@ -342,6 +389,7 @@ int load_impl(pp_model* m, const pp_weights* w) {
       PP_CUDA(cudaEventCreateWithFlags(&m->ring_ready[s], cudaEventDisableTiming));
       PP_CUDA(cudaEventCreateWithFlags(&m->ring_free[s], cudaEventDisableTiming));
       PP_CUDA(cudaEventRecord(m->ring_free[s], m->stream));
+      if (m->engine == PP_GEMM_TC) PP_TRY(make_weight_maps(m, m->ring[s]));
     }
   }
   PP_CUDA(cudaStreamSynchronize(m->stream));
@@ -371,7 +419,7 @@ int check_prefill_args(pp_model* m, int n, int start_pos, int chunk) {
     set_err("bad prefill arguments: n=%d start_pos=%d chunk=%d (max_chunk %d)", n, start_pos, chunk, m->cfg.max_chunk);
     return PP_ERR_ARG;
   }
-  if ((int64_t)start_pos + n > m->cfg.max_seq) {
+  if ((int64_t)start_pos + n > m->cfg.max_seq || (m->trace && (int64_t)start_pos + n > m->trace_pos)) {
     set_err("start_pos + n = %lld exceeds max_seq %d", (long long)start_pos + n, m->cfg.max_seq);
     return PP_ERR_CAPACITY;
   }
@@ -430,12 +478,17 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     m->ev_pool.push_back(e);
   }
   cudaStream_t cs = c.mode == PP_MODE_STREAMED ? m->stream : st;
+  __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
   for (int c0 = 0; c0 < n; c0 += chunk) {
     const int C = std::min(chunk, n - c0);
     const int pos0 = start_pos + c0;
     PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, cs); }));
     for (int l = 0; l < c.n_layers; ++l, ++visit) {
+      if (m->trace)
+        PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)l * m->trace_pos + pos0) * D, m->x, sizeof(float) * C * D,
+                                cudaMemcpyDeviceToDevice, cs));
       const uint8_t* base;
+      const int mg = c.mode == PP_MODE_STREAMED ? visit % c.ring_slots : l;
       if (c.mode == PP_MODE_STREAMED) {
         PP_TRY(stream_layer(m, cs, visit, n_visits, &base));
       } else {
@@ -446,9 +499,9 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       float* vcl = m->vc + kvl * l;
       // attention block
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, nullptr, m->as, cs);
+        return launch_norm_quant(m->x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
       }));
-      PP_TRY(gemm(m, cs, EPI_STORE, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
+      PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
       PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
         return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
       }));
@@ -456,25 +509,28 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
         return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, cs);
       }));
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, nullptr, m->as, cs);
+        return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, q16, m->as, cs);
       }));
-      PP_TRY(gemm(m, cs, EPI_RESID, L.so, L.wo, C, D, QD, m->x, D));
+      PP_TRY(gemm(m, cs, EPI_RESID, mg, 1, L.so, L.wo, C, D, QD, m->x, D));
       // FFN block
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, nullptr, m->as, cs);
+        return launch_norm_quant(m->x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
       }));
-      PP_TRY(gemm(m, cs, EPI_SWIGLU, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
+      PP_TRY(gemm(m, cs, EPI_SWIGLU, mg, 2, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, nullptr, m->as, cs);
+        return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, q16, m->as, cs);
       }));
-      PP_TRY(gemm(m, cs, EPI_RESID, L.sd, L.wd, C, D, F, m->x, D));
+      PP_TRY(gemm(m, cs, EPI_RESID, mg, 3, L.sd, L.wd, C, D, F, m->x, D));
       if (c.mode == PP_MODE_STREAMED) PP_CUDA(cudaEventRecord(m->ring_free[visit % c.ring_slots], cs));
     }
+    if (m->trace)
+      PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)c.n_layers * m->trace_pos + pos0) * D, m->x,
+                              sizeof(float) * C * D, cudaMemcpyDeviceToDevice, cs));
     if (c0 + C == n) {
       // last position only: final RMSNorm -> quantise -> output projection
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
         return launch_norm_quant(m->x + (size_t)(C - 1) * D, D, m->final_norm, 1, D, c.rms_eps, nullptr, m->a8,
-                                 nullptr, m->as, cs);
+                                 q16, m->as, cs);
       }));
       PP_TRY(launch(m, PP_KERNEL_LM_HEAD, cs, [&] {
         return launch_lm_head(m->a8, m->as, m->w_out, m->s_out, c.vocab, D, d_logits, cs);
@@ -638,6 +694,17 @@ int pp_reset_stats(pp_model* m) {
 
 int pp_model_gemm_engine(const pp_model* m) { return m ? m->engine : PP_ERR_ARG; }
 
+int pp_set_trace(pp_model* m, float* d_trace, int32_t max_pos) {
+  if (!m || (d_trace && max_pos <= 0)) {
+    set_err("bad pp_set_trace arguments");
+    return PP_ERR_ARG;
+  }
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  m->trace = d_trace;
+  m->trace_pos = d_trace ? max_pos : 0;
+  return PP_OK;
+}
+
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class) {
   if (!m || kernel_class < PP_KERNEL_NONE || kernel_class >= PP_KERNEL_COUNT) {
     set_err("bad pp_set_profile_kernel arguments");
@@ -680,21 +747,41 @@ static int check_gemm(int32_t engine, const int8_t* a8, const uint16_t* a16, con
     set_err("bad GEMM shape m=%d n=%d k=%d (k%%64, n%%32)", m, n, k);
     return PP_ERR_ARG;
   }
-  if (engine == PP_GEMM_MMA || engine == PP_GEMM_AUTO) {
-    if (!a8) { set_err("engine needs the int8 activations"); return PP_ERR_ARG; }
+  if (engine == PP_GEMM_MMA) {
+    if (!a8) { set_err("the mma.sync engine needs the int8 activations"); return PP_ERR_ARG; }
     return PP_OK;
   }
-  (void)a16;
-  set_err("gemm engine %d is not available in this build", engine);
-  return PP_ERR_UNSUPPORTED;
+  if (engine == PP_GEMM_TC) {
+    if (!tc_available()) { set_err("the tcgen05 engine needs an sm_103 device"); return PP_ERR_UNSUPPORTED; }
+    if (!a16 || n % 256 || (reinterpret_cast<uintptr_t>(a16) & 15) || (reinterpret_cast<uintptr_t>(w) & 15)) {
+      set_err("the tcgen05 engine needs fp16 activations, n %% 256 == 0 and 16-byte aligned operands");
+      return PP_ERR_ARG;
+    }
+    return PP_OK;
+  }
+  set_err("unknown gemm engine %d", engine);
+  return PP_ERR_ARG;
+}
+
+
+static cudaError_t op_gemm_launch(int32_t engine, int epi, const int8_t* a8, const uint16_t* a16, const int8_t* w,
+                                  const float* ws, const float* as, int m, int n, int k, float* out, int ldo,
+                                  int32_t* acc, cudaStream_t st) {
+  if (engine == PP_GEMM_MMA) return launch_gemm_mma(epi, a8, w, ws, as, m, n, k, out, ldo, acc, st);
+  CUtensorMap ma, mw;
+  cudaError_t e = make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_w(&mw, w, n, k);
+  if (e != cudaSuccess) return e;
+  return launch_gemm_tc(epi, ma, mw, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), nullptr, st);
 }
 
 int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
                    int32_t k, int32_t* acc, void* stream) {
   PP_TRY(check_gemm(engine, a8, a16, w, m, n, k));
   if (!acc) { set_err("null acc"); return PP_ERR_ARG; }
-  return ok_launch(launch_gemm_mma(EPI_ACC, a8, w, nullptr, nullptr, m, n, k, nullptr, 0, acc,
-                                   static_cast<cudaStream_t>(stream)),
+  return ok_launch(op_gemm_launch(engine, EPI_ACC, a8, a16, w, nullptr, nullptr, m, n, k, nullptr, 0, acc,
+                                  static_cast<cudaStream_t>(stream)),
                    "gemm_acc");
 }
 
@@ -704,13 +791,22 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
   PP_TRY(check_gemm(engine, a8, a16, w, m, n, k));
   const int out_cols = epilogue == PP_EPI_SWIGLU ? n / 2 : n;
   if (!w_scale || !a_scale || !out || ldo < out_cols || (epilogue < PP_EPI_STORE || epilogue > PP_EPI_SWIGLU) ||
-      ldo % 2) {
-    set_err("bad pp_op_gemm arguments");
+      ldo % 4 || (reinterpret_cast<uintptr_t>(out) & 15)) {
+    set_err("bad pp_op_gemm arguments (ldo %% 4, 16-byte aligned out)");
     return PP_ERR_ARG;
   }
-  return ok_launch(launch_gemm_mma(epilogue, a8, w, w_scale, a_scale, m, n, k, out, ldo, nullptr,
-                                   static_cast<cudaStream_t>(stream)),
+  return ok_launch(op_gemm_launch(engine, epilogue, a8, a16, w, w_scale, a_scale, m, n, k, out, ldo, nullptr,
+                                  static_cast<cudaStream_t>(stream)),
                    "gemm");
+}
+
+int pp_set_exact_segment(int32_t seg_k) {
+  if (seg_k < 64 || seg_k > kTcSegK || seg_k % 64) {
+    set_err("exact segment must be a multiple of 64 in [64, %d]", kTcSegK);
+    return PP_ERR_ARG;
+  }
+  g_tc_seg.store(seg_k);
+  return PP_OK;
 }
 
 int pp_op_rope_table(int32_t max_pos, int32_t head_dim, float theta, float* rope_table, void* stream) {

@@ -1,8 +1,11 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include <cstdint>
 
@@ -31,6 +34,16 @@ cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t*
 // mma.sync engine (k_gemm_mma.cu): a8 [m][k] int8, w [n][k] int8.
 cudaError_t launch_gemm_mma(int epi, const int8_t* a8, const int8_t* w, const float* ws, const float* as, int m,
                             int n, int k, float* out, int ldo, int32_t* acc, cudaStream_t s);
+
+// tcgen05 engine (k_gemm_tc.cu): a16 [m][k] fp16 codes via a tensor map, w [n][k] int8 via a tensor map.
+// n % 256 == 0, k % 64 == 0; exact f32 segments of seg_k (<= 1024) along k.
+bool tc_available();
+cudaError_t make_tmap_a(CUtensorMap* map, const __half* a16, int rows, int k);
+cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k);
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, const float* ws, const float* as,
+                           int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k, int* status,
+                           cudaStream_t s);
+constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)
 cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,

@@ -174,3 +174,17 @@ def test_every_matrix_reaches_the_output(zero):
     _, h_full = oracle.OracleModel(_micro(seed=6)).prefill(toks, 0, 4, want_hidden=True)
     _, h_zero = oracle.OracleModel(_micro(seed=6, zero=zero)).prefill(toks, 0, 4, want_hidden=True)
     assert not np.array_equal(h_full, h_zero)
+
+
+def test_layer_by_layer_composes_to_prefill(tiny_model):
+    # the single-layer entry point, applied layer after layer from the
+    # embedding rows, and the final projection reproduce the whole prefill
+    toks = synth.prompt(tiny_model.cfg, 20)
+    om = oracle.OracleModel(tiny_model)
+    ref, hidden = om.prefill(toks, 0, 20, want_hidden=True)
+    om.kv_reset()
+    x = tiny_model.tok_emb[toks].astype(np.float32)
+    for L in range(tiny_model.cfg.n_layers):
+        x = om.layer(L, x, 0)
+    assert np.array_equal(x[-1], hidden)
+    assert np.array_equal(_bits(om.final_logits(x[-1])), _bits(ref))
