@@ -369,6 +369,63 @@ def run_ours(args, cfg, world, rank, local, pg):
     return 0
 
 
+# ----------------------------------------------------------------------------- one kernel
+def run_op(args):
+    """Time one kernel alone at a given shape (for ncu captures and per-kernel
+    rooflines): --op gemm --engine 1|2 --m --n --k, or --op attention --m
+    (query rows) --start (start position) on the 8B head layout."""
+    import torch
+
+    import prompt_prefill_gb300 as pp
+    import synth
+
+    peaks = load_peaks()
+    torch.cuda.set_device(0)
+    m, n, k = args.m, args.n, args.k
+    if args.op == "gemm":
+        a = torch.from_numpy(synth.uniform_i8(1, 1, (m, k))).cuda()
+        a16 = a.to(torch.float16)
+        w = torch.from_numpy(synth.uniform_i8(1, 2, (n, k))).cuda()
+        ws = torch.full((n,), 1e-3, device="cuda")
+        as_ = torch.full((m,), 1e-2, device="cuda")
+        out = torch.empty((m, n), device="cuda")
+        engine = args.engine or pp.PP_GEMM_TC
+
+        def once():
+            pp.pp_op_gemm(engine, pp.PP_EPI_STORE, a, a16, w, ws, as_, m, n, k, out, n)
+        work, unit, bound = 2.0 * m * n * k, "TFLOP/s", "tensor"
+    elif args.op == "attention":
+        H, Hkv, hd = 32, 8, 128
+        start = args.start
+        q = torch.randn((m, H, hd), device="cuda")
+        kc = torch.randn((start + m, Hkv, hd), device="cuda")
+        vc = torch.randn((start + m, Hkv, hd), device="cuda")
+        o = torch.empty_like(q)
+
+        def once():
+            pp.pp_op_attention(q, kc, vc, m, start, H, Hkv, hd, o)
+        pairs = sum(start + i + 1 for i in range(m))
+        work, unit, bound = 4.0 * hd * H * pairs, "TFLOP/s", "alu"
+    else:
+        raise SystemExit(f"unknown --op {args.op}")
+    for _ in range(args.warmup):
+        once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    achieved = work / (ms / 1000) / 1e12
+    peak, src = peak_for(bound, peaks)
+    print(json.dumps({"op": args.op, "m": m, "n": n, "k": k, "start": args.start, "engine": args.engine,
+                      "ms": ms, "achieved": achieved, "unit": unit, "peak": peak, "frac": achieved / peak,
+                      "peak_source": src}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -382,7 +439,14 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention")
+    ap.add_argument("--m", type=int, default=512)
+    ap.add_argument("--n", type=int, default=28672)
+    ap.add_argument("--k", type=int, default=4096)
+    ap.add_argument("--start", type=int, default=3584)
     args = ap.parse_args(argv)
+    if args.op:
+        return run_op(args)
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least 3 warm-up steps
     import synth
