@@ -183,14 +183,20 @@ int pp_reset_stats(pp_model* m);
  * and summed duration appear in pp_stats (prof_launches, prof_ms). */
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
-/* Record the residual stream at every layer boundary: while set, each
- * prefill call copies the rows of positions p (start_pos <= p < start_pos+n)
- * entering layer l to d_trace[l][p][0..dim) and the rows leaving the last
- * layer to d_trace[n_layers][p]. d_trace is a device buffer of
- * (n_layers + 1) * max_pos * dim f32 owned by the caller, who keeps it alive
- * while it is set; NULL switches tracing off. Calls whose positions exceed
- * max_pos fail with PP_ERR_CAPACITY while tracing is on. */
-int pp_set_trace(pp_model* m, float* d_trace, int32_t max_pos);
+/* Record the residual stream at every layer boundary and the int8 codes at
+ * every quantisation point (for layer-by-layer verification). While set,
+ * each prefill call writes, for its positions p < max_pos:
+ *  - d_x [(n_layers+1)][max_pos][dim] f32: the rows entering layer l at
+ *    d_x[l][p], the rows leaving the last layer at d_x[n_layers][p];
+ *  - d_codes [n_layers][4][max_pos][kmax] int8 with kmax = max(dim,
+ *    n_heads*head_dim, ffn) and d_scales [n_layers][4][max_pos] f32: the
+ *    codes and row scales of quantisation point q of layer l (0 attention
+ *    input, 1 attention output, 2 FFN input, 3 SwiGLU output), each row
+ *    starting at its kmax pitch (d_codes/d_scales may be NULL).
+ * The caller owns the device buffers and keeps them alive while set; d_x
+ * NULL switches tracing off. Calls whose positions exceed max_pos fail with
+ * PP_ERR_CAPACITY while tracing is on. */
+int pp_set_trace(pp_model* m, float* d_x, int8_t* d_codes, float* d_scales, int32_t max_pos);
 
 /* The GEMM engine the model resolved to (PP_GEMM_MMA or PP_GEMM_TC). */
 int pp_model_gemm_engine(const pp_model* m);

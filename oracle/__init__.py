@@ -35,6 +35,13 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+class OrcForce(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p * 4), ("scales", ctypes.c_void_p * 4), ("kmax", ctypes.c_int),
+                ("mismatches", ctypes.c_int64 * 4), ("scale_mismatches", ctypes.c_int64 * 4),
+                ("max_margin", ctypes.c_float * 4), ("max_code_diff", ctypes.c_int * 4),
+                ("max_scale_rel", ctypes.c_float * 4)]
+
+
 class OrcConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("dim", "n_layers", "n_heads", "n_kv_heads", "head_dim", "ffn",
                                                "vocab", "max_seq")] + [("rms_eps", ctypes.c_float),
@@ -75,6 +82,7 @@ def lib():
                 "orc_attention": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, i32], None),
                 "orc_layer": ([vp, i32, vp, i32, i32], i32),
                 "orc_final_logits": ([vp, vp, vp], i32),
+                "orc_layer_forced": ([vp, i32, vp, i32, i32, vp], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -230,6 +238,26 @@ class OracleModel:
         if rc != ORC_OK:
             raise RuntimeError(f"orc_layer failed: {rc}")
         return y
+
+    def layer_forced(self, layer: int, x, codes, scales, start_pos: int = 0):
+        """Layer `layer` over rows x [n, dim] taking the given codes [4, n, kmax]
+        int8 and scales [4, n] at its quantisation points; returns the output
+        rows and, per point, where the oracle's own decisions differed."""
+        y = np.array(x, dtype=np.float32, order="C", copy=True)
+        codes = np.ascontiguousarray(codes, dtype=np.int8)
+        scales = np.ascontiguousarray(scales, dtype=np.float32)
+        f = OrcForce()
+        for i in range(4):
+            f.codes[i] = codes[i].ctypes.data
+            f.scales[i] = scales[i].ctypes.data
+        f.kmax = codes.shape[2]
+        rc = lib().orc_layer_forced(self.h, layer, _p(y), y.shape[0], start_pos, ctypes.byref(f))
+        if rc != ORC_OK:
+            raise RuntimeError(f"orc_layer_forced failed: {rc}")
+        stats = {"mismatches": list(f.mismatches), "scale_mismatches": list(f.scale_mismatches),
+                 "max_margin": list(f.max_margin), "max_code_diff": list(f.max_code_diff),
+                 "max_scale_rel": list(f.max_scale_rel)}
+        return y, stats
 
     def final_logits(self, x_row) -> np.ndarray:
         x = np.ascontiguousarray(x_row, dtype=np.float32)

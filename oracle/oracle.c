@@ -320,6 +320,44 @@ static int orc_work_alloc(const orc_config* c, int cm, orc_work* w) {
   return ORC_OK;
 }
 
+/* Quantise rows as the method does; if `f` is given, compare the result with
+ * the codes another implementation decided for the same quantisation point
+ * and continue with those (see orc_layer_forced). */
+static void orc_quantize_forced(const float* y, int rows, int k, int8_t* qa, float* as, orc_force* f, int pt,
+                                int row0) {
+  orc_quantize_rows(y, rows, k, qa, as);
+  if (!f) return;
+  for (int r = 0; r < rows; ++r) {
+    const int8_t* fc = f->codes[pt] + (size_t)(row0 + r) * f->kmax;
+    const float fs = f->scales[pt][row0 + r];
+    if (fs != as[r]) {
+      f->scale_mismatches[pt] += 1;
+      float rel = fabsf(fs - as[r]) / (as[r] > 0.0f ? as[r] : 1.0f);
+      if (rel > f->max_scale_rel[pt]) f->max_scale_rel[pt] = rel;
+    }
+    float amax_row = 0.0f;
+    for (int i = 0; i < k; ++i) {
+      float a = fabsf(y[(size_t)r * k + i]);
+      if (a > amax_row) amax_row = a;
+    }
+    const float inv = amax_row == 0.0f ? 0.0f : 127.0f / amax_row;
+    for (int i = 0; i < k; ++i) {
+      const int8_t mine = qa[(size_t)r * k + i];
+      if (mine != fc[i]) {
+        f->mismatches[pt] += 1;
+        int d = mine - fc[i];
+        if (d < 0) d = -d;
+        if (d > f->max_code_diff[pt]) f->max_code_diff[pt] = d;
+        const float t = y[(size_t)r * k + i] * inv;
+        const float margin = fabsf(t - (floorf(t) + 0.5f));
+        if (margin > f->max_margin[pt]) f->max_margin[pt] = margin;
+      }
+      qa[(size_t)r * k + i] = fc[i];
+    }
+    as[r] = fs;
+  }
+}
+
 /*
  * One decoder layer over one chunk of C positions pos0 .. pos0+C-1, in place
  * on the residual rows x [C][dim]. "Batched Prefill", "The Solution": the
@@ -328,7 +366,8 @@ static int orc_work_alloc(const orc_config* c, int cm, orc_work* w) {
  * chunk's K/V rows are written (each K/V row depends only on its own
  * position, so writing the chunk's rows first changes no position's history).
  */
-static void orc_layer_chunk(orc_model* m, orc_work* w, int L, float* x, int C, int pos0) {
+static void orc_layer_chunk(orc_model* m, orc_work* w, int L, float* x, int C, int pos0, orc_force* f,
+                            int row0) {
   const orc_config* c = &m->cfg;
   const int D = c->dim, H = c->n_heads, HKV = c->n_kv_heads, HD = c->head_dim, F = c->ffn;
   const int QD = H * HD, KVD = HKV * HD;
@@ -340,7 +379,7 @@ static void orc_layer_chunk(orc_model* m, orc_work* w, int L, float* x, int C, i
 
   /* attention block: norm -> quantise once -> Q, K, V projections */
   orc_rmsnorm_rows(x, m->w.attn_norm[L], C, D, c->rms_eps, w->y);
-  orc_quantize_rows(w->y, C, D, w->qa, w->as);
+  orc_quantize_forced(w->y, C, D, w->qa, w->as, f, 0, row0);
   orc_gemm_i8(w->qa, W[0], C, QD, D, w->acc, m->n_threads);
   orc_dequant_block(w->acc, S[0], w->as, C, QD, w->qf);
   orc_gemm_i8(w->qa, W[1], C, KVD, D, w->acc, m->n_threads);
@@ -360,14 +399,14 @@ static void orc_layer_chunk(orc_model* m, orc_work* w, int L, float* x, int C, i
   orc_attention(w->qf, Kc, Vc, C, pos0, H, HKV, HD, w->o, m->n_threads);
 
   /* O projection + residual */
-  orc_quantize_rows(w->o, C, QD, w->qa, w->as);
+  orc_quantize_forced(w->o, C, QD, w->qa, w->as, f, 1, row0);
   orc_gemm_i8(w->qa, W[3], C, D, QD, w->acc, m->n_threads);
   orc_dequant_block(w->acc, S[3], w->as, C, D, w->proj);
   for (size_t e = 0; e < (size_t)C * D; ++e) x[e] = x[e] + w->proj[e];
 
   /* FFN: norm -> quantise -> gate, up -> SwiGLU -> quantise -> down + residual */
   orc_rmsnorm_rows(x, m->w.ffn_norm[L], C, D, c->rms_eps, w->y);
-  orc_quantize_rows(w->y, C, D, w->qa, w->as);
+  orc_quantize_forced(w->y, C, D, w->qa, w->as, f, 2, row0);
   orc_gemm_i8(w->qa, W[4], C, F, D, w->acc, m->n_threads);
   orc_gemm_i8(w->qa, W[5], C, F, D, w->acc2, m->n_threads);
   for (int i = 0; i < C; ++i)
@@ -377,7 +416,7 @@ static void orc_layer_chunk(orc_model* m, orc_work* w, int L, float* x, int C, i
       float u = orc_dequant(w->acc2[e], S[5][j], w->as[i]);
       w->hb[e] = orc_silu_mul(g, u);
     }
-  orc_quantize_rows(w->hb, C, F, w->qa, w->as);
+  orc_quantize_forced(w->hb, C, F, w->qa, w->as, f, 3, row0);
   orc_gemm_i8(w->qa, W[6], C, D, F, w->acc, m->n_threads);
   orc_dequant_block(w->acc, S[6], w->as, C, D, w->proj);
   for (size_t e = 0; e < (size_t)C * D; ++e) x[e] = x[e] + w->proj[e];
@@ -410,7 +449,21 @@ int orc_layer(orc_model* m, int layer, float* x, int n, int start_pos) {
   if ((int64_t)start_pos + n > m->cfg.max_seq) return ORC_ERR_CAPACITY;
   orc_work w;
   if (orc_work_alloc(&m->cfg, n, &w) != ORC_OK) return ORC_ERR_OOM;
-  orc_layer_chunk(m, &w, layer, x, n, start_pos);
+  orc_layer_chunk(m, &w, layer, x, n, start_pos, NULL, 0);
+  orc_work_free(&w);
+  return ORC_OK;
+}
+
+/* Layer L over rows x [n][dim] (one chunk at start_pos), taking at each of
+ * its four quantisation points (0 attention input, 1 attention output,
+ * 2 FFN input, 3 SwiGLU output) the codes and scales of `f` in place of its
+ * own, after recording where its own decision differs. */
+int orc_layer_forced(orc_model* m, int layer, float* x, int n, int start_pos, orc_force* f) {
+  if (!m || !x || !f || n <= 0 || start_pos < 0 || layer < 0 || layer >= m->cfg.n_layers) return ORC_ERR_ARG;
+  if ((int64_t)start_pos + n > m->cfg.max_seq) return ORC_ERR_CAPACITY;
+  orc_work w;
+  if (orc_work_alloc(&m->cfg, n, &w) != ORC_OK) return ORC_ERR_OOM;
+  orc_layer_chunk(m, &w, layer, x, n, start_pos, f, 0);
   orc_work_free(&w);
   return ORC_OK;
 }
@@ -444,7 +497,7 @@ int orc_prefill(orc_model* m, const int32_t* tokens, int n, int start_pos, int c
   for (int c0 = 0; c0 < n; c0 += chunk) {
     const int C = (n - c0) < chunk ? (n - c0) : chunk;
     for (int i = 0; i < C; ++i) memcpy(x + (size_t)i * D, m->w.tok_emb + (size_t)tokens[c0 + i] * D, sizeof(float) * D);
-    for (int L = 0; L < c->n_layers; ++L) orc_layer_chunk(m, &w, L, x, C, start_pos + c0);
+    for (int L = 0; L < c->n_layers; ++L) orc_layer_chunk(m, &w, L, x, C, start_pos + c0, NULL, 0);
     if (c0 + C == n) memcpy(xlast, x + (size_t)(C - 1) * D, sizeof(float) * D);
   }
   if (hidden) memcpy(hidden, xlast, sizeof(float) * D);

@@ -72,6 +72,21 @@ int orc_prefill(orc_model* m, const int32_t* tokens, int n, int start_pos, int c
 /* One layer alone over rows x [n][dim] at positions start_pos .. start_pos+n-1
  * (as one chunk), in place; K/V rows of earlier positions come from the cache. */
 int orc_layer(orc_model* m, int layer, float* x, int n, int start_pos);
+/* Codes decided by another implementation at the four quantisation points
+ * of a layer (0 attention input [dim], 1 attention output [n_heads*head_dim],
+ * 2 FFN input [dim], 3 SwiGLU output [ffn]); rows have a pitch of kmax bytes.
+ * The oracle fills in where its own decisions differed. */
+typedef struct {
+  const int8_t* codes[4];
+  const float* scales[4];
+  int kmax;
+  int64_t mismatches[4];        /* codes that differ */
+  int64_t scale_mismatches[4];  /* row scales that differ */
+  float max_margin[4];          /* largest distance of a differing code's f32 value from a half-integer tie */
+  int max_code_diff[4];         /* largest |difference| of differing codes */
+  float max_scale_rel[4];       /* largest relative difference of differing row scales */
+} orc_force;
+int orc_layer_forced(orc_model* m, int layer, float* x, int n, int start_pos, orc_force* f);
 /* Final RMSNorm + quantise + output projection of one residual row [dim]. */
 int orc_final_logits(const orc_model* m, const float* x_row, float* logits);
 /* Per-token reference: prefill of one token at `pos`. */

@@ -74,7 +74,7 @@ SIGNATURES = {
     "pp_reset_stats": ([_vp], ctypes.c_int),
     "pp_model_gemm_engine": ([_vp], ctypes.c_int),
     "pp_set_profile_kernel": ([_vp, _i32], ctypes.c_int),
-    "pp_set_trace": ([_vp, _vp, _i32], ctypes.c_int),
+    "pp_set_trace": ([_vp, _vp, _vp, _vp, _i32], ctypes.c_int),
     "pp_status_str": ([ctypes.c_int], ctypes.c_char_p),
     "pp_last_error": ([], ctypes.c_char_p),
     "pp_op_quantize": ([_vp, _i32, _i32, _vp, _vp, _vp, _vp], ctypes.c_int),
@@ -235,8 +235,8 @@ def pp_set_profile_kernel(h: int, kernel_class: int):
     _check(lib().pp_set_profile_kernel(h, kernel_class), "pp_set_profile_kernel")
 
 
-def pp_set_trace(h: int, d_trace, max_pos: int):
-    _check(lib().pp_set_trace(h, _ptr(d_trace), max_pos), "pp_set_trace")
+def pp_set_trace(h: int, d_x, d_codes, d_scales, max_pos: int):
+    _check(lib().pp_set_trace(h, _ptr(d_x), _ptr(d_codes), _ptr(d_scales), max_pos), "pp_set_trace")
 
 
 def pp_model_gemm_engine(h: int) -> int:
@@ -353,8 +353,8 @@ class PrefillModel:
     def set_profile_kernel(self, kernel_class):
         pp_set_profile_kernel(self.h, kernel_class)
 
-    def set_trace(self, d_trace, max_pos):
-        pp_set_trace(self.h, d_trace, max_pos)
+    def set_trace(self, d_x, d_codes, d_scales, max_pos):
+        pp_set_trace(self.h, d_x, d_codes, d_scales, max_pos)
 
     def device_status(self):
         return pp_device_status(self.h)

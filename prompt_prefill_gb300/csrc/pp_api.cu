@@ -166,6 +166,8 @@ struct pp_model {
   int32_t* tok = nullptr;
   int* status = nullptr;
   float* trace = nullptr;  // optional residual-stream trace [(n_layers+1)][trace_pos][dim]
+  int8_t* trace_codes = nullptr;  // [n_layers][4][trace_pos][kmax]
+  float* trace_scales = nullptr;  // [n_layers][4][trace_pos]
   int trace_pos = 0;
   // tcgen05 engine: tensor maps of every weight matrix (per layer, or per ring
   // slot in streamed mode: qkv, o, gate/up, down) and of the fp16 activation
@@ -460,6 +462,17 @@ int stream_layer(pp_model* m, cudaStream_t st, int v, int n_visits, const uint8_
   return PP_OK;
 }
 
+int trace_codes(pp_model* m, cudaStream_t cs, int layer, int point, int pos0, int C, int K) {
+  if (!m->trace_codes) return PP_OK;
+  const pp_config& c = m->cfg;
+  const size_t kmax = std::max(std::max((size_t)c.dim, (size_t)c.n_heads * c.head_dim), (size_t)c.ffn);
+  const size_t rec = (size_t)(layer * 4 + point) * m->trace_pos + pos0;
+  PP_CUDA(cudaMemcpy2DAsync(m->trace_codes + rec * kmax, kmax, m->a8, K, K, C, cudaMemcpyDeviceToDevice, cs));
+  if (m->trace_scales)
+    PP_CUDA(cudaMemcpyAsync(m->trace_scales + rec, m->as, sizeof(float) * C, cudaMemcpyDeviceToDevice, cs));
+  return PP_OK;
+}
+
 int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
                  cudaStream_t st) {
   const pp_config& c = m->cfg;
@@ -501,6 +514,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
         return launch_norm_quant(m->x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
       }));
+      PP_TRY(trace_codes(m, cs, l, 0, pos0, C, D));
       PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
       PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
         return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
@@ -511,15 +525,18 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
         return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, q16, m->as, cs);
       }));
+      PP_TRY(trace_codes(m, cs, l, 1, pos0, C, QD));
       PP_TRY(gemm(m, cs, EPI_RESID, mg, 1, L.so, L.wo, C, D, QD, m->x, D));
       // FFN block
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
         return launch_norm_quant(m->x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
       }));
+      PP_TRY(trace_codes(m, cs, l, 2, pos0, C, D));
       PP_TRY(gemm(m, cs, EPI_SWIGLU, mg, 2, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
         return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, q16, m->as, cs);
       }));
+      PP_TRY(trace_codes(m, cs, l, 3, pos0, C, F));
       PP_TRY(gemm(m, cs, EPI_RESID, mg, 3, L.sd, L.wd, C, D, F, m->x, D));
       if (c.mode == PP_MODE_STREAMED) PP_CUDA(cudaEventRecord(m->ring_free[visit % c.ring_slots], cs));
     }
@@ -694,14 +711,16 @@ int pp_reset_stats(pp_model* m) {
 
 int pp_model_gemm_engine(const pp_model* m) { return m ? m->engine : PP_ERR_ARG; }
 
-int pp_set_trace(pp_model* m, float* d_trace, int32_t max_pos) {
-  if (!m || (d_trace && max_pos <= 0)) {
+int pp_set_trace(pp_model* m, float* d_x, int8_t* d_codes, float* d_scales, int32_t max_pos) {
+  if (!m || (d_x && max_pos <= 0)) {
     set_err("bad pp_set_trace arguments");
     return PP_ERR_ARG;
   }
   PP_CUDA(cudaStreamSynchronize(m->stream));
-  m->trace = d_trace;
-  m->trace_pos = d_trace ? max_pos : 0;
+  m->trace = d_x;
+  m->trace_codes = d_x ? d_codes : nullptr;
+  m->trace_scales = d_x ? d_scales : nullptr;
+  m->trace_pos = d_x ? max_pos : 0;
   return PP_OK;
 }
 

@@ -13,7 +13,7 @@ import pytest
 import oracle
 import prompt_prefill_gb300 as pp
 import synth
-from tests.gpu_util import bits, load, logits_close, teacher_forced, torch_cuda
+from tests.gpu_util import bits, layerwise_forced, load, logits_close, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -159,7 +159,11 @@ def test_device_path_equals_host_path(tiny):
 
 
 # ------------------------------------------------------------------ 350M class
-def test_350m_teacher_forced_layers_and_logits():
+def _summary(report):
+    return [(sum(st["mismatches"]), max(st["max_margin"])) for st in report]
+
+
+def test_350m_layer_by_layer_and_logits():
     torch_cuda()
     c = synth.CONFIGS["350m"]
     m = synth.make_model(c)
@@ -167,11 +171,11 @@ def test_350m_teacher_forced_layers_and_logits():
     g = load(m, max_seq=c.max_seq, max_chunk=32)
     try:
         g.reset_stats()
-        got, ref, errs = teacher_forced(m, g, toks, 32)
+        got, ref, report = layerwise_forced(m, g, toks, 32)
         s = g.stats()
     finally:
         g.close()
-    print("350m per-layer max|d|, mean|d| (x std):", [f"{a:.1e}/{b:.1e}" for a, b in errs])
+    print("350m per-layer (tie decisions, max margin):", _summary(report))
     _assert_e2e(got, ref, "350m final")
     layer_w = c.layer_bytes() + 4 * (c.qkv_rows + c.dim + 2 * c.ffn + c.dim)
     assert s["weight_bytes_read"] == 24 * c.n_layers * layer_w + c.vocab * c.dim + 4 * c.vocab
@@ -210,11 +214,11 @@ def test_1b_second_call_continues_cache(one_b):
     assert np.array_equal(bits(second), bits(whole))
 
 
-def test_1b_teacher_forced_layers_and_logits(one_b):
+def test_1b_layer_by_layer_and_logits(one_b):
     m, g = one_b
     toks = synth.prompt(m.cfg, 256)
-    got, ref, errs = teacher_forced(m, g, toks, 128)
-    print("1b per-layer max|d|, mean|d| (x std):", [f"{a:.1e}/{b:.1e}" for a, b in errs])
+    got, ref, report = layerwise_forced(m, g, toks, 128)
+    print("1b per-layer (tie decisions, max margin):", _summary(report))
     _assert_e2e(got, ref, "1b final")
 
 

@@ -188,3 +188,55 @@ def test_layer_by_layer_composes_to_prefill(tiny_model):
         x = om.layer(L, x, 0)
     assert np.array_equal(x[-1], hidden)
     assert np.array_equal(_bits(om.final_logits(x[-1])), _bits(ref))
+
+
+def test_forced_layer_with_own_codes_is_the_layer():
+    # Forcing the oracle's layer with the codes it decides itself (obtained by
+    # composing the pinned steps) reports no disagreement and changes nothing.
+    m = _micro(seed=7)
+    toks = np.array([2, 9, 4, 4, 13, 1], np.int32)
+    c = m.cfg
+    n = len(toks)
+    x = m.tok_emb[toks].astype(np.float32)
+    W, S = m.w, m.w_scale
+    kmax = max(c.dim, c.n_heads * c.head_dim, c.ffn)
+    codes = np.zeros((4, n, kmax), np.int8)
+    scales = np.zeros((4, n), np.float32)
+    q8, a = oracle.quantize_rows(oracle.rmsnorm_rows(x, m.attn_norm[0], c.rms_eps))
+    codes[0, :, :c.dim], scales[0] = q8, a
+    Q = oracle.rope_rows(oracle.dequant_block(oracle.gemm_i8(q8, W[0]), S[0], a).reshape(n, c.n_heads, c.head_dim), 0,
+                         c.rope_theta)
+    K = oracle.rope_rows(oracle.dequant_block(oracle.gemm_i8(q8, W[1]), S[1], a).reshape(n, c.n_kv_heads, c.head_dim),
+                         0, c.rope_theta)
+    V = oracle.dequant_block(oracle.gemm_i8(q8, W[2]), S[2], a).reshape(n, c.n_kv_heads, c.head_dim)
+    q8, a = oracle.quantize_rows(oracle.attention(Q, K, V, 0).reshape(n, -1))
+    codes[1, :, :c.n_heads * c.head_dim], scales[1] = q8, a
+    x1 = x + oracle.dequant_block(oracle.gemm_i8(q8, W[3]), S[3], a)
+    q8, a = oracle.quantize_rows(oracle.rmsnorm_rows(x1, m.ffn_norm[0], c.rms_eps))
+    codes[2, :, :c.dim], scales[2] = q8, a
+    g = oracle.dequant_block(oracle.gemm_i8(q8, W[4]), S[4], a)
+    u = oracle.dequant_block(oracle.gemm_i8(q8, W[5]), S[5], a)
+    h = np.vectorize(lambda gg, uu: float(oracle.silu_mul(gg, uu)), otypes=[np.float32])(g, u)
+    q8, a = oracle.quantize_rows(h)
+    codes[3, :, :c.ffn], scales[3] = q8, a
+    om = oracle.OracleModel(m)
+    y, st = om.layer_forced(0, x, codes, scales, 0)
+    om.kv_reset()
+    assert st["mismatches"] == [0, 0, 0, 0] and st["scale_mismatches"] == [0, 0, 0, 0]
+    assert np.array_equal(y, om.layer(0, x, 0))
+
+
+def test_forced_layer_with_zero_codes_adds_nothing_and_counts_disagreements():
+    m = _micro(seed=8)
+    toks = np.array([5, 6, 7], np.int32)
+    c = m.cfg
+    x = m.tok_emb[toks].astype(np.float32)
+    kmax = max(c.dim, c.n_heads * c.head_dim, c.ffn)
+    y, st = oracle.OracleModel(m).layer_forced(0, x, np.zeros((4, 3, kmax), np.int8), np.zeros((4, 3), np.float32), 0)
+    # zero codes make every projection add exactly zero
+    assert np.array_equal(y, x)
+    own, _ = oracle.quantize_rows(oracle.rmsnorm_rows(x, m.attn_norm[0], c.rms_eps))
+    assert st["mismatches"][0] == int(np.count_nonzero(own))
+    own2, _ = oracle.quantize_rows(oracle.rmsnorm_rows(x, m.ffn_norm[0], c.rms_eps))
+    assert st["mismatches"][2] == int(np.count_nonzero(own2))
+    assert st["mismatches"][1] == 0 and st["mismatches"][3] == 0  # zero inputs quantise to zero
