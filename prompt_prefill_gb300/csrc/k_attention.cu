@@ -85,21 +85,28 @@ __global__ void __launch_bounds__(THREADS, 2)
       for (int e = 0; e < 4; ++e) O[a][i][e] = 0.f;
   }
 
-  for (int kb = 0; kb < nblocks; ++kb) {
-    const int key0 = kb * KB;
-    __syncthreads();  // previous block's P and V are consumed
+  // K/V tiles stream through shared memory with cp.async: K of block kb+1
+  // loads while P V of block kb runs, V of block kb+1 while S of block kb+1
+  // runs. Keys past the tile's last position are zero-filled.
+  auto load_tile = [&](float* dst, const float* src, int key0, bool swizzle) {
     for (int e = tid; e < KB * C4; e += THREADS) {
       const int j = e / C4, c = e % C4;
       const int kp = key0 + j;
-      float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
-      if (kp <= pmax) {
-        kv4 = *reinterpret_cast<const float4*>(kc + ((size_t)kp * Hkv + kvh) * HD + 4 * c);
-        vv4 = *reinterpret_cast<const float4*>(vc + ((size_t)kp * Hkv + kvh) * HD + 4 * c);
-      }
-      *reinterpret_cast<float4*>(&Ks[swz<HD>(j, 4 * c)]) = kv4;
-      *reinterpret_cast<float4*>(&Vs[j * HD + 4 * c]) = vv4;
+      const bool ok = kp <= pmax;
+      const float* g = src + ((size_t)(ok ? kp : 0) * Hkv + kvh) * HD + 4 * c;
+      float* d = swizzle ? &dst[swz<HD>(j, 4 * c)] : &dst[j * HD + 4 * c];
+      ppdev::cp_async16(d, g, ok ? 16 : 0);
     }
-    __syncthreads();
+    ppdev::cp_async_commit();
+  };
+  load_tile(Ks, kc, 0, true);
+  load_tile(Vs, vc, 0, false);
+  ppdev::cp_async_wait<1>();  // K of block 0
+  __syncthreads();
+
+  for (int kb = 0; kb < nblocks; ++kb) {
+    const int key0 = kb * KB;
+    const bool more = kb + 1 < nblocks;
 
     // S = Q K^T for rows ty+16a, keys tx+8b, in d order.
     float S[4][8];
@@ -124,6 +131,9 @@ __global__ void __launch_bounds__(THREADS, 2)
           S[a][b] = fmaf(qv[a].w, kv[b].w, S[a][b]);
         }
     }
+    __syncthreads();  // every warp is done with Ks
+    if (more) load_tile(Ks, kc, key0 + KB, true);
+    else ppdev::cp_async_commit();
 
     // Causal mask, online softmax (base 2), P -> smem.
 #pragma unroll
@@ -156,6 +166,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) O[a][i][e] *= alpha;
     }
+    ppdev::cp_async_wait<1>();  // V of this block (the K prefetch may still be in flight)
     __syncthreads();
 
     // O += P V, keys in order.
@@ -176,7 +187,13 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
       }
     }
+    __syncthreads();  // every warp is done with Vs and Ps
+    if (more) load_tile(Vs, vc, key0 + KB, false);
+    else ppdev::cp_async_commit();
+    ppdev::cp_async_wait<1>();  // K of the next block
+    __syncthreads();
   }
+  ppdev::cp_async_wait<0>();
 
   // o[i][h][:] = O / l
 #pragma unroll
