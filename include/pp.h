@@ -233,8 +233,9 @@ int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const 
                    int32_t n, int32_t k, int32_t* acc, void* stream);
 
 /* The same GEMM with its dequantising epilogue PP_EPI_* (f32, in the fixed
- * order (float(acc) * w_scale[r]) * a_scale[t]); out is f32 with leading
- * dimension ldo. */
+ * order (float(acc) * w_scale[r]) * a_scale[t]); out is f32, 16-byte aligned,
+ * with leading dimension ldo (a multiple of 4); PP_GEMM_TC also needs 16-byte
+ * aligned w_scale. */
 int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_t* a16, const int8_t* w,
                const float* w_scale, const float* a_scale, int32_t m, int32_t n, int32_t k, float* out,
                int32_t ldo, void* stream);

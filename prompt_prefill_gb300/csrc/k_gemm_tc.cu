@@ -22,7 +22,10 @@
 // 0x6400 | (b ^ 0x80) is the fp16 number 1024 + 128 + b, minus 1152 gives b).
 // Warp 0 issues TMA, warp 1 (leader CTA) issues the MMAs, warps 4-11 convert
 // and run the epilogue, each thread holding 128 int32 running sums (register
-// split by setmaxnreg). Persistent over tiles; two TMEM accumulators of 256 columns alternate
+// split by setmaxnreg). Converter warps never block on the MMA: they drain a
+// segment only once its accumulator is complete (polled between conversions)
+// and emit a finished tile's epilogue in chunks between the next tile's
+// conversions, so the stages ahead of the tensor core stay filled. Persistent over tiles; two TMEM accumulators of 256 columns alternate
 // between segments. Every mbarrier wait is bounded: on
 // expiry the kernel records a timeout in the status word and winds down.
 #include <cuda.h>
@@ -50,7 +53,9 @@ constexpr int CONV_WARP0 = 4;
 constexpr int REGS_ROLE = 40, REGS_CONV = 232;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_SEG_KB = 16;      // 16 x 64 = 1024 products per exact f32 segment
-constexpr int LAG = 2;              // k-blocks converted past a segment before draining it
+constexpr int MIN_SK_KB = 96;       // stream-K only when each cluster owns >= 96 k-blocks (measured: fixups
+                                    // cost more than they recover at ~40 k-blocks per cluster)
+constexpr int EPI_EVERY = 2;        // conversions between two epilogue chunks of a finished tile
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 
@@ -64,6 +69,35 @@ struct TcParams {
   int ldo;
   int32_t* acc_out;
   int* status;
+  // stream-K: cluster c owns iterations [c*ipc, (c+1)*ipc) of the (tile, k-block)
+  // space; partial tiles meet in `part` (int32 [tile][slot][cta][128][256]) and the
+  // last contributor, counted in `cnt` ([tile][cta], zero between launches), adds
+  // the partial sums and runs the epilogue. ipc == 0: whole tiles round robin.
+  int ipc;
+  int max_slots;
+  int32_t* part;
+  int* cnt;
+};
+
+// The units (tile, k-block range) a cluster works on, in order.
+struct Sched {
+  int cluster, n_clusters, num_tiles, nkb, ipc, it0, it1;
+  __device__ Sched(const TcParams& p, int c, int nc) : cluster(c), n_clusters(nc), num_tiles(p.num_tiles),
+      nkb(p.K / BK), ipc(p.ipc) {
+    const long long total = (long long)num_tiles * nkb;
+    it0 = ipc ? (int)min((long long)c * ipc, total) : 0;
+    it1 = ipc ? (int)min((long long)(c + 1) * ipc, total) : 0;
+  }
+  __device__ int units() const {
+    if (!ipc) return num_tiles > cluster ? (num_tiles - cluster + n_clusters - 1) / n_clusters : 0;
+    return it1 > it0 ? (it1 - 1) / nkb - it0 / nkb + 1 : 0;
+  }
+  __device__ void unit(int u, int& tile, int& kb0, int& kb1) const {
+    if (!ipc) { tile = cluster + u * n_clusters; kb0 = 0; kb1 = nkb; return; }
+    tile = it0 / nkb + u;
+    kb0 = u == 0 ? it0 % nkb : 0;
+    kb1 = tile == (it1 - 1) / nkb ? (it1 - 1) % nkb + 1 : nkb;
+  }
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -98,6 +132,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
       : "r"(a), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// Non-blocking test of a barrier phase (lane 0 tests, the warp agrees).
+__device__ __forceinline__ bool mbar_test_warp(uint32_t a, uint32_t parity) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0)
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 // Bounded wait: false after ~2 s without the phase completing.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
@@ -197,7 +243,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t rank = cta_rank();
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   const int nkb = p.K / BK;
-  const int nseg = (nkb + p.seg_kb - 1) / p.seg_kb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -211,6 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     mbar_init(done_b, 1);
     *abort_flag = 0;
+    abort_flag[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -236,10 +282,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       int issued[STAGES] = {0};
-      for (int t = cluster; t < p.num_tiles && !*abort_flag; t += n_clusters) {
+      const Sched sc(p, cluster, n_clusters);
+      for (int u = 0; u < sc.units() && !*abort_flag; ++u) {
+        int t, kb0, kb1;
+        sc.unit(u, t, kb0, kb1);
         const int m_row = (t % p.num_m_tiles) * 2 * BM + (int)rank * BM;
         const int n_row = (t / p.num_m_tiles) * BN + (int)rank * (BN / 2);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_b(s), ph ^ 1)) { fail(); break; }
           mbar_expect_tx(full_b(s), A_BYTES + W_BYTES);
           tma_load_2d(sA(s), &tmA, kb * BK, m_row, full_b(s));
@@ -266,13 +315,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t ph = 0;
       int g = 0;
       bool ok = true;
-      for (int t = cluster; t < p.num_tiles && ok; t += n_clusters) {
-        for (int seg = 0; seg < nseg && ok; ++seg, ++g) {
+      const Sched sc(p, cluster, n_clusters);
+      for (int u = 0; u < sc.units() && ok; ++u) {
+        int t, ukb0, ukb1;
+        sc.unit(u, t, ukb0, ukb1);
+        for (int seg_k0 = ukb0; seg_k0 < ukb1 && ok; seg_k0 += p.seg_kb, ++g) {
           const int buf = g & 1;
           if (!mbar_wait(acce_b(buf), ((g >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + buf * 256;
-          const int kb0 = seg * p.seg_kb, kb1 = min(nkb, kb0 + p.seg_kb);
+          const int kb0 = seg_k0, kb1 = min(ukb1, seg_k0 + p.seg_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(ready_b(s), ph)) { fail(); ok = false; break; }
             tc_fence_after();
@@ -304,22 +356,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int32_t run[128];
     int s = 0;
     uint32_t ph = 0;
-    int done_kb = 0;      // k-blocks converted so far (all tiles)
-    int next_seg = 0;     // next segment to drain (all tiles)
-    const int my_tiles = p.num_tiles > cluster ? (p.num_tiles - cluster + n_clusters - 1) / n_clusters : 0;
-    const int total_segs = my_tiles * nseg;
-    bool ok = true;
+    int done_kb = 0;      // k-blocks converted so far (all units)
+    int next_seg = 0;     // segments drained so far (all units; selects the accumulator buffer)
+    const Sched sc(p, cluster, n_clusters);
+    const int n_units = sc.units();
+    int total_kb = 0;
+    for (int u = 0; u < n_units; ++u) {
+      int t, a, b;
+      sc.unit(u, t, a, b);
+      total_kb += b - a;
+    }
+    // drain cursor: segment dseg of unit du, whose k-blocks start at conversion index dbase
+    int du = 0, dseg = 0, dbase = 0, dtile = 0, dkb0 = 0, dkb1 = 0;
+    if (n_units > 0) sc.unit(0, dtile, dkb0, dkb1);
+    volatile int* last_flag = abort_flag + 1;
 
-    auto seg_last_kb = [&](int g) {  // global index of the last k-block of segment g
-      const int it = g / nseg, seg = g % nseg;
-      return it * nkb + min(nkb, (seg + 1) * p.seg_kb) - 1;
-    };
-    auto drain = [&](int g) -> bool {
+    // Fold segment g's complete f32 accumulator into the int32 running sums.
+    auto drain = [&](int g, bool first) {  // `first`: the unit's first segment starts the running sums
       const int buf = g & 1;
-      if (!mbar_wait(accf_b(buf), (g >> 1) & 1)) { fail(); return false; }
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * 256 + colq * 128;
-      const bool first = g % nseg == 0;  // a tile's first segment starts the running sums
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t r[16];
@@ -333,63 +389,120 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce_b(buf), 0);
-      if (g % nseg != nseg - 1) return true;
-      // last segment of a tile: dequantise and store
-      const int t = cluster + (g / nseg) * n_clusters;
-      const int row = (t % p.num_m_tiles) * 2 * BM + (int)rank * BM + quarter * 32 + lane;
-      const int n0 = (t / p.num_m_tiles) * BN + colq * 128;
-      if (row < p.M) {
-        if (EPI == EPI_ACC) {
-          int4* dst = reinterpret_cast<int4*>(p.acc_out + (size_t)row * p.N + n0);
+    };
+
+    // Stream-K: this CTA's partial sums of `tile` meet the other contributors'.
+    // Returns true for the last contributor, whose run[] then holds the totals.
+    auto finish_partial = [&](int tile) -> bool {
+      const int c_first = (int)(((long long)tile * nkb) / p.ipc);
+      const int c_last = (int)((((long long)tile + 1) * nkb - 1) / p.ipc);
+      const int n_contrib = c_last - c_first + 1;
+      const int row = quarter * 32 + lane;
+      auto slot_ptr = [&](int slot) {
+        return p.part + ((((size_t)tile * p.max_slots + slot) * 2 + rank) * BM + row) * BN + colq * 128;
+      };
+      int4* mine = reinterpret_cast<int4*>(slot_ptr(cluster - c_first));
 #pragma unroll
-          for (int j = 0; j < 32; ++j) dst[j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
-        } else {
-          const float a_s = p.as[row];
-          if (EPI == EPI_SWIGLU) {
-            float* dst = p.out + (size_t)row * p.ldo + n0 / 2;
+      for (int j = 0; j < 32; ++j) mine[j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_CONV_WARPS) : "memory");
+      if (et == 0) *last_flag = atomicAdd(p.cnt + 2 * tile + rank, 1) == n_contrib - 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_CONV_WARPS) : "memory");
+      if (!*last_flag) return false;
+      __threadfence();
+      for (int sl = 0; sl < n_contrib; ++sl) {
+        if (sl == cluster - c_first) continue;
+        const int4* other = reinterpret_cast<const int4*>(slot_ptr(sl));
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {  // 32 columns = 16 gate rows then their 16 up rows
-#pragma unroll
-              for (int i = 0; i < 16; i += 4) {
-                float h[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int cg = 32 * b + i + e;
-                  const float gv = ppdev::dequant(run[cg], __ldg(p.ws + n0 + cg), a_s);
-                  const float uv = ppdev::dequant(run[cg + 16], __ldg(p.ws + n0 + cg + 16), a_s);
-                  h[e] = ppdev::silu_mul(gv, uv);
-                }
-                *reinterpret_cast<float4*>(dst + 16 * b + i) = make_float4(h[0], h[1], h[2], h[3]);
-              }
-              asm volatile("" ::: "memory");  // keep each group's loads next to their use
-            }
-          } else {
-            float* dst = p.out + (size_t)row * p.ldo + n0;
-#pragma unroll
-            for (int j = 0; j < 128; j += 4) {
-              float v[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) v[e] = ppdev::dequant(run[j + e], __ldg(p.ws + n0 + j + e), a_s);
-              if (EPI == EPI_RESID) {
-                const float4 r0 = *reinterpret_cast<const float4*>(dst + j);
-                v[0] = __fadd_rn(r0.x, v[0]);
-                v[1] = __fadd_rn(r0.y, v[1]);
-                v[2] = __fadd_rn(r0.z, v[2]);
-                v[3] = __fadd_rn(r0.w, v[3]);
-              }
-              *reinterpret_cast<float4*>(dst + j) = make_float4(v[0], v[1], v[2], v[3]);
-              if ((j & 15) == 12) asm volatile("" ::: "memory");  // groups of 16 columns
-            }
-          }
+        for (int j = 0; j < 32; ++j) {
+          const int4 v = __ldcg(other + j);
+          run[4 * j] += v.x;
+          run[4 * j + 1] += v.y;
+          run[4 * j + 2] += v.z;
+          run[4 * j + 3] += v.w;
         }
       }
+      if (et == 0) p.cnt[2 * tile + rank] = 0;  // ready for the next launch
       return true;
     };
 
-    const int total_kb = my_tiles * nkb;
-    while (ok) {
-      if (done_kb < total_kb) {
-        if (*abort_flag || !mbar_wait(full_b(s), ph)) { fail(); break; }
+    // Epilogue of a finished tile in chunks of 16 output columns (32 accumulator
+    // columns for SwiGLU): (float(acc) * w_scale) * a_scale, then store,
+    // residual add or SwiGLU. Rows past M are skipped.
+    int epi_left = 0, epi_row0 = 0, epi_n0 = 0;
+    constexpr int EPI_CHUNKS = EPI == EPI_SWIGLU ? 4 : 8;
+    auto epi_chunk = [&](int c) {
+      const int row = epi_row0 + lane;
+      if (row >= p.M) return;
+      if (EPI == EPI_ACC) {
+        int4* dst = reinterpret_cast<int4*>(p.acc_out + (size_t)row * p.N + epi_n0 + 16 * c);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          dst[k] = make_int4(run[16 * c + 4 * k], run[16 * c + 4 * k + 1], run[16 * c + 4 * k + 2], run[16 * c + 4 * k + 3]);
+        return;
+      }
+      const float a_s = p.as[row];
+      float v[16];
+      if (EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int cg = 32 * c + i;
+          v[i] = ppdev::silu_mul(ppdev::dequant(run[cg], __ldg(p.ws + epi_n0 + cg), a_s),
+                                 ppdev::dequant(run[cg + 16], __ldg(p.ws + epi_n0 + cg + 16), a_s));
+        }
+        float4* dst = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + epi_n0 / 2 + 16 * c);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = ppdev::dequant(run[16 * c + i], __ldg(p.ws + epi_n0 + 16 * c + i), a_s);
+        float4* dst = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + epi_n0 + 16 * c);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          if (EPI == EPI_RESID) {
+            const float4 x = dst[k];
+            o = make_float4(__fadd_rn(x.x, o.x), __fadd_rn(x.y, o.y), __fadd_rn(x.z, o.z), __fadd_rn(x.w, o.w));
+          }
+          dst[k] = o;
+        }
+      }
+    };
+    auto epi_next = [&]() {  // the next pending chunk (each branch has compile-time indices)
+      const int c = EPI_CHUNKS - epi_left;
+#pragma unroll
+      for (int k = 0; k < EPI_CHUNKS; ++k)
+        if (k == c) epi_chunk(k);
+      --epi_left;
+    };
+
+    int since_epi = 0;
+    long long idle_since = clock64();
+    while (true) {
+      bool progressed = false;
+      const bool seg_done = du < n_units && dbase + min(dkb1 - dkb0, (dseg + 1) * p.seg_kb) - 1 < done_kb &&
+                            mbar_test_warp(accf_b(next_seg & 1), (next_seg >> 1) & 1);
+      if (seg_done && epi_left == 0) {
+        drain(next_seg++, dseg == 0);
+        ++dseg;
+        if (dkb0 + dseg * p.seg_kb >= dkb1) {  // the unit is complete
+          const bool whole = dkb0 == 0 && dkb1 == nkb;
+          if (whole || finish_partial(dtile)) {  // queue the tile's epilogue
+            epi_row0 = (dtile % p.num_m_tiles) * 2 * BM + (int)rank * BM + quarter * 32;
+            epi_n0 = (dtile / p.num_m_tiles) * BN + colq * 128;
+            epi_left = EPI_CHUNKS;
+            since_epi = EPI_EVERY;
+          }
+          dbase += dkb1 - dkb0;
+          dseg = 0;
+          if (++du < n_units) sc.unit(du, dtile, dkb0, dkb1);
+        }
+        progressed = true;
+      } else if (epi_left > 0 && (seg_done || since_epi >= EPI_EVERY || done_kb == total_kb)) {
+        epi_next();  // a finished tile's sums must be written before the next drain reuses them
+        since_epi = 0;
+        progressed = true;
+      } else if (done_kb < total_kb && mbar_test_warp(full_b(s), ph)) {
         // widen this CTA's 128 weight rows x 64 k of int8 to fp16, UMMA layout
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -410,13 +523,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive_cluster(ready_b(s), 0);
         if (++s == STAGES) { s = 0; ph ^= 1; }
         ++done_kb;
+        ++since_epi;
+        progressed = true;
       }
-      // drain every segment whose last k-block is LAG k-blocks behind (all, at the end)
-      if (next_seg < total_segs && (done_kb == total_kb || seg_last_kb(next_seg) + LAG < done_kb)) {
-        ok = drain(next_seg++);
-        continue;
+      if (done_kb == total_kb && du == n_units && epi_left == 0) break;
+      if (progressed) {
+        idle_since = clock64();
+      } else {
+        if (*abort_flag || clock64() - idle_since > WAIT_CYCLES) { fail(); break; }
+        __nanosleep(20);
       }
-      if (done_kb == total_kb && next_seg == total_segs) break;
     }
   }
 
@@ -471,14 +587,13 @@ int max_clusters() {
 }
 
 template <int EPI>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int clusters = std::min(p.num_tiles, max_clusters());
   k_gemm_tc<EPI><<<2 * clusters, THREADS, SMEM_BYTES, s>>>(ma, mw, p);
   return cudaGetLastError();
 }
@@ -519,27 +634,76 @@ cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+
+// Stream-K plan of one GEMM (ipc == 0: whole tiles round robin).
+struct Plan {
+  int num_tiles, clusters, ipc, max_slots;
+  size_t part_elems;
+};
+
+Plan plan(int m, int n, int k) {
+  Plan pl{};
+  const int nmt = (m + 2 * BM - 1) / (2 * BM);
+  const int nkb = k / BK;
+  pl.num_tiles = nmt * (n / BN);
+  const int mc = max_clusters();
+  if (pl.num_tiles >= 2 * mc || pl.num_tiles * nkb < 2 * mc) {
+    pl.clusters = std::min(pl.num_tiles, mc);
+    return pl;
+  }
+  const long long total = (long long)pl.num_tiles * nkb;
+  pl.ipc = std::max((int)((total + mc - 1) / mc), MAX_SEG_KB);  // at least one exact segment per cluster
+  if (pl.ipc < MIN_SK_KB) {  // too little work per cluster to amortise a partial-tile fixup
+    pl.ipc = 0;
+    pl.clusters = std::min(pl.num_tiles, mc);
+    return pl;
+  }
+  pl.clusters = (int)((total + pl.ipc - 1) / pl.ipc);
+  pl.max_slots = (nkb + pl.ipc - 1) / pl.ipc + 1;
+  pl.part_elems = (size_t)pl.num_tiles * pl.max_slots * 2 * BM * BN;
+  return pl;
+}
+
+}  // namespace
+
+void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters) {
+  const Plan pl = plan(m, n, k);
+  *part_bytes = pl.part_elems * sizeof(int32_t);
+  *counters = pl.ipc ? (size_t)pl.num_tiles * 2 : 0;
+}
+
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, const float* ws, const float* as,
                            int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k, int* status,
-                           cudaStream_t s) {
-  TcParams p;
+                           const TcWorkspace& wsp, cudaStream_t s) {
+  TcParams p{};
   p.M = m;
   p.N = n;
   p.K = k;
   p.seg_kb = std::max(1, std::min(MAX_SEG_KB, seg_k / BK));
   p.num_m_tiles = (m + 2 * BM - 1) / (2 * BM);
-  p.num_tiles = p.num_m_tiles * (n / BN);
   p.ws = ws;
   p.as = as;
   p.out = out;
   p.ldo = ldo;
   p.acc_out = acc;
   p.status = status;
+  Plan pl = plan(m, n, k);
+  p.num_tiles = pl.num_tiles;
+  if (pl.ipc && wsp.part && wsp.cnt && wsp.part_bytes >= pl.part_elems * sizeof(int32_t) &&
+      wsp.counters >= (size_t)pl.num_tiles * 2) {
+    p.ipc = pl.ipc;
+    p.max_slots = pl.max_slots;
+    p.part = wsp.part;
+    p.cnt = wsp.cnt;
+  } else {
+    pl.clusters = std::min(pl.num_tiles, max_clusters());  // no workspace: whole tiles
+  }
   switch (epi) {
-    case EPI_STORE: return launch_t<EPI_STORE>(ma, mw, p, s);
-    case EPI_RESID: return launch_t<EPI_RESID>(ma, mw, p, s);
-    case EPI_SWIGLU: return launch_t<EPI_SWIGLU>(ma, mw, p, s);
-    case EPI_ACC: return launch_t<EPI_ACC>(ma, mw, p, s);
+    case EPI_STORE: return launch_t<EPI_STORE>(ma, mw, p, pl.clusters, s);
+    case EPI_RESID: return launch_t<EPI_RESID>(ma, mw, p, pl.clusters, s);
+    case EPI_SWIGLU: return launch_t<EPI_SWIGLU>(ma, mw, p, pl.clusters, s);
+    case EPI_ACC: return launch_t<EPI_ACC>(ma, mw, p, pl.clusters, s);
     default: return cudaErrorInvalidValue;
   }
 }

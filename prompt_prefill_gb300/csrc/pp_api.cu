@@ -174,6 +174,7 @@ struct pp_model {
   // buffer viewed with each GEMM's k (dim, n_heads*head_dim, ffn)
   std::vector<CUtensorMap> wmap;
   CUtensorMap amap_d{}, amap_qd{}, amap_f{};
+  TcWorkspace tcws;  // stream-K partial tiles and counters of the projection GEMMs
   // stats and timing
   pp_stats stats{};
   std::vector<cudaEvent_t> ev_pool;
@@ -253,7 +254,8 @@ int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* 
     const CUtensorMap& wm = m->wmap[(size_t)mg * 4 + which];
     const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
     return launch(m, PP_KERNEL_GEMM, st, [&] {
-      return launch_gemm_tc(epi, am, wm, ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, st);
+      return launch_gemm_tc(epi, am, wm, ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
+                            st);
     });
   }
   return launch(m, PP_KERNEL_GEMM, st, [&] {
@@ -354,6 +356,23 @@ int load_impl(pp_model* m, const pp_weights* w) {
   PP_CUDA(cudaMemsetAsync(m->status, 0, sizeof(int), m->stream));
   PP_CUDA(cudaMemsetAsync(m->a16, 0, MC * KMAX * sizeof(__half), m->stream));
   if (m->engine == PP_GEMM_TC) {
+    // stream-K workspace: the largest need over every chunk-row count and projection
+    size_t part = 0, cnt = 0;
+    const int shapes[4][2] = {{(int)QKV, (int)D}, {(int)D, (int)QD}, {(int)(2 * F), (int)D}, {(int)D, (int)F}};
+    for (size_t rows = 256; rows < MC + 256; rows += 256)
+      for (auto& sh : shapes) {
+        size_t pb = 0, cc = 0;
+        tc_workspace_need((int)std::min(rows, MC), sh[0], sh[1], &pb, &cc);
+        part = std::max(part, pb);
+        cnt = std::max(cnt, cc);
+      }
+    if (part) {
+      PP_TRY(dalloc(m, &m->tcws.part, part / sizeof(int32_t)));
+      PP_TRY(dalloc(m, &m->tcws.cnt, cnt));
+      PP_CUDA(cudaMemsetAsync(m->tcws.cnt, 0, cnt * sizeof(int), m->stream));
+      m->tcws.part_bytes = part;
+      m->tcws.counters = cnt;
+    }
     PP_CUDA(make_tmap_a(&m->amap_d, m->a16, (int)MC, (int)D));
     PP_CUDA(make_tmap_a(&m->amap_qd, m->a16, (int)MC, (int)QD));
     PP_CUDA(make_tmap_a(&m->amap_f, m->a16, (int)MC, (int)F));
@@ -662,7 +681,11 @@ int pp_device_status(pp_model* m) {
   PP_CUDA(cudaMemcpy(&s, m->status, sizeof(int), cudaMemcpyDeviceToHost));
   if (s != DEV_OK) PP_CUDA(cudaMemset(m->status, 0, sizeof(int)));
   if (s == DEV_BAD_TOKEN) { set_err("a token id outside [0, vocab) reached the device"); return PP_ERR_ARG; }
-  if (s == DEV_TIMEOUT) { set_err("a bounded device wait gave up"); return PP_ERR_DEVICE_TIMEOUT; }
+  if (s == DEV_TIMEOUT) {
+    if (m->tcws.cnt) cudaMemset(m->tcws.cnt, 0, m->tcws.counters * sizeof(int));
+    set_err("a bounded device wait gave up");
+    return PP_ERR_DEVICE_TIMEOUT;
+  }
   return PP_OK;
 }
 
@@ -783,6 +806,33 @@ static int check_gemm(int32_t engine, const int8_t* a8, const uint16_t* a16, con
 }
 
 
+// Process-wide stream-K workspace of the single-step GEMM entry points, grown
+// on demand (growing synchronises the device) and kept until exit.
+static std::mutex g_op_ws_mu;
+static TcWorkspace g_op_ws;
+
+static cudaError_t op_workspace(int m, int n, int k, TcWorkspace* out) {
+  size_t part = 0, cnt = 0;
+  tc_workspace_need(m, n, k, &part, &cnt);
+  std::lock_guard<std::mutex> lk(g_op_ws_mu);
+  if (part > g_op_ws.part_bytes || cnt > g_op_ws.counters) {
+    if (g_op_ws.part) cudaFree(g_op_ws.part);
+    if (g_op_ws.cnt) cudaFree(g_op_ws.cnt);
+    g_op_ws = TcWorkspace{};
+    const size_t pb = std::max(part, (size_t)256), cc = std::max(cnt, (size_t)64);
+    cudaError_t e = cudaMalloc(&g_op_ws.part, pb);
+    if (e != cudaSuccess) return e;
+    e = cudaMalloc(&g_op_ws.cnt, cc * sizeof(int));
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(g_op_ws.cnt, 0, cc * sizeof(int));
+    if (e != cudaSuccess) return e;
+    g_op_ws.part_bytes = pb;
+    g_op_ws.counters = cc;
+  }
+  *out = g_op_ws;
+  return cudaSuccess;
+}
+
 static cudaError_t op_gemm_launch(int32_t engine, int epi, const int8_t* a8, const uint16_t* a16, const int8_t* w,
                                   const float* ws, const float* as, int m, int n, int k, float* out, int ldo,
                                   int32_t* acc, cudaStream_t st) {
@@ -792,7 +842,10 @@ static cudaError_t op_gemm_launch(int32_t engine, int epi, const int8_t* a8, con
   if (e != cudaSuccess) return e;
   e = make_tmap_w(&mw, w, n, k);
   if (e != cudaSuccess) return e;
-  return launch_gemm_tc(epi, ma, mw, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), nullptr, st);
+  TcWorkspace wsp;
+  e = op_workspace(m, n, k, &wsp);
+  if (e != cudaSuccess) return e;
+  return launch_gemm_tc(epi, ma, mw, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), nullptr, wsp, st);
 }
 
 int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
@@ -808,6 +861,10 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
                const float* w_scale, const float* a_scale, int32_t m, int32_t n, int32_t k, float* out, int32_t ldo,
                void* stream) {
   PP_TRY(check_gemm(engine, a8, a16, w, m, n, k));
+  if (engine == PP_GEMM_TC && (reinterpret_cast<uintptr_t>(w_scale) & 15)) {
+    set_err("the tcgen05 engine needs 16-byte aligned row scales");
+    return PP_ERR_ARG;
+  }
   const int out_cols = epilogue == PP_EPI_SWIGLU ? n / 2 : n;
   if (!w_scale || !a_scale || !out || ldo < out_cols || (epilogue < PP_EPI_STORE || epilogue > PP_EPI_SWIGLU) ||
       ldo % 4 || (reinterpret_cast<uintptr_t>(out) & 15)) {

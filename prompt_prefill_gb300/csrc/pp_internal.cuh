@@ -40,9 +40,18 @@ cudaError_t launch_gemm_mma(int epi, const int8_t* a8, const int8_t* w, const fl
 bool tc_available();
 cudaError_t make_tmap_a(CUtensorMap* map, const __half* a16, int rows, int k);
 cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k);
+// Stream-K workspace: int32 partial tiles and per-tile counters (zero between launches).
+struct TcWorkspace {
+  int32_t* part = nullptr;
+  size_t part_bytes = 0;
+  int* cnt = nullptr;
+  size_t counters = 0;
+};
+// Workspace a GEMM of this shape uses (0 when it runs whole tiles).
+void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters);
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, const float* ws, const float* as,
                            int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k, int* status,
-                           cudaStream_t s);
+                           const TcWorkspace& wsp, cudaStream_t s);
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)
@@ -93,6 +102,8 @@ __device__ __forceinline__ float dequant(int32_t acc, float ws, float as) {
   return __fmul_rn(__fmul_rn(__int2float_rn(acc), ws), as);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// SwiGLU gate: silu(g) * u = g / (1 + exp(-g)) * u with the fast exponential and
+// division (a few ulp; g < -87 gives exp(-g) = inf and a zero result).
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 }  // namespace ppdev

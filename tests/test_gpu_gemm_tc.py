@@ -120,7 +120,7 @@ def test_tc_swiglu(torch):
     g = oracle.dequant_block(oracle.gemm_i8(a, wg), sg, as_)
     u = oracle.dequant_block(oracle.gemm_i8(a, wu), su, as_)
     ref = np.vectorize(lambda x, y: float(oracle.silu_mul(x, y)), otypes=[np.float32])(g, u)
-    assert np.abs(got.astype(np.float64) - ref).max() <= 2e-6 * max(1.0, np.abs(ref).max())
+    assert np.abs(got.astype(np.float64) - ref).max() <= 4e-6 * max(1.0, np.abs(ref).max())  # fast exp/div
     assert np.array_equal(bits(got), bits(host(out_mma)))  # same epilogue code, same integers
 
 
