@@ -53,7 +53,7 @@ constexpr int CONV_WARP0 = 4;
 constexpr int REGS_ROLE = 40, REGS_CONV = 232;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_SEG_KB = 16;      // 16 x 64 = 1024 products per exact f32 segment
-constexpr int MIN_SK_KB = 96;       // stream-K only when each cluster owns >= 96 k-blocks (measured: fixups
+constexpr int MIN_SK_KB = 64;       // stream-K only when each cluster owns >= 64 k-blocks (measured: fixups
                                     // cost more than they recover at ~40 k-blocks per cluster)
 constexpr int EPI_EVERY = 2;        // conversions between two epilogue chunks of a finished tile
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
