@@ -246,6 +246,28 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
  * shorter segments only add drains. Errors: PP_ERR_ARG out of range. */
 int pp_set_exact_segment(int32_t seg_k);
 
+/* The tcgen05 GEMM of pp_op_gemm (engine PP_GEMM_TC) without any device
+ * allocation, for callers that may not allocate device memory while they run
+ * (an application whose device memory is all held by its own pool allocator,
+ * or a latency-critical loop where cudaMalloc/cudaFree would block or
+ * synchronise the device). The pages have no counterpart: it only changes
+ * where the GEMM's stream-K scratch lives.
+ * The scratch (partial int32 tiles of GEMMs with few output tiles and long K,
+ * and their arrival counters) is a fixed array inside the library: 32 MiB plus
+ * 4096 counters, placed on every device that loads the library's device code
+ * and kept until the process exits. Shapes whose plan needs more fail with
+ * PP_ERR_ARG and a message naming both sizes (e.g. m = 1024, n = 4096,
+ * k = 14336); shapes that need no scratch always run.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * All calls on a device share its one array, which keeps the last call's
+ * contents (the counters are cleared on `stream` at the start of every call):
+ * calls on the same device whose executions overlap, for example on two
+ * streams, race and give wrong results. Arguments and errors as pp_op_gemm,
+ * with a16, w and w_scale 16-byte aligned. */
+int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, const float* w_scale,
+                       const float* a_scale, int32_t m, int32_t n, int32_t k, float* out, int32_t ldo, void* stream);
+
 /* RoPE + K/V write for `rows` positions start_pos..: qkv [rows][(H+2Hkv)*hd]
  * f32 (q heads, then k heads, then v heads) -> q_out [rows][H][hd] rotated,
  * k rotated into k_cache[start_pos+i], v copied into v_cache[start_pos+i]

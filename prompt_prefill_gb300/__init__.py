@@ -82,6 +82,7 @@ SIGNATURES = {
     "pp_op_gemm_acc": ([_i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp], ctypes.c_int),
     "pp_op_gemm": ([_i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp], ctypes.c_int),
     "pp_set_exact_segment": ([_i32], ctypes.c_int),
+    "pp_op_gemm_noalloc": ([_i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp], ctypes.c_int),
     "pp_op_rope_kv": ([_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "pp_op_rope_table": ([_i32, _i32, _f32, _vp, _vp], ctypes.c_int),
     "pp_op_attention": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp], ctypes.c_int),
@@ -262,6 +263,13 @@ def pp_op_gemm_acc(engine, a8, a16, w, m, n, k, acc, stream=None):
 def pp_op_gemm(engine, epilogue, a8, a16, w, w_scale, a_scale, m, n, k, out, ldo, stream=None):
     _check(lib().pp_op_gemm(engine, epilogue, _ptr(a8), _ptr(a16), _ptr(w), _ptr(w_scale), _ptr(a_scale), m, n, k,
                             _ptr(out), ldo, _stream(stream)), "pp_op_gemm")
+
+
+def pp_op_gemm_noalloc(epilogue, a16, w, w_scale, a_scale, m, n, k, out, ldo, stream=None):
+    """pp_op_gemm on the tcgen05 engine with no device allocation (fixed scratch
+    inside the library; see include/pp.h for the size limit and sharing rules)."""
+    _check(lib().pp_op_gemm_noalloc(epilogue, _ptr(a16), _ptr(w), _ptr(w_scale), _ptr(a_scale), m, n, k, _ptr(out),
+                                    ldo, _stream(stream)), "pp_op_gemm_noalloc")
 
 
 def pp_set_exact_segment(seg_k: int):

@@ -876,6 +876,86 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
                    "gemm");
 }
 
+// ---------------------------------------------------------------------------
+// The GEMM with its stream-K scratch in this library's own device memory, for
+// callers that may not allocate device memory while they run: for example a
+// host application that has already handed all device memory to its own pool
+// allocator, or a latency-critical loop where cudaMalloc/cudaFree would block
+// or synchronise the device. The scratch is a fixed array that the CUDA runtime
+// places on each device when the library's device code is loaded there; it
+// stays allocated until the process exits.
+namespace {
+constexpr size_t kStaticPartBytes = size_t(32) << 20;  // partial int32 tiles
+constexpr int kStaticCounters = 4096;                   // per-tile arrival counters
+static __device__ __align__(256) int32_t g_static_part[kStaticPartBytes / sizeof(int32_t)];
+static __device__ __align__(256) int g_static_cnt[kStaticCounters];
+
+struct StaticScratch {
+  bool ready = false;
+  int32_t* part = nullptr;
+  int* cnt = nullptr;
+};
+std::mutex g_static_mu;
+StaticScratch g_static_dev[128];  // by device ordinal
+
+// Device addresses of the static arrays on the current device, looked up once.
+int static_scratch(StaticScratch* out) {
+  int dev = 0;
+  PP_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 128) {
+    set_err("device ordinal %d out of range", dev);
+    return PP_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticScratch& sc = g_static_dev[dev];
+  if (!sc.ready) {
+    void* part = nullptr;
+    void* cnt = nullptr;
+    PP_CUDA(cudaGetSymbolAddress(&part, g_static_part));
+    PP_CUDA(cudaGetSymbolAddress(&cnt, g_static_cnt));
+    sc.part = static_cast<int32_t*>(part);
+    sc.cnt = static_cast<int*>(cnt);
+    sc.ready = true;
+  }
+  *out = sc;
+  return PP_OK;
+}
+}  // namespace
+
+int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, const float* w_scale,
+                       const float* a_scale, int32_t m, int32_t n, int32_t k, float* out, int32_t ldo, void* stream) {
+  PP_TRY(check_gemm(PP_GEMM_TC, nullptr, a16, w, m, n, k));
+  const int out_cols = epilogue == PP_EPI_SWIGLU ? n / 2 : n;
+  if (!w_scale || !a_scale || !out || ldo < out_cols || (epilogue < PP_EPI_STORE || epilogue > PP_EPI_SWIGLU) ||
+      ldo % 4 || (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(w_scale) & 15)) {
+    set_err("bad pp_op_gemm_noalloc arguments");
+    return PP_ERR_ARG;
+  }
+  size_t need_part = 0, need_cnt = 0;
+  tc_workspace_need(m, n, k, &need_part, &need_cnt);
+  if (need_part > kStaticPartBytes || need_cnt > (size_t)kStaticCounters) {
+    set_err("GEMM m=%d n=%d k=%d needs %zu bytes of scratch and %zu counters; the fixed scratch holds %zu bytes and %d",
+            m, n, k, need_part, need_cnt, kStaticPartBytes, kStaticCounters);
+    return PP_ERR_ARG;
+  }
+  StaticScratch sc;
+  PP_TRY(static_scratch(&sc));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: counters must start at zero
+  if (need_cnt) PP_CUDA(cudaMemsetAsync(sc.cnt, 0, need_cnt * sizeof(int), st));
+  CUtensorMap ma, mw;
+  PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
+  PP_CUDA(make_tmap_w(&mw, w, n, k));
+  TcWorkspace wsp;
+  wsp.part = sc.part;
+  wsp.part_bytes = kStaticPartBytes;
+  wsp.cnt = sc.cnt;
+  wsp.counters = kStaticCounters;
+  return ok_launch(launch_gemm_tc(epilogue, ma, mw, w_scale, a_scale, m, n, k, out, ldo, nullptr, g_tc_seg.load(),
+                                  nullptr, wsp, st),
+                   "gemm_noalloc");
+}
+
 int pp_set_exact_segment(int32_t seg_k) {
   if (seg_k < 64 || seg_k > kTcSegK || seg_k % 64) {
     set_err("exact segment must be a multiple of 64 in [64, %d]", kTcSegK);
