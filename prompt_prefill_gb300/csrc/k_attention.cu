@@ -178,12 +178,18 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int i = 0; i < ND; ++i) {
         const float4 v = *reinterpret_cast<const float4*>(&Vs[j * HD + 4 * tx + 32 * i]);
+        const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-          O[a][i][0] = fmaf(p[a], v.x, O[a][i][0]);
-          O[a][i][1] = fmaf(p[a], v.y, O[a][i][1]);
-          O[a][i][2] = fmaf(p[a], v.z, O[a][i][2]);
-          O[a][i][3] = fmaf(p[a], v.w, O[a][i][3]);
+          // packed f32 FMA: two independent round-to-nearest FMAs per instruction
+          const float2 pp = make_float2(p[a], p[a]);
+          float2 o01 = make_float2(O[a][i][0], O[a][i][1]), o23 = make_float2(O[a][i][2], O[a][i][3]);
+          o01 = __ffma2_rn(pp, v01, o01);
+          o23 = __ffma2_rn(pp, v23, o23);
+          O[a][i][0] = o01.x;
+          O[a][i][1] = o01.y;
+          O[a][i][2] = o23.x;
+          O[a][i][3] = o23.y;
         }
       }
     }
