@@ -153,18 +153,24 @@ int pp_prefill(pp_model* m, const int32_t* tokens, int32_t n, int32_t start_pos,
                float* logits_out);
 
 /* Same computation with device-resident ids d_tokens [n] and device output
- * d_logits [vocab], enqueued on `stream` (a cudaStream_t; NULL selects the
- * model's own stream) without host synchronisation. Ids are checked on the
- * device: an id outside [0, vocab) gives a zero embedding row and records
- * PP_ERR_ARG in the model's device status, read by pp_device_status(). */
+ * d_logits [vocab], enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream, as for the pp_op_* calls) without host synchronisation:
+ * work enqueued on `stream` afterwards (an event, a copy of d_logits) sees the
+ * finished result. Each call is ordered after the model's previous call,
+ * whatever stream that one was given (they share the K/V cache and scratch).
+ * In streamed mode the layer copies run on the model's copy stream and the
+ * compute on its own stream, joined to `stream` by events at both ends. Ids
+ * are checked on the device: an id outside [0, vocab) gives a zero embedding
+ * row and records PP_ERR_ARG in the model's device status, read by
+ * pp_device_status(). */
 int pp_prefill_device(pp_model* m, const int32_t* d_tokens, int32_t n, int32_t start_pos, int32_t chunk,
                       float* d_logits, void* stream);
 
 /* The per-token path: pp_prefill(m, &token, 1, pos, 1, logits_out). */
 int pp_forward_one(pp_model* m, int32_t token, int32_t pos, float* logits_out);
 
-/* Synchronise the model's streams and return (and clear) the device status
- * word: PP_OK, PP_ERR_ARG (bad id seen by pp_prefill_device) or
+/* Wait for the model's streams and its last call (on whatever stream it was
+ * enqueued) and return (and clear) the device status word: PP_OK, PP_ERR_ARG (bad id seen by pp_prefill_device) or
  * PP_ERR_DEVICE_TIMEOUT. */
 int pp_device_status(pp_model* m);
 

@@ -146,6 +146,7 @@ struct pp_model {
   LayerLayout lay{};
   cudaStream_t stream = nullptr;       // compute stream (owned)
   cudaStream_t copy_stream = nullptr;  // streamed mode: layer copies
+  cudaEvent_t done = nullptr;          // recorded on the caller's stream at the end of every prefill
   // weights
   uint8_t* d_layers = nullptr;  // resident: n_layers packed blocks
   uint8_t* h_layers = nullptr;  // streamed: pinned host packed blocks
@@ -195,7 +196,16 @@ int ev_get(pp_model* m, cudaEvent_t* e) {
   return PP_OK;
 }
 
-// Fold finished event pairs into the statistics (the stream must be idle).
+// Wait for everything the model has enqueued: its own streams and the last
+// prefill on a caller's stream (the `done` event).
+int sync_model(pp_model* m) {
+  PP_CUDA(cudaStreamSynchronize(m->stream));
+  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  if (m->done) PP_CUDA(cudaEventSynchronize(m->done));
+  return PP_OK;
+}
+
+// Fold finished event pairs into the statistics (after sync_model).
 int collect(pp_model* m) {
   for (auto& p : m->prof_pending) {
     float ms = 0.f;
@@ -319,6 +329,7 @@ int load_impl(pp_model* m, const pp_weights* w) {
   }
   m->engine = c.gemm_engine == PP_GEMM_MMA ? PP_GEMM_MMA : (tc ? PP_GEMM_TC : PP_GEMM_MMA);
   PP_CUDA(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
+  PP_CUDA(cudaEventCreateWithFlags(&m->done, cudaEventDisableTiming));
   m->lay = make_layout(c);
   const size_t D = c.dim, V = c.vocab, QD = (size_t)c.n_heads * c.head_dim,
                QKV = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn, MC = c.max_chunk;
@@ -420,6 +431,10 @@ int load_impl(pp_model* m, const pp_weights* w) {
 void free_impl(pp_model* m) {
   if (m->stream) cudaStreamSynchronize(m->stream);
   if (m->copy_stream) cudaStreamSynchronize(m->copy_stream);
+  if (m->done) {
+    cudaEventSynchronize(m->done);
+    cudaEventDestroy(m->done);
+  }
   for (auto& p : m->prof_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
   for (auto& p : m->prefetch_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
   for (auto e : m->ev_pool) cudaEventDestroy(e);
@@ -501,6 +516,9 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   const int n_chunks = (n + chunk - 1) / chunk;
   const int n_visits = n_chunks * c.n_layers;
   int visit = 0;
+  // The model's scratch, K/V cache and ring are shared by every call: order
+  // this call after the previous one, whichever stream that one ran on.
+  PP_CUDA(cudaStreamWaitEvent(st, m->done, 0));
   if (c.mode == PP_MODE_STREAMED && st != m->stream) {
     // keep the ring's events on one compute stream
     cudaEvent_t e;
@@ -580,6 +598,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     PP_CUDA(cudaStreamWaitEvent(st, e, 0));
     m->ev_pool.push_back(e);
   }
+  PP_CUDA(cudaEventRecord(m->done, st));
   m->stats.calls += 1;
   m->stats.chunks += n_chunks;
   m->stats.tokens += n;
@@ -648,8 +667,8 @@ int pp_prefill_device(pp_model* m, const int32_t* d_tokens, int32_t n, int32_t s
                       float* d_logits, void* stream) {
   PP_TRY(check_prefill_args(m, n, start_pos, chunk));
   if (!d_tokens || !d_logits) { set_err("null device pointer"); return PP_ERR_ARG; }
-  cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : m->stream;
-  return prefill_impl(m, d_tokens, n, start_pos, chunk, d_logits, st);
+  // NULL is the legacy default stream, as for every other entry point
+  return prefill_impl(m, d_tokens, n, start_pos, chunk, d_logits, static_cast<cudaStream_t>(stream));
 }
 
 int pp_prefill(pp_model* m, const int32_t* tokens, int32_t n, int32_t start_pos, int32_t chunk, float* logits_out) {
@@ -675,8 +694,7 @@ int pp_forward_one(pp_model* m, int32_t token, int32_t pos, float* logits_out) {
 
 int pp_device_status(pp_model* m) {
   if (!m) return PP_ERR_ARG;
-  PP_CUDA(cudaStreamSynchronize(m->stream));
-  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  PP_TRY(sync_model(m));
   int s = 0;
   PP_CUDA(cudaMemcpy(&s, m->status, sizeof(int), cudaMemcpyDeviceToHost));
   if (s != DEV_OK) PP_CUDA(cudaMemset(m->status, 0, sizeof(int)));
@@ -693,6 +711,7 @@ int pp_kv_reset(pp_model* m) {
   if (!m) return PP_ERR_ARG;
   const pp_config& c = m->cfg;
   const size_t KVE = (size_t)c.n_layers * c.max_seq * c.n_kv_heads * c.head_dim;
+  PP_TRY(sync_model(m));
   PP_CUDA(cudaMemsetAsync(m->kc, 0, KVE * 4, m->stream));
   PP_CUDA(cudaMemsetAsync(m->vc, 0, KVE * 4, m->stream));
   PP_CUDA(cudaStreamSynchronize(m->stream));
@@ -708,7 +727,7 @@ int pp_kv_read(pp_model* m, int32_t layer, int32_t which, int32_t pos0, int32_t 
   const pp_config& c = m->cfg;
   const size_t row = (size_t)c.n_kv_heads * c.head_dim;
   const float* src = (which ? m->vc : m->kc) + (size_t)layer * c.max_seq * row + (size_t)pos0 * row;
-  PP_CUDA(cudaStreamSynchronize(m->stream));
+  PP_TRY(sync_model(m));
   PP_CUDA(cudaMemcpy(out, src, sizeof(float) * row * n_pos, cudaMemcpyDeviceToHost));
   return PP_OK;
 }
@@ -716,8 +735,7 @@ int pp_kv_read(pp_model* m, int32_t layer, int32_t which, int32_t pos0, int32_t 
 int pp_get_stats(const pp_model* cm, pp_stats* out) {
   if (!cm || !out) return PP_ERR_ARG;
   pp_model* m = const_cast<pp_model*>(cm);
-  PP_CUDA(cudaStreamSynchronize(m->stream));
-  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  PP_TRY(sync_model(m));
   PP_TRY(collect(m));
   *out = m->stats;
   return PP_OK;
@@ -725,8 +743,7 @@ int pp_get_stats(const pp_model* cm, pp_stats* out) {
 
 int pp_reset_stats(pp_model* m) {
   if (!m) return PP_ERR_ARG;
-  PP_CUDA(cudaStreamSynchronize(m->stream));
-  if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  PP_TRY(sync_model(m));
   PP_TRY(collect(m));
   m->stats = pp_stats{};
   return PP_OK;
@@ -739,7 +756,7 @@ int pp_set_trace(pp_model* m, float* d_x, int8_t* d_codes, float* d_scales, int3
     set_err("bad pp_set_trace arguments");
     return PP_ERR_ARG;
   }
-  PP_CUDA(cudaStreamSynchronize(m->stream));
+  PP_TRY(sync_model(m));
   m->trace = d_x;
   m->trace_codes = d_x ? d_codes : nullptr;
   m->trace_scales = d_x ? d_scales : nullptr;

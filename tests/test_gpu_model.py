@@ -158,6 +158,27 @@ def test_device_path_equals_host_path(tiny):
     assert np.array_equal(bits(d_logits.cpu().numpy()), bits(ref))
 
 
+def test_device_path_on_a_side_stream(tiny):
+    """The call is enqueued on the stream it is given: a copy of the logits
+    enqueued on that stream afterwards, waited for on that stream alone, sees
+    the result."""
+    torch = torch_cuda()
+    m, g = tiny
+    toks = synth.prompt(m.cfg)
+    g.kv_reset()
+    ref = g.prefill(toks, 0, 8)
+    g.kv_reset()
+    d_tok = torch.from_numpy(toks).cuda()
+    d_logits = torch.zeros(m.cfg.vocab, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.prefill_device(d_tok, len(toks), 0, 8, d_logits, s)
+        out = d_logits.clone()
+    s.synchronize()
+    assert np.array_equal(bits(out.cpu().numpy()), bits(ref))
+
+
 # ------------------------------------------------------------------ 350M class
 def _summary(report):
     return [(sum(st["mismatches"]), max(st["max_margin"])) for st in report]

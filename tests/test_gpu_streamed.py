@@ -64,3 +64,37 @@ def test_streamed_continuation_and_chunk_invariance(model_1b):
     cont = g.prefill(toks[100:], 100, 128)
     g.close()
     assert np.array_equal(bits(whole), bits(cont))
+
+
+@pytest.mark.parametrize("side_stream", [False, True])
+def test_streamed_device_call_is_ordered_on_the_callers_stream(model_1b, side_stream):
+    """pp_prefill_device in streamed mode: the copies and the compute run on
+    the model's own streams, joined to the caller's stream at both ends. Work
+    enqueued on the caller's stream after the call (CUDA events, a copy of the
+    logits) must see the whole call: the events bracket at least the time the
+    layer copies need at 1 TB/s (well above any host link), and the logits
+    read on that stream alone equal the host path's."""
+    torch = torch_cuda()
+    m = model_1b
+    c = m.cfg
+    toks = synth.prompt(c, 256)
+    g = load(m, max_seq=1024, max_chunk=256, mode=pp.PP_MODE_STREAMED, ring_slots=2)
+    ref = g.prefill(toks, 0, 256)
+    d_tok = torch.from_numpy(toks).cuda()
+    d_logits = torch.zeros(c.vocab, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream() if side_stream else torch.cuda.current_stream()
+    g.reset_stats()
+    with torch.cuda.stream(s):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.prefill_device(d_tok, len(toks), 0, 256, d_logits, s)
+        e1.record(s)
+        out = d_logits.clone()
+    s.synchronize()
+    got = out.cpu().numpy()
+    ms = e0.elapsed_time(e1)
+    h2d = g.stats()["h2d_bytes"]
+    g.close()
+    assert np.array_equal(bits(got), bits(ref))
+    assert ms >= h2d / 1e12 * 1e3, f"{ms:.3f} ms for {h2d} bytes of layer copies"
