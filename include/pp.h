@@ -291,7 +291,11 @@ int pp_op_rope_table(int32_t max_pos, int32_t head_dim, float theta, float* rope
  * kv[0..i]): q [rows][H][hd] at positions start_pos+i, k/v caches
  * [*][Hkv][hd]; o [rows][H][hd] = softmax((q.k_j)/sqrt(hd), j <= pos) v.
  * Query head h reads KV head h / (H / Hkv). f32 on CUDA cores; every
- * query's reduction order depends only on its absolute position. */
+ * query's reduction order depends only on its absolute position (keys are
+ * reduced in ranges of 512 at fixed positions, then the ranges in order).
+ * When start_pos + rows > 512 the call uses a library-owned device
+ * workspace, grown on first need (that growth synchronises the device) and
+ * shared by all calls: calls on different streams must not overlap. */
 int pp_op_attention(const float* q, const float* k_cache, const float* v_cache, int32_t rows, int32_t start_pos,
                     int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float* o, void* stream);
 

@@ -6,24 +6,32 @@
 // "What Stays Sequential": attention is sequential in positions; here every
 // position of the chunk is one independent query row, which is equivalent.
 //
-// One CTA = one KV head x a tile of 64 query rows (64/G positions x the G
-// query heads that share the KV head), streaming the key axis in blocks of
-// 64 keys aligned to absolute positions. Per row: online softmax in base 2
-// (q pre-scaled by log2(e)/sqrt(hd)), warp-shuffle max/sum over the 8 lanes
-// that hold the row, then O += P V. Blocks are walked in the same order for
-// every query; a block past a row's own position is fully masked, which
-// leaves its state bit-for-bit unchanged (alpha = 1, p = 0). A row's result
-// therefore depends only on its absolute position and the cache, not on the
-// chunk it was computed in.
+// Work split. A query tile is 64 rows (64/G positions x the G query heads
+// that share a KV head). Its keys are cut into ranges of kAttnRange keys at
+// fixed absolute positions (0, 512, 1024, ...), and one CTA runs one (tile,
+// KV head, range) item, heaviest items first, so the grid fills every SM
+// evenly whatever the chunk's position. Within an item the key axis streams
+// through shared memory in blocks of 64 keys; per row: online softmax in
+// base 2 (q pre-scaled by log2(e)/sqrt(hd)), warp-shuffle max/sum over the 8
+// lanes that hold the row, then O += P V. A tile whose keys fit one range
+// writes o directly; otherwise every item writes its (O, m, l) state and a
+// second kernel combines the ranges of each row in range order.
+//
+// Chunk invariance. The ranges, the blocks within a range and the order of
+// every reduction depend only on a row's absolute position: a block or a
+// range past the row's position is fully masked and leaves its state (or the
+// merged result) bit-for-bit unchanged, so a row's result does not depend on
+// the chunk it was computed in.
 #include "pp_internal.cuh"
 
 namespace pp {
 namespace {
 
-constexpr int ROWS = 64;     // query rows per CTA
-constexpr int KB = 64;       // keys per block
-constexpr int THREADS = 128; // 16 row groups (ty) x 8 lanes (tx)
-constexpr int PS = 68;       // padded stride of the P tile
+constexpr int ROWS = 64;      // query rows per CTA
+constexpr int KB = 64;        // keys per block
+constexpr int THREADS = 128;  // 16 row groups (ty) x 8 lanes (tx)
+constexpr int PS = 68;        // padded stride of the P tile, [key][4 ty + a]
+static_assert(kAttnRange % KB == 0, "a key range is a whole number of key blocks");
 
 // XOR swizzle of 16-byte chunks within a row of the Q and K tiles: rows r and
 // r' with r = r' (mod 8) never share a bank group when read at the same d.
@@ -32,32 +40,53 @@ __device__ __forceinline__ int swz(int r, int d) {
   return r * HD + ((((d >> 2) ^ (r & 7))) << 2) + (d & 3);
 }
 
+struct Tile {
+  int tile, kvh, i0, pmax, nr;  // query tile, KV head, first row, last position, number of key ranges
+};
+
+__device__ __forceinline__ Tile tile_of(int j, int n_tiles, int Hkv, int bq, int C, int start_pos) {
+  Tile t;
+  t.tile = n_tiles - 1 - j / Hkv;  // later positions (more keys) first
+  t.kvh = j % Hkv;
+  t.i0 = t.tile * bq;
+  t.pmax = start_pos + min(t.i0 + bq, C) - 1;
+  t.nr = t.pmax / kAttnRange + 1;
+  return t;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 2)
     k_attention(const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int C,
-                int start_pos, int H, int Hkv, float* __restrict__ o, float qscale) {
+                int start_pos, int H, int Hkv, float* __restrict__ o, float qscale, float* __restrict__ part,
+                int n_ranges) {
   extern __shared__ __align__(16) float sm[];
-  float* Qs = sm;                  // [ROWS][HD] swizzled
-  float* Ks = Qs + ROWS * HD;      // [KB][HD] swizzled
-  float* Vs = Ks + KB * HD;        // [KB][HD]
-  float* Ps = Vs + KB * HD;        // [KB][PS]
+  float* Qs = sm;              // [ROWS][HD] swizzled
+  float* Ks = Qs + ROWS * HD;  // [KB][HD] swizzled
+  float* Vs = Ks + KB * HD;    // [KB][HD]
+  float* Ps = Vs + KB * HD;    // [KB][PS]
 
   const int G = H / Hkv;
   const int bq = ROWS / G;  // positions per tile
-  const int kvh = blockIdx.y;
-  const int i0 = blockIdx.x * bq;
+  const int n_tiles = (C + bq - 1) / bq;
+  const int per_range = n_tiles * Hkv;
+  const int r = blockIdx.x / per_range;
+  const Tile T = tile_of(blockIdx.x % per_range, n_tiles, Hkv, bq, C, start_pos);
+  if (r >= T.nr) return;  // no key of this range is visible to the tile
+  const int kvh = T.kvh, i0 = T.i0, pmax = T.pmax;
+  const int kb_begin = r * (kAttnRange / KB);
+  const int kb_end = min(pmax, (r + 1) * kAttnRange - 1) / KB + 1;
   const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
 
-  // Load the query tile (row r = position-in-tile * G + head-in-group).
+  // Query tile (row rr = position-in-tile * G + head-in-group).
   constexpr int C4 = HD / 4;
   for (int e = tid; e < ROWS * C4; e += THREADS) {
-    const int r = e / C4, c = e % C4;
-    int i = i0 + r / G;
+    const int rr = e / C4, c = e % C4;
+    int i = i0 + rr / G;
     if (i > C - 1) i = C - 1;  // padding rows recompute the last position; never stored
-    const int h = kvh * G + r % G;
+    const int h = kvh * G + rr % G;
     float4 v = *reinterpret_cast<const float4*>(q + ((size_t)i * H + h) * HD + 4 * c);
     v.x *= qscale; v.y *= qscale; v.z *= qscale; v.w *= qscale;
-    *reinterpret_cast<float4*>(&Qs[swz<HD>(r, 4 * c)]) = v;
+    *reinterpret_cast<float4*>(&Qs[swz<HD>(rr, 4 * c)]) = v;
   }
 
   // This thread's rows: ty + 16a; its keys in a block: tx + 8b; its dims: 4tx + 32i + e.
@@ -68,9 +97,6 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (i > C - 1) i = C - 1;
     pos[a] = start_pos + i;
   }
-  const int last_i = min(i0 + bq, C) - 1;
-  const int pmax = start_pos + last_i;
-  const int nblocks = pmax / KB + 1;
 
   constexpr int ND = HD / 32;  // float4 groups of dims per thread
   float O[4][ND][4];
@@ -99,16 +125,16 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     ppdev::cp_async_commit();
   };
-  load_tile(Ks, kc, 0, true);
-  load_tile(Vs, vc, 0, false);
-  ppdev::cp_async_wait<1>();  // K of block 0
+  load_tile(Ks, kc, kb_begin * KB, true);
+  load_tile(Vs, vc, kb_begin * KB, false);
+  ppdev::cp_async_wait<1>();  // K of the first block
   __syncthreads();
 
-  for (int kb = 0; kb < nblocks; ++kb) {
+  for (int kb = kb_begin; kb < kb_end; ++kb) {
     const int key0 = kb * KB;
-    const bool more = kb + 1 < nblocks;
+    const bool more = kb + 1 < kb_end;
 
-    // S = Q K^T for rows ty+16a, keys tx+8b, in d order.
+    // S = Q K^T for rows ty+16a, keys tx+8b, in d order (one d for all 32 sums at a time).
     float S[4][8];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -124,18 +150,26 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          S[a][b] = fmaf(qv[a].x, kv[b].x, S[a][b]);
-          S[a][b] = fmaf(qv[a].y, kv[b].y, S[a][b]);
-          S[a][b] = fmaf(qv[a].z, kv[b].z, S[a][b]);
-          S[a][b] = fmaf(qv[a].w, kv[b].w, S[a][b]);
-        }
+        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].x, kv[b].x, S[a][b]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].y, kv[b].y, S[a][b]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].z, kv[b].z, S[a][b]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].w, kv[b].w, S[a][b]);
     }
     __syncthreads();  // every warp is done with Ks
     if (more) load_tile(Ks, kc, key0 + KB, true);
     else ppdev::cp_async_commit();
 
-    // Causal mask, online softmax (base 2), P -> smem.
+    // Causal mask, online softmax (base 2). A row that has seen no key of this
+    // range yet (m = -inf) keeps m = -inf, l = 0, O = 0 through masked blocks.
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       float mb = -INFINITY;
@@ -149,12 +183,13 @@ __global__ void __launch_bounds__(THREADS, 2)
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
       const float mn = fmaxf(m[a], mb);
       const float alpha = (mn == m[a]) ? 1.f : exp2f(m[a] - mn);
+      const float mref = (mn == -INFINITY) ? 0.f : mn;
       float ls = 0.f;
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
-        const float p = exp2f(S[a][b] - mn);
+        const float p = exp2f(S[a][b] - mref);
         ls += p;
-        Ps[(tx + 8 * b) * PS + ty + 16 * a] = p;
+        S[a][b] = p;
       }
       ls += __shfl_xor_sync(0xffffffffu, ls, 1);
       ls += __shfl_xor_sync(0xffffffffu, ls, 2);
@@ -166,15 +201,18 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) O[a][i][e] *= alpha;
     }
+    // P -> smem, the thread's 4 rows of one key as one 16-byte store
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+      *reinterpret_cast<float4*>(&Ps[(tx + 8 * b) * PS + 4 * ty]) = make_float4(S[0][b], S[1][b], S[2][b], S[3][b]);
     ppdev::cp_async_wait<1>();  // V of this block (the K prefetch may still be in flight)
     __syncthreads();
 
     // O += P V, keys in order.
 #pragma unroll 4
     for (int j = 0; j < KB; ++j) {
-      float p[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) p[a] = Ps[j * PS + ty + 16 * a];
+      const float4 p4 = *reinterpret_cast<const float4*>(&Ps[j * PS + 4 * ty]);
+      const float p[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
       for (int i = 0; i < ND; ++i) {
         const float4 v = *reinterpret_cast<const float4*>(&Vs[j * HD + 4 * tx + 32 * i]);
@@ -201,25 +239,89 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   ppdev::cp_async_wait<0>();
 
-  // o[i][h][:] = O / l
+  if (T.nr == 1) {
+    // o[i][h][:] = O / l
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int rr = ty + 16 * a;
+      const int i = i0 + rr / G;
+      if (i >= C) continue;
+      const int h = kvh * G + rr % G;
+      const float inv_l = 1.0f / l[a];
+      float* dst = o + ((size_t)i * H + h) * HD;
+#pragma unroll
+      for (int ii = 0; ii < ND; ++ii)
+        *reinterpret_cast<float4*>(dst + 4 * tx + 32 * ii) =
+            make_float4(O[a][ii][0] * inv_l, O[a][ii][1] * inv_l, O[a][ii][2] * inv_l, O[a][ii][3] * inv_l);
+    }
+    return;
+  }
+  // This range's state: O (not normalised) [ROWS][HD], then (m, l) [ROWS].
+  float* po = part + ((size_t)(T.tile * Hkv + kvh) * n_ranges + r) * ROWS * (HD + 2);
+  float* pml = po + ROWS * HD;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
-    const int r = ty + 16 * a;
-    const int i = i0 + r / G;
-    if (i >= C) continue;
-    const int h = kvh * G + r % G;
-    const float inv_l = 1.0f / l[a];
-    float* dst = o + ((size_t)i * H + h) * HD;
+    const int rr = ty + 16 * a;
 #pragma unroll
     for (int ii = 0; ii < ND; ++ii)
-      *reinterpret_cast<float4*>(dst + 4 * tx + 32 * ii) =
-          make_float4(O[a][ii][0] * inv_l, O[a][ii][1] * inv_l, O[a][ii][2] * inv_l, O[a][ii][3] * inv_l);
+      *reinterpret_cast<float4*>(po + rr * HD + 4 * tx + 32 * ii) =
+          make_float4(O[a][ii][0], O[a][ii][1], O[a][ii][2], O[a][ii][3]);
+    if (tx == 0) *reinterpret_cast<float2*>(pml + 2 * rr) = make_float2(m[a], l[a]);
   }
+}
+
+// Combine the ranges of every tile that has more than one, in range order,
+// one thread per (row, 4 dims): m = max_r m_r, O = sum_r O_r 2^(m_r - m),
+// l = sum_r l_r 2^(m_r - m), o = O / l. A range with m_r = -inf (no key of it
+// is visible to the row) is skipped, so a row that sees one range gets
+// O_0 * 1 / l_0 * 1: the same bits as the single-range path.
+template <int HD>
+__global__ void __launch_bounds__(256)
+    k_attention_merge(int C, int start_pos, int H, int Hkv, float* __restrict__ o, const float* __restrict__ part,
+                      int n_ranges) {
+  constexpr int F4 = HD / 4;
+  constexpr int CTAS_PER_TILE = ROWS * F4 / 256;
+  const int G = H / Hkv;
+  const int bq = ROWS / G;
+  const int n_tiles = (C + bq - 1) / bq;
+  const Tile T = tile_of(blockIdx.x / CTAS_PER_TILE, n_tiles, Hkv, bq, C, start_pos);
+  if (T.nr == 1) return;
+  const int e = (blockIdx.x % CTAS_PER_TILE) * 256 + threadIdx.x;
+  const int rr = e / F4, d4 = e % F4;
+  const int i = T.i0 + rr / G;
+  if (i >= C) return;
+  const size_t stride = (size_t)ROWS * (HD + 2);
+  const float* base = part + (size_t)(T.tile * Hkv + T.kvh) * n_ranges * stride;
+  float mx = -INFINITY;
+#pragma unroll 8
+  for (int r = 0; r < T.nr; ++r) mx = fmaxf(mx, base[r * stride + ROWS * HD + 2 * rr]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  bool first = true;
+#pragma unroll 8
+  for (int r = 0; r < T.nr; ++r) {
+    const float2 ml = *reinterpret_cast<const float2*>(base + r * stride + ROWS * HD + 2 * rr);
+    if (ml.x == -INFINITY) continue;
+    const float s = exp2f(ml.x - mx);
+    const float4 v = *reinterpret_cast<const float4*>(base + r * stride + rr * HD + 4 * d4);
+    if (first) {
+      acc = make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
+      L = ml.y * s;
+      first = false;
+    } else {
+      acc = make_float4(fmaf(v.x, s, acc.x), fmaf(v.y, s, acc.y), fmaf(v.z, s, acc.z), fmaf(v.w, s, acc.w));
+      L = fmaf(ml.y, s, L);
+    }
+  }
+  const float inv_l = 1.0f / L;
+  const int h = T.kvh * G + rr % G;
+  *reinterpret_cast<float4*>(o + ((size_t)i * H + h) * HD + 4 * d4) =
+      make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
 }
 
 template <int HD>
 cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H, int Hkv,
-                     float* o, cudaStream_t s) {
+                     float* o, float* part, size_t part_bytes, cudaStream_t s) {
   constexpr int smem = (ROWS * HD + 2 * KB * HD + KB * PS) * (int)sizeof(float);
   static bool attr = false;
   if (!attr) {
@@ -229,18 +331,33 @@ cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows,
   }
   const int G = H / Hkv;
   const int bq = ROWS / G;
-  dim3 grid((rows + bq - 1) / bq, Hkv);
+  const int n_tiles = (rows + bq - 1) / bq;
+  const int n_ranges = (start_pos + rows - 1) / kAttnRange + 1;
+  if (n_ranges > 1 && (!part || part_bytes < attention_workspace_bytes(rows, start_pos, H, Hkv, HD)))
+    return cudaErrorInvalidValue;
   const float qscale = (float)(1.4426950408889634 / sqrt((double)HD));
-  k_attention<HD><<<grid, THREADS, smem, s>>>(q, kc, vc, rows, start_pos, H, Hkv, o, qscale);
+  k_attention<HD><<<n_tiles * Hkv * n_ranges, THREADS, smem, s>>>(q, kc, vc, rows, start_pos, H, Hkv, o, qscale,
+                                                                  part, n_ranges);
+  if (n_ranges > 1)
+    k_attention_merge<HD><<<n_tiles * Hkv * (ROWS * HD / 4 / 256), 256, 0, s>>>(rows, start_pos, H, Hkv, o, part,
+                                                                                  n_ranges);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t attention_workspace_bytes(int rows, int start_pos, int H, int Hkv, int hd) {
+  const int bq = ROWS / (H / Hkv);
+  const size_t n_tiles = (size_t)(rows + bq - 1) / bq;
+  const size_t n_ranges = (size_t)(start_pos + rows - 1) / kAttnRange + 1;
+  if (n_ranges == 1) return 0;
+  return n_tiles * Hkv * n_ranges * ROWS * (hd + 2) * sizeof(float);
+}
+
 cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,
-                             int Hkv, int hd, float* o, cudaStream_t s) {
-  if (hd == 64) return launch_t<64>(q, kc, vc, rows, start_pos, H, Hkv, o, s);
-  if (hd == 128) return launch_t<128>(q, kc, vc, rows, start_pos, H, Hkv, o, s);
+                             int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s) {
+  if (hd == 64) return launch_t<64>(q, kc, vc, rows, start_pos, H, Hkv, o, part, part_bytes, s);
+  if (hd == 128) return launch_t<128>(q, kc, vc, rows, start_pos, H, Hkv, o, part, part_bytes, s);
   return cudaErrorInvalidValue;
 }
 

@@ -176,6 +176,8 @@ struct pp_model {
   std::vector<CUtensorMap> wmap;
   CUtensorMap amap_d{}, amap_qd{}, amap_f{};
   TcWorkspace tcws;  // stream-K partial tiles and counters of the projection GEMMs
+  float* attn_part = nullptr;  // per-key-range partial attention state of one chunk
+  size_t attn_part_bytes = 0;
   // stats and timing
   pp_stats stats{};
   std::vector<cudaEvent_t> ev_pool;
@@ -357,6 +359,12 @@ int load_impl(pp_model* m, const pp_weights* w) {
   PP_TRY(dalloc(m, &m->qkv, MC * QKV));
   PP_TRY(dalloc(m, &m->qr, MC * QD));
   PP_TRY(dalloc(m, &m->o, MC * QD));
+  {
+    // largest chunk at the end of the cache: the most tiles times the most key ranges
+    const int rows = (int)std::min<size_t>(MC, (size_t)c.max_seq);
+    m->attn_part_bytes = attention_workspace_bytes(rows, c.max_seq - rows, c.n_heads, c.n_kv_heads, c.head_dim);
+    if (m->attn_part_bytes) PP_TRY(dalloc(m, &m->attn_part, m->attn_part_bytes / sizeof(float)));
+  }
   PP_TRY(dalloc(m, &m->h, MC * F));
   PP_TRY(dalloc(m, &m->a8, MC * KMAX));
   PP_TRY(dalloc(m, &m->a16, MC * KMAX));
@@ -557,8 +565,9 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
         return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
       }));
       PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
-        return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, cs);
+        return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
       }));
+      if (attention_workspace_bytes(C, pos0, H, Hkv, hd)) m->stats.kernel_launches += 1;  // the range merge
       PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
         return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, q16, m->as, cs);
       }));
@@ -1004,6 +1013,13 @@ int pp_op_rope_kv(const float* qkv, int32_t rows, int32_t start_pos, int32_t n_h
                    "rope_kv");
 }
 
+// Per-key-range partial state of the single-step attention entry point,
+// grown on demand and kept until exit; calls are serialised by the mutex
+// only on the host, so concurrent calls on different streams would share it.
+static std::mutex g_attn_ws_mu;
+static float* g_attn_ws = nullptr;
+static size_t g_attn_ws_bytes = 0;
+
 int pp_op_attention(const float* q, const float* k_cache, const float* v_cache, int32_t rows, int32_t start_pos,
                     int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float* o, void* stream) {
   if (!q || !k_cache || !v_cache || !o || rows <= 0 || start_pos < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
@@ -1011,8 +1027,19 @@ int pp_op_attention(const float* q, const float* k_cache, const float* v_cache, 
     set_err("bad pp_op_attention arguments");
     return PP_ERR_ARG;
   }
+  const size_t need = attention_workspace_bytes(rows, start_pos, n_heads, n_kv_heads, head_dim);
+  std::lock_guard<std::mutex> lk(g_attn_ws_mu);
+  if (need > g_attn_ws_bytes) {
+    // grow the process-wide range workspace (cudaFree waits for the device)
+    if (g_attn_ws) cudaFree(g_attn_ws);
+    g_attn_ws = nullptr;
+    g_attn_ws_bytes = 0;
+    cudaError_t e = cudaMalloc(&g_attn_ws, need);
+    if (e != cudaSuccess) return ok_launch(e, "attention workspace");
+    g_attn_ws_bytes = need;
+  }
   return ok_launch(launch_attention(q, k_cache, v_cache, rows, start_pos, n_heads, n_kv_heads, head_dim, o,
-                                    static_cast<cudaStream_t>(stream)),
+                                    g_attn_ws, g_attn_ws_bytes, static_cast<cudaStream_t>(stream)),
                    "attention");
 }
 

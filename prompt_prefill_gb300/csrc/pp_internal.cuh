@@ -55,8 +55,12 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)
+// Keys per range of the attention work split, at fixed absolute positions.
+constexpr int kAttnRange = 512;
+// Bytes of per-range partial state a launch of this size needs (0: one range).
+size_t attention_workspace_bytes(int rows, int start_pos, int H, int Hkv, int hd);
 cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,
-                             int Hkv, int hd, float* o, cudaStream_t s);
+                             int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s);
 
 // Rows of the interleaved gate/up matrix: blocks of 16 gate rows then 16 up rows.
 constexpr int kSwiGluBlock = 16;

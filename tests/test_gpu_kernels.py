@@ -150,8 +150,11 @@ def test_rope_kv(torch, rows, start, H, Hkv, hd, theta):
     assert np.all(kc[:start] == 7.0) and np.all(kc[start + rows:] == 7.0) and np.all(vc[:start] == 7.0)
 
 
+# rows, start, H, Hkv, hd. Keys are reduced in ranges of 512 at fixed positions:
+# the later cases cross range boundaries (1024, 2048) and merge 16 ranges.
 ATTN_CASES = [(1, 0, 4, 4, 64), (8, 0, 4, 4, 64), (32, 5, 16, 8, 64), (37, 100, 32, 8, 64), (64, 250, 32, 8, 128),
-              (3, 700, 32, 8, 128), (130, 0, 8, 8, 128)]
+              (3, 700, 32, 8, 128), (130, 0, 8, 8, 128), (40, 1000, 32, 8, 128), (64, 2040, 16, 8, 64),
+              (16, 8000, 32, 8, 128)]
 
 
 @pytest.mark.parametrize("rows,start,H,Hkv,hd", ATTN_CASES)
@@ -167,10 +170,13 @@ def test_attention_matches_oracle(torch, rows, start, H, Hkv, hd):
     assert np.abs(host(o) - ref).max() <= 1e-5 * np.abs(V).max()
 
 
-def test_attention_row_result_independent_of_chunk(torch):
+@pytest.mark.parametrize("rows,start", [(50, 37), (64, 480), (100, 1500)])
+def test_attention_row_result_independent_of_chunk(torch, rows, start):
     # Each query's reduction order depends only on its absolute position:
-    # one launch over 50 rows equals 50 launches of one row, bit for bit.
-    rows, start, H, Hkv, hd = 50, 37, 32, 8, 128
+    # one launch over the rows equals one launch per row, bit for bit, also
+    # where the chunk straddles a key-range boundary (512, 1536) so that some
+    # of its rows merge two ranges and the rest see one.
+    H, Hkv, hd = 32, 8, 128
     n = start + rows
     q = synth.normal_f32(64, 1, (rows, H, hd), 0.0, 2.0)
     K = dev(synth.normal_f32(64, 2, (n, Hkv, hd), 0.0, 1.0))
