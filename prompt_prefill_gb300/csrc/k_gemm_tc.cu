@@ -4,30 +4,30 @@
 // whole chunk of token columns, with activations quantised once per chunk.
 // sm_103a has no integer tcgen05 MMA kind, so the integer GEMM runs on
 // tcgen05.mma.kind::f16 with operands that hold the int8 codes exactly:
-//   - every integer in [-127, 127] is an fp16 value, and so is every product
-//     (|a*w| <= 16129 < 2^11 * 2^... fits the 22-bit product of two 11-bit
-//     significands);
+//   - every integer in [-127, 127] is an fp16 value, and every product of two
+//     such values (|a*w| <= 16129) is exact in the f32 accumulator;
 //   - an f32 sum of such products is exact while every partial sum stays below
 //     2^24 in magnitude, i.e. for up to floor(2^24 / 127^2) = 1040 products.
 // The K axis is therefore cut into segments of at most 1024 (16 k-blocks of
-// 64); each segment accumulates into its own f32 TMEM buffer, which the
-// epilogue warps read back, convert to int32 (exact) and add to int32
-// registers. The result equals the int32 dot product bit for bit.
+// 64); each segment accumulates into its own f32 TMEM buffer, which drain
+// warps read back, convert to int32 (exact) and add to int32 registers. The
+// result equals the int32 dot product bit for bit.
 //
 // Layout: a CTA pair (cluster of 2, cta_group::2) computes a 256-token x
-// 256-weight-row tile; each CTA holds 128 token rows of A (fp16 codes, TMA,
-// 128-byte swizzle) and 128 weight rows of B. Weights stay int8 in HBM: TMA
-// brings int8 rows into shared memory and 8 converter warps widen them to
+// BN-weight-row tile (BN = 256, 192 or 128, chosen per shape so that the
+// tiles fill the 76 pairs); each CTA holds 128 token rows of A (fp16 codes,
+// TMA, 128-byte swizzle) and BN/2 weight rows of B. Weights stay int8 in HBM:
+// TMA brings int8 rows into shared memory and converter warps widen them to
 // fp16 in the UMMA K-major 128-byte-swizzled layout (exponent-bias method:
 // 0x6400 | (b ^ 0x80) is the fp16 number 1024 + 128 + b, minus 1152 gives b).
-// Warp 0 issues TMA, warp 1 (leader CTA) issues the MMAs, warps 4-11 convert
-// and run the epilogue, each thread holding 128 int32 running sums (register
-// split by setmaxnreg). Converter warps never block on the MMA: they drain a
-// segment only once its accumulator is complete (polled between conversions)
-// and emit a finished tile's epilogue in chunks between the next tile's
-// conversions, so the stages ahead of the tensor core stay filled. Persistent over tiles; two TMEM accumulators of 256 columns alternate
-// between segments. Every mbarrier wait is bounded: on
-// expiry the kernel records a timeout in the status word and winds down.
+//
+// Roles (16 warps): warp 0 issues TMA, warp 1 (leader CTA) issues the MMAs,
+// warpgroup 1 only converts, warpgroups 2-3 only drain accumulators and run
+// the epilogue (each thread holds BN/2 int32 running sums). Conversion never
+// waits behind a drain or an epilogue, so the stages ahead of the tensor core
+// stay filled. Persistent over tiles; two TMEM accumulators of BN columns
+// alternate between segments. Every mbarrier wait is bounded: on expiry the
+// kernel records a timeout in the status word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,27 +37,36 @@ namespace pp {
 namespace {
 
 constexpr int BM = 128;             // token rows per CTA (256 per pair)
-constexpr int BN = 256;             // weight rows per pair tile (128 per CTA)
 constexpr int BK = 64;              // k per stage: 128 bytes of fp16
-constexpr int STAGES = 5;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int B_BYTES = (BN / 2) * BK * 2;    // 16 KB, converted weights
-constexpr int W_BYTES = (BN / 2) * BK;        // 8 KB, int8 weights
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + W_BYTES;
-constexpr int N_CONV_WARPS = 8;         // 2 per TMEM lane quarter, 128 accumulator columns each
-constexpr int THREADS = 384;            // warpgroup 0: TMA, MMA, 2 idle; warpgroups 1-2: converters
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int N_CONV_WARPS = 4;     // warpgroup 1: int8 -> fp16 conversion
+constexpr int N_DRAIN_WARPS = 8;    // warpgroups 2-3: 2 per TMEM lane quarter, BN/2 accumulator columns each
+constexpr int THREADS = 512;        // warpgroup 0: TMA, MMA, 2 idle
 constexpr int CONV_WARP0 = 4;
-// Register split (setmaxnreg): launched at 168 per thread (12 x 32 x 168 = 64512 in the
-// pool); warpgroup 0 drops to 40 and the converter warpgroups rise to 232:
-// 4 x 32 x 40 + 8 x 32 x 232 = 64512, and per SM sub-partition (40 + 232 + 232) x 32 <= 16384.
-constexpr int REGS_ROLE = 40, REGS_CONV = 232;
-constexpr int TMEM_COLS = 512;
+constexpr int DRAIN_WARP0 = 8;
+// Register split (setmaxnreg): launched at 128 per thread (16 x 32 x 128 = 65536 in the
+// pool); warpgroup 0 drops to 40, the converters to 72 and the drain warpgroups rise to
+// 200: 128 x 40 + 128 x 72 + 256 x 200 = 65536, and per SM sub-partition
+// (40 + 72 + 200 + 200) x 32 = 16384.
+constexpr int REGS_ROLE = 40, REGS_CONV = 72, REGS_DRAIN = 200;
 constexpr int MAX_SEG_KB = 16;      // 16 x 64 = 1024 products per exact f32 segment
 constexpr int MIN_SK_KB = 64;       // stream-K only when each cluster owns >= 64 k-blocks (measured: fixups
-                                    // cost more than they recover at ~40 k-blocks per cluster)
-constexpr int EPI_EVERY = 2;        // conversions between two epilogue chunks of a finished tile
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+                                    // cost more than they recover at ~30-40 k-blocks per cluster)
+constexpr int STAGE_BUDGET = 204 * 1024;  // shared memory for the pipeline stages
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+
+// Per-tile-width constants.
+template <int BN>
+struct Cfg {
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;  // converted weights of one CTA
+  static constexpr int W_BYTES = (BN / 2) * BK;      // int8 weights of one CTA
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + W_BYTES;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES;  // 5 (256), 6 (192), 7 (128)
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 2 * BN * 4 /*w_scale*/;
+  static constexpr int COLS = BN / 2;                 // accumulator columns per drain warp
+  static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0, "stage buffers keep the 1024-byte swizzle alignment");
+};
 
 struct TcParams {
   int M, N, K;
@@ -70,7 +79,7 @@ struct TcParams {
   int32_t* acc_out;
   int* status;
   // stream-K: cluster c owns iterations [c*ipc, (c+1)*ipc) of the (tile, k-block)
-  // space; partial tiles meet in `part` (int32 [tile][slot][cta][128][256]) and the
+  // space; partial tiles meet in `part` (int32 [tile][slot][cta][128][BN]) and the
   // last contributor, counted in `cnt` ([tile][cta], zero between launches), adds
   // the partial sums and runs the epilogue. ipc == 0: whole tiles round robin.
   int ipc;
@@ -133,18 +142,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of a barrier phase (lane 0 tests, the warp agrees).
-__device__ __forceinline__ bool mbar_test_warp(uint32_t a, uint32_t parity) {
-  uint32_t ok = 0;
-  if ((threadIdx.x & 31) == 0)
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
 // Bounded wait: false after ~2 s without the phase completing.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
   if (mbar_try(a, parity)) return true;
@@ -198,6 +195,14 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t a) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -219,14 +224,17 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 // Byte offset of fp16 chunk j (8 elements) of row r in a K-major 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int r, int j) { return (r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4); }
 
-template <int EPI>
+
+template <int EPI, int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const TcParams p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ppdev::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + STAGES * STAGE_BYTES;
+  const uint32_t bars = base + STAGES * C::STAGE_BYTES;
   auto full_b = [&](int s) { return bars + 8 * s; };
   auto ready_b = [&](int s) { return bars + 8 * (STAGES + s); };
   auto empty_b = [&](int s) { return bars + 8 * (2 * STAGES + s); };
@@ -235,9 +243,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t done_b = bars + 8 * (3 * STAGES + 4);
   const uint32_t tmem_slot = bars + 8 * (3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (tmem_slot + 8 - base));
-  auto sA = [&](int s) { return base + s * STAGE_BYTES; };
-  auto sB = [&](int s) { return base + s * STAGE_BYTES + A_BYTES; };
-  auto sW = [&](int s) { return base + s * STAGE_BYTES + A_BYTES + B_BYTES; };
+  float* const ws_s = reinterpret_cast<float*>(gbase + STAGES * C::STAGE_BYTES + 256);  // [2][BN] weight scales
+  auto sA = [&](int s) { return base + s * C::STAGE_BYTES; };
+  auto sB = [&](int s) { return base + s * C::STAGE_BYTES + A_BYTES; };
+  auto sW = [&](int s) { return base + s * C::STAGE_BYTES + A_BYTES + C::B_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cta_rank();
@@ -252,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_b(b), 1);
-      mbar_init(acce_b(b), 2 * N_CONV_WARPS);
+      mbar_init(acce_b(b), 2 * N_DRAIN_WARPS);
     }
     mbar_init(done_b, 1);
     *abort_flag = 0;
@@ -261,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot),
-                 "r"(TMEM_COLS));
+                 "r"(C::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   tc_fence_before();
@@ -290,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int n_row = (t / p.num_m_tiles) * BN + (int)rank * (BN / 2);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_b(s), ph ^ 1)) { fail(); break; }
-          mbar_expect_tx(full_b(s), A_BYTES + W_BYTES);
+          mbar_expect_tx(full_b(s), A_BYTES + C::W_BYTES);
           tma_load_2d(sA(s), &tmA, kb * BK, m_row, full_b(s));
           tma_load_2d(sW(s), &tmW, kb * BK, n_row, full_b(s));
           issued[s] = 1;
@@ -323,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const int buf = g & 1;
           if (!mbar_wait(acce_b(buf), ((g >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
           tc_fence_after();
-          const uint32_t d = tmem + buf * 256;
+          const uint32_t d = tmem + buf * BN;
           const int kb0 = seg_k0, kb1 = min(ukb1, seg_k0 + p.seg_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(ready_b(s), ph)) { fail(); ok = false; break; }
@@ -347,37 +356,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp < CONV_WARP0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_ROLE));
-  } else {
-    // ---------------------------------------------------------------- converters + epilogue
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_CONV));
-    const int et = threadIdx.x - 32 * CONV_WARP0;  // 0..255
-    const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
-    const int colq = (warp - CONV_WARP0) >> 2;     // accumulator columns 128*colq .. +127
-    int32_t run[128];
-    int s = 0;
-    uint32_t ph = 0;
-    int done_kb = 0;      // k-blocks converted so far (all units)
-    int next_seg = 0;     // segments drained so far (all units; selects the accumulator buffer)
+  } else if (warp < DRAIN_WARP0) {
+    // ---------------------------------------------------------------- converters
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CONV));
+    const int et = threadIdx.x - 32 * CONV_WARP0;  // 0..127
     const Sched sc(p, cluster, n_clusters);
-    const int n_units = sc.units();
     int total_kb = 0;
-    for (int u = 0; u < n_units; ++u) {
+    for (int u = 0; u < sc.units(); ++u) {
       int t, a, b;
       sc.unit(u, t, a, b);
       total_kb += b - a;
     }
-    // drain cursor: segment dseg of unit du, whose k-blocks start at conversion index dbase
-    int du = 0, dseg = 0, dbase = 0, dtile = 0, dkb0 = 0, dkb1 = 0;
-    if (n_units > 0) sc.unit(0, dtile, dkb0, dkb1);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int kb = 0; kb < total_kb; ++kb) {
+      if (*abort_flag || !mbar_wait(full_b(s), ph)) { fail(); break; }
+      // widen this CTA's BN/2 weight rows x 64 k of int8 to fp16, UMMA layout
+      uint8_t* bt = gbase + (sB(s) - base);
+      const uint8_t* wt = gbase + (sW(s) - base);
+#pragma unroll
+      for (int i = 0; i < BN / 64; ++i) {
+        const int c = et + 128 * i;  // 16-byte int8 chunk: row c/4, k = 16*(c%4) ..
+        const int r = c >> 2, q = c & 3;
+        const uint4 w = *reinterpret_cast<const uint4*>(wt + r * 64 + q * 16);
+        uint4 o0, o1;
+        i8x4_to_f16x4(w.x, o0.x, o0.y);
+        i8x4_to_f16x4(w.y, o0.z, o0.w);
+        i8x4_to_f16x4(w.z, o1.x, o1.y);
+        i8x4_to_f16x4(w.w, o1.z, o1.w);
+        *reinterpret_cast<uint4*>(bt + sw128(r, 2 * q)) = o0;
+        *reinterpret_cast<uint4*>(bt + sw128(r, 2 * q + 1)) = o1;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(ready_b(s), 0);
+      if (++s == STAGES) { s = 0; ph ^= 1; }
+    }
+  } else {
+    // ---------------------------------------------------------------- drains + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_DRAIN));
+    constexpr int COLS = C::COLS;
+    const int et = threadIdx.x - 32 * DRAIN_WARP0;  // 0..255
+    const int quarter = warp & 3;                   // TMEM lanes 32*quarter .. +31
+    const int colq = (warp - DRAIN_WARP0) >> 2;     // accumulator columns COLS*colq .. +COLS-1
+    int32_t run[COLS];
     volatile int* last_flag = abort_flag + 1;
 
     // Fold segment g's complete f32 accumulator into the int32 running sums.
     auto drain = [&](int g, bool first) {  // `first`: the unit's first segment starts the running sums
       const int buf = g & 1;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * 256 + colq * 128;
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN + colq * COLS;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < COLS / 16; ++c) {
         uint32_t r[16];
         tmem_ld16(taddr + c * 16, r);
 #pragma unroll
@@ -399,22 +430,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int n_contrib = c_last - c_first + 1;
       const int row = quarter * 32 + lane;
       auto slot_ptr = [&](int slot) {
-        return p.part + ((((size_t)tile * p.max_slots + slot) * 2 + rank) * BM + row) * BN + colq * 128;
+        return p.part + ((((size_t)tile * p.max_slots + slot) * 2 + rank) * BM + row) * BN + colq * COLS;
       };
       int4* mine = reinterpret_cast<int4*>(slot_ptr(cluster - c_first));
 #pragma unroll
-      for (int j = 0; j < 32; ++j) mine[j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
+      for (int j = 0; j < COLS / 4; ++j) mine[j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
       __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_CONV_WARPS) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
       if (et == 0) *last_flag = atomicAdd(p.cnt + 2 * tile + rank, 1) == n_contrib - 1;
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_CONV_WARPS) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
       if (!*last_flag) return false;
       __threadfence();
       for (int sl = 0; sl < n_contrib; ++sl) {
         if (sl == cluster - c_first) continue;
         const int4* other = reinterpret_cast<const int4*>(slot_ptr(sl));
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < COLS / 4; ++j) {
           const int4 v = __ldcg(other + j);
           run[4 * j] += v.x;
           run[4 * j + 1] += v.y;
@@ -428,111 +459,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
     // Epilogue of a finished tile in chunks of 16 output columns (32 accumulator
     // columns for SwiGLU): (float(acc) * w_scale) * a_scale, then store,
-    // residual add or SwiGLU. Rows past M are skipped.
-    int epi_left = 0, epi_row0 = 0, epi_n0 = 0;
-    constexpr int EPI_CHUNKS = EPI == EPI_SWIGLU ? 4 : 8;
-    auto epi_chunk = [&](int c) {
-      const int row = epi_row0 + lane;
+    // residual add or SwiGLU. Rows past M are skipped. wsv: this warp's COLS
+    // weight scales in shared memory; a_s: the row's activation scale.
+    auto epilogue = [&](int row, int n0, const float* wsv, float a_s) {
       if (row >= p.M) return;
       if (EPI == EPI_ACC) {
-        int4* dst = reinterpret_cast<int4*>(p.acc_out + (size_t)row * p.N + epi_n0 + 16 * c);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_int4(run[16 * c + 4 * k], run[16 * c + 4 * k + 1], run[16 * c + 4 * k + 2], run[16 * c + 4 * k + 3]);
+        for (int c = 0; c < COLS / 16; ++c) {
+          int4* dst = reinterpret_cast<int4*>(p.acc_out + (size_t)row * p.N + n0 + 16 * c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_int4(run[16 * c + 4 * k], run[16 * c + 4 * k + 1], run[16 * c + 4 * k + 2], run[16 * c + 4 * k + 3]);
+        }
         return;
       }
-      const float a_s = p.as[row];
-      float v[16];
       if (EPI == EPI_SWIGLU) {
+        // accumulator columns come in blocks of 16 gate rows then 16 up rows
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int cg = 32 * c + i;
-          v[i] = ppdev::silu_mul(ppdev::dequant(run[cg], __ldg(p.ws + epi_n0 + cg), a_s),
-                                 ppdev::dequant(run[cg + 16], __ldg(p.ws + epi_n0 + cg + 16), a_s));
+        for (int c = 0; c < COLS / 32; ++c) {
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int cg = 32 * c + i;
+            v[i] = ppdev::silu_mul(ppdev::dequant(run[cg], wsv[cg], a_s), ppdev::dequant(run[cg + 16], wsv[cg + 16], a_s));
+          }
+          float4* dst = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + n0 / 2 + 16 * c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         }
-        float4* dst = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + epi_n0 / 2 + 16 * c);
+        return;
+      }
+      float4* rowp = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + n0);
+      float4 xr[4];
+      if (EPI == EPI_RESID) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-      } else {
+        for (int k = 0; k < 4; ++k) xr[k] = rowp[k];
+      }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = ppdev::dequant(run[16 * c + i], __ldg(p.ws + epi_n0 + 16 * c + i), a_s);
-        float4* dst = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + epi_n0 + 16 * c);
+      for (int c = 0; c < COLS / 16; ++c) {
+        float4 xn[4];
+        if (EPI == EPI_RESID && c + 1 < COLS / 16) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) xn[k] = rowp[4 * (c + 1) + k];  // next chunk's residual, loaded ahead
+        }
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = ppdev::dequant(run[16 * c + i], wsv[16 * c + i], a_s);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-          if (EPI == EPI_RESID) {
-            const float4 x = dst[k];
-            o = make_float4(__fadd_rn(x.x, o.x), __fadd_rn(x.y, o.y), __fadd_rn(x.z, o.z), __fadd_rn(x.w, o.w));
-          }
-          dst[k] = o;
+          if (EPI == EPI_RESID)
+            o = make_float4(__fadd_rn(xr[k].x, o.x), __fadd_rn(xr[k].y, o.y), __fadd_rn(xr[k].z, o.z),
+                            __fadd_rn(xr[k].w, o.w));
+          rowp[4 * c + k] = o;
+        }
+        if (EPI == EPI_RESID && c + 1 < COLS / 16) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) xr[k] = xn[k];
         }
       }
-    };
-    auto epi_next = [&]() {  // the next pending chunk (each branch has compile-time indices)
-      const int c = EPI_CHUNKS - epi_left;
-#pragma unroll
-      for (int k = 0; k < EPI_CHUNKS; ++k)
-        if (k == c) epi_chunk(k);
-      --epi_left;
     };
 
-    int since_epi = 0;
-    long long idle_since = clock64();
-    while (true) {
-      bool progressed = false;
-      const bool seg_done = du < n_units && dbase + min(dkb1 - dkb0, (dseg + 1) * p.seg_kb) - 1 < done_kb &&
-                            mbar_test_warp(accf_b(next_seg & 1), (next_seg >> 1) & 1);
-      if (seg_done && epi_left == 0) {
-        drain(next_seg++, dseg == 0);
-        ++dseg;
-        if (dkb0 + dseg * p.seg_kb >= dkb1) {  // the unit is complete
-          const bool whole = dkb0 == 0 && dkb1 == nkb;
-          if (whole || finish_partial(dtile)) {  // queue the tile's epilogue
-            epi_row0 = (dtile % p.num_m_tiles) * 2 * BM + (int)rank * BM + quarter * 32;
-            epi_n0 = (dtile / p.num_m_tiles) * BN + colq * 128;
-            epi_left = EPI_CHUNKS;
-            since_epi = EPI_EVERY;
-          }
-          dbase += dkb1 - dkb0;
-          dseg = 0;
-          if (++du < n_units) sc.unit(du, dtile, dkb0, dkb1);
-        }
-        progressed = true;
-      } else if (epi_left > 0 && (seg_done || since_epi >= EPI_EVERY || done_kb == total_kb)) {
-        epi_next();  // a finished tile's sums must be written before the next drain reuses them
-        since_epi = 0;
-        progressed = true;
-      } else if (done_kb < total_kb && mbar_test_warp(full_b(s), ph)) {
-        // widen this CTA's 128 weight rows x 64 k of int8 to fp16, UMMA layout
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = et + 256 * i;  // 16-byte int8 chunk: row c/4, k = 16*(c%4) ..
-          const int r = c >> 2, q = c & 3;
-          const uint4 w = *reinterpret_cast<const uint4*>(gbase + (sW(s) - base) + r * 64 + q * 16);
-          uint4 o0, o1;
-          i8x4_to_f16x4(w.x, o0.x, o0.y);
-          i8x4_to_f16x4(w.y, o0.z, o0.w);
-          i8x4_to_f16x4(w.z, o1.x, o1.y);
-          i8x4_to_f16x4(w.w, o1.z, o1.w);
-          uint8_t* bt = gbase + (sB(s) - base);
-          *reinterpret_cast<uint4*>(bt + sw128(r, 2 * q)) = o0;
-          *reinterpret_cast<uint4*>(bt + sw128(r, 2 * q + 1)) = o1;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(ready_b(s), 0);
-        if (++s == STAGES) { s = 0; ph ^= 1; }
-        ++done_kb;
-        ++since_epi;
-        progressed = true;
+    const Sched sc(p, cluster, n_clusters);
+    int g = 0;  // segments drained so far (selects the accumulator buffer and its phase)
+    bool ok = true;
+    for (int u = 0; u < sc.units() && ok; ++u) {
+      int t, kb0, kb1;
+      sc.unit(u, t, kb0, kb1);
+      const int row = (t % p.num_m_tiles) * 2 * BM + (int)rank * BM + quarter * 32 + lane;
+      // scales for the epilogue, loaded now so their latency hides behind the mainloop
+      const int ncol = (t / p.num_m_tiles) * BN + et;  // et < BN: this thread's weight scale of the tile
+      const float ws_r = (EPI != EPI_ACC && et < BN && ncol < p.N) ? __ldg(p.ws + ncol) : 0.f;
+      const float as_r = (EPI != EPI_ACC && row < p.M) ? __ldg(p.as + row) : 0.f;
+      for (int k0 = kb0; k0 < kb1; k0 += p.seg_kb, ++g) {
+        if (*abort_flag || !mbar_wait(accf_b(g & 1), (g >> 1) & 1)) { fail(); ok = false; break; }
+        drain(g, k0 == kb0);
       }
-      if (done_kb == total_kb && du == n_units && epi_left == 0) break;
-      if (progressed) {
-        idle_since = clock64();
-      } else {
-        if (*abort_flag || clock64() - idle_since > WAIT_CYCLES) { fail(); break; }
-        __nanosleep(20);
-      }
+      if (!ok) break;
+      float* wsb = ws_s + (u & 1) * BN;  // two buffers: unit u+1 writes the other one
+      if (et < BN) wsb[et] = ws_r;
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
+      const bool whole = kb0 == 0 && kb1 == nkb;
+      if (whole || finish_partial(t)) epilogue(row, (t / p.num_m_tiles) * BN + colq * COLS, wsb + colq * COLS, as_r);
     }
   }
 
@@ -542,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
   }
 }
 
@@ -558,23 +566,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
+// Co-resident CTA pairs of the widest configuration (one pair per 2 SMs).
 int max_clusters() {
   static int n = 0;
   if (!n) {
+    using C = Cfg<256>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.attrs = attr;
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.numAttrs = 0;  // the kernel declares its cluster shape
     int c = 0;
-    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (cudaOccupancyMaxActiveClusters(&c, k_gemm_tc<EPI_STORE>, &cfg) != cudaSuccess || c <= 0) {
+    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (cudaOccupancyMaxActiveClusters(&c, k_gemm_tc<EPI_STORE, 256>, &cfg) != cudaSuccess || c <= 0) {
       cudaGetLastError();
       int dev = 0, sms = 0;
       cudaGetDevice(&dev);
@@ -586,16 +590,26 @@ int max_clusters() {
   return n;
 }
 
-template <int EPI>
+template <int EPI, int BN>
 cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters, cudaStream_t s) {
+  using C = Cfg<BN>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_tc<EPI><<<2 * clusters, THREADS, SMEM_BYTES, s>>>(ma, mw, p);
+  k_gemm_tc<EPI, BN><<<2 * clusters, THREADS, C::SMEM_BYTES, s>>>(ma, mw, p);
   return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_bn(int bn, const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters,
+                      cudaStream_t s) {
+  if (bn == 256) return launch_t<EPI, 256>(ma, mw, p, clusters, s);
+  if (bn == 192) return launch_t<EPI, 192>(ma, mw, p, clusters, s);
+  if (bn == 128) return launch_t<EPI, 128>(ma, mw, p, clusters, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -621,12 +635,13 @@ cudaError_t make_tmap_a(CUtensorMap* map, const __half* a16, int rows, int k) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k) {
+cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k, int bn) {
   auto enc = encoder();
   if (!enc) return cudaErrorNotSupported;
+  if (bn != 256 && bn != 192 && bn != 128) return cudaErrorInvalidValue;
   cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)n};
   cuuint64_t strides[1] = {(cuuint64_t)k};
-  cuuint32_t box[2] = {BK, BN / 2};
+  cuuint32_t box[2] = {BK, (cuuint32_t)(bn / 2)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(w), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -634,19 +649,42 @@ cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tile width for an m x n x k GEMM: among the widths that divide n, the one
+// whose waves of tiles over the CTA pairs cost the fewest weight columns per
+// pair (ceil(tiles / pairs) x width); ties go to the wider tile. Shapes that
+// stream-K covers (few tiles, long k) keep the widest tile.
+int tc_bn(int m, int n, int k) {
+  const int mc = max_clusters();
+  const int nmt = (m + 2 * BM - 1) / (2 * BM);
+  int best = 0;
+  long long best_cost = 0;
+  for (int bn : {256, 192, 128}) {
+    if (n % bn) continue;
+    const long long tiles = (long long)nmt * (n / bn);
+    const long long cost = (tiles + mc - 1) / mc * bn;
+    if (!best || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 namespace {
 
 // Stream-K plan of one GEMM (ipc == 0: whole tiles round robin).
 struct Plan {
-  int num_tiles, clusters, ipc, max_slots;
+  int bn, num_tiles, clusters, ipc, max_slots;
   size_t part_elems;
 };
 
 Plan plan(int m, int n, int k) {
   Plan pl{};
+  pl.bn = tc_bn(m, n, k);
+  if (!pl.bn) return pl;
   const int nmt = (m + 2 * BM - 1) / (2 * BM);
   const int nkb = k / BK;
-  pl.num_tiles = nmt * (n / BN);
+  pl.num_tiles = nmt * (n / pl.bn);
   const int mc = max_clusters();
   if (pl.num_tiles >= 2 * mc || pl.num_tiles * nkb < 2 * mc) {
     pl.clusters = std::min(pl.num_tiles, mc);
@@ -661,7 +699,7 @@ Plan plan(int m, int n, int k) {
   }
   pl.clusters = (int)((total + pl.ipc - 1) / pl.ipc);
   pl.max_slots = (nkb + pl.ipc - 1) / pl.ipc + 1;
-  pl.part_elems = (size_t)pl.num_tiles * pl.max_slots * 2 * BM * BN;
+  pl.part_elems = (size_t)pl.num_tiles * pl.max_slots * 2 * BM * pl.bn;
   return pl;
 }
 
@@ -673,9 +711,9 @@ void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters
   *counters = pl.ipc ? (size_t)pl.num_tiles * 2 : 0;
 }
 
-cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, const float* ws, const float* as,
-                           int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k, int* status,
-                           const TcWorkspace& wsp, cudaStream_t s) {
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
+                           const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
+                           int* status, const TcWorkspace& wsp, cudaStream_t s) {
   TcParams p{};
   p.M = m;
   p.N = n;
@@ -689,6 +727,7 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
   p.acc_out = acc;
   p.status = status;
   Plan pl = plan(m, n, k);
+  if (!pl.bn || pl.bn != bn) return cudaErrorInvalidValue;  // the weight map was made for another tile width
   p.num_tiles = pl.num_tiles;
   if (pl.ipc && wsp.part && wsp.cnt && wsp.part_bytes >= pl.part_elems * sizeof(int32_t) &&
       wsp.counters >= (size_t)pl.num_tiles * 2) {
@@ -700,10 +739,10 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
     pl.clusters = std::min(pl.num_tiles, max_clusters());  // no workspace: whole tiles
   }
   switch (epi) {
-    case EPI_STORE: return launch_t<EPI_STORE>(ma, mw, p, pl.clusters, s);
-    case EPI_RESID: return launch_t<EPI_RESID>(ma, mw, p, pl.clusters, s);
-    case EPI_SWIGLU: return launch_t<EPI_SWIGLU>(ma, mw, p, pl.clusters, s);
-    case EPI_ACC: return launch_t<EPI_ACC>(ma, mw, p, pl.clusters, s);
+    case EPI_STORE: return launch_bn<EPI_STORE>(bn, ma, mw, p, pl.clusters, s);
+    case EPI_RESID: return launch_bn<EPI_RESID>(bn, ma, mw, p, pl.clusters, s);
+    case EPI_SWIGLU: return launch_bn<EPI_SWIGLU>(bn, ma, mw, p, pl.clusters, s);
+    case EPI_ACC: return launch_bn<EPI_ACC>(bn, ma, mw, p, pl.clusters, s);
     default: return cudaErrorInvalidValue;
   }
 }

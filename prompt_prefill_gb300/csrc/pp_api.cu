@@ -263,10 +263,11 @@ int tc_segment() { return g_tc_seg.load(); }
 int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* ws, const int8_t* w, int M, int N,
          int K, float* out, int ldo) {
   if (m->engine == PP_GEMM_TC) {
-    const CUtensorMap& wm = m->wmap[(size_t)mg * 4 + which];
+    const int bi = tc_bn_index(M, N, K);
+    const CUtensorMap& wm = m->wmap[((size_t)mg * 4 + which) * 3 + bi];
     const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
     return launch(m, PP_KERNEL_GEMM, st, [&] {
-      return launch_gemm_tc(epi, am, wm, ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
+      return launch_gemm_tc(epi, am, wm, kTcBn[bi], ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
                             st);
     });
   }
@@ -279,12 +280,15 @@ int make_weight_maps(pp_model* m, const uint8_t* block) {
   const pp_config& c = m->cfg;
   const LayerPtrs L = layer_ptrs(m->lay, block);
   const int D = c.dim, QD = c.n_heads * c.head_dim, QKV = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn;
-  CUtensorMap t[4];
-  PP_CUDA(make_tmap_w(&t[0], L.wqkv, QKV, D));
-  PP_CUDA(make_tmap_w(&t[1], L.wo, D, QD));
-  PP_CUDA(make_tmap_w(&t[2], L.wgu, 2 * F, D));
-  PP_CUDA(make_tmap_w(&t[3], L.wd, D, F));
-  for (auto& x : t) m->wmap.push_back(x);
+  // one map per tile width: the width a launch uses depends on its chunk's row count
+  const int8_t* w[4] = {L.wqkv, L.wo, L.wgu, L.wd};
+  const int n[4] = {QKV, D, 2 * F, D}, k[4] = {D, QD, D, F};
+  for (int i = 0; i < 4; ++i)
+    for (int b = 0; b < 3; ++b) {
+      CUtensorMap t;
+      PP_CUDA(make_tmap_w(&t, w[i], n[i], k[i], kTcBn[b]));
+      m->wmap.push_back(t);
+    }
   return PP_OK;
 }
 
@@ -320,9 +324,13 @@ int validate_cfg(const pp_config* c) {
 int load_impl(pp_model* m, const pp_weights* w) {
   const pp_config& c = m->cfg;
   PP_CUDA(cudaGetDevice(&m->device));
-  const bool tc = tc_available();
+  // the tcgen05 engine tiles weight rows in multiples of 128
+  const int qkv_rows = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const bool tc_shapes = qkv_rows % 128 == 0 && c.dim % 128 == 0 && (2 * c.ffn) % 128 == 0;
+  const bool tc = tc_available() && tc_shapes;
   if (c.gemm_engine == PP_GEMM_TC && !tc) {
-    set_err("the tcgen05 engine needs an sm_103 device");
+    set_err(tc_shapes ? "the tcgen05 engine needs an sm_103 device"
+                      : "the tcgen05 engine needs (H + 2 Hkv) hd, dim and 2 ffn to be multiples of 128");
     return PP_ERR_UNSUPPORTED;
   }
   if (c.gemm_engine != PP_GEMM_AUTO && c.gemm_engine != PP_GEMM_MMA && c.gemm_engine != PP_GEMM_TC) {
@@ -821,8 +829,8 @@ static int check_gemm(int32_t engine, const int8_t* a8, const uint16_t* a16, con
   }
   if (engine == PP_GEMM_TC) {
     if (!tc_available()) { set_err("the tcgen05 engine needs an sm_103 device"); return PP_ERR_UNSUPPORTED; }
-    if (!a16 || n % 256 || (reinterpret_cast<uintptr_t>(a16) & 15) || (reinterpret_cast<uintptr_t>(w) & 15)) {
-      set_err("the tcgen05 engine needs fp16 activations, n %% 256 == 0 and 16-byte aligned operands");
+    if (!a16 || n % 128 || (reinterpret_cast<uintptr_t>(a16) & 15) || (reinterpret_cast<uintptr_t>(w) & 15)) {
+      set_err("the tcgen05 engine needs fp16 activations, n %% 128 == 0 and 16-byte aligned operands");
       return PP_ERR_ARG;
     }
     return PP_OK;
@@ -866,12 +874,13 @@ static cudaError_t op_gemm_launch(int32_t engine, int epi, const int8_t* a8, con
   CUtensorMap ma, mw;
   cudaError_t e = make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k);
   if (e != cudaSuccess) return e;
-  e = make_tmap_w(&mw, w, n, k);
+  const int bn = tc_bn(m, n, k);
+  e = make_tmap_w(&mw, w, n, k, bn);
   if (e != cudaSuccess) return e;
   TcWorkspace wsp;
   e = op_workspace(m, n, k, &wsp);
   if (e != cudaSuccess) return e;
-  return launch_gemm_tc(epi, ma, mw, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), nullptr, wsp, st);
+  return launch_gemm_tc(epi, ma, mw, bn, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), nullptr, wsp, st);
 }
 
 int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
@@ -971,13 +980,14 @@ int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, c
   if (need_cnt) PP_CUDA(cudaMemsetAsync(sc.cnt, 0, need_cnt * sizeof(int), st));
   CUtensorMap ma, mw;
   PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
-  PP_CUDA(make_tmap_w(&mw, w, n, k));
+  const int bn = tc_bn(m, n, k);
+  PP_CUDA(make_tmap_w(&mw, w, n, k, bn));
   TcWorkspace wsp;
   wsp.part = sc.part;
   wsp.part_bytes = kStaticPartBytes;
   wsp.cnt = sc.cnt;
   wsp.counters = kStaticCounters;
-  return ok_launch(launch_gemm_tc(epilogue, ma, mw, w_scale, a_scale, m, n, k, out, ldo, nullptr, g_tc_seg.load(),
+  return ok_launch(launch_gemm_tc(epilogue, ma, mw, bn, w_scale, a_scale, m, n, k, out, ldo, nullptr, g_tc_seg.load(),
                                   nullptr, wsp, st),
                    "gemm_noalloc");
 }

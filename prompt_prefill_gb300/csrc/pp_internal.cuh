@@ -36,10 +36,17 @@ cudaError_t launch_gemm_mma(int epi, const int8_t* a8, const int8_t* w, const fl
                             int n, int k, float* out, int ldo, int32_t* acc, cudaStream_t s);
 
 // tcgen05 engine (k_gemm_tc.cu): a16 [m][k] fp16 codes via a tensor map, w [n][k] int8 via a tensor map.
-// n % 256 == 0, k % 64 == 0; exact f32 segments of seg_k (<= 1024) along k.
+// n % 128 == 0, k % 64 == 0; exact f32 segments of seg_k (<= 1024) along k. The weight map's box
+// is made for one tile width bn (256, 192 or 128): the one tc_bn(m, n, k) picks for the launch.
 bool tc_available();
+constexpr int kTcBn[3] = {256, 192, 128};
+int tc_bn(int m, int n, int k);
+inline int tc_bn_index(int m, int n, int k) {
+  const int bn = tc_bn(m, n, k);
+  return bn == 256 ? 0 : (bn == 192 ? 1 : 2);
+}
 cudaError_t make_tmap_a(CUtensorMap* map, const __half* a16, int rows, int k);
-cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k);
+cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k, int bn);
 // Stream-K workspace: int32 partial tiles and per-tile counters (zero between launches).
 struct TcWorkspace {
   int32_t* part = nullptr;
@@ -49,9 +56,9 @@ struct TcWorkspace {
 };
 // Workspace a GEMM of this shape uses (0 when it runs whole tiles).
 void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters);
-cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, const float* ws, const float* as,
-                           int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k, int* status,
-                           const TcWorkspace& wsp, cudaStream_t s);
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
+                           const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
+                           int* status, const TcWorkspace& wsp, cudaStream_t s);
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)

@@ -35,7 +35,12 @@ def _acc(torch, engine, a, w):
 
 
 TC_SHAPES = [(1, 256, 64), (8, 768, 256), (37, 256, 768), (130, 512, 320), (200, 2048, 1024), (300, 512, 4096),
-             (512, 1024, 14336), (600, 768, 2048)]
+             (512, 1024, 14336), (600, 768, 2048), (33, 384, 704)]
+
+# One shape per tile width on 76 CTA pairs: a weight-row tile of 256 (76 tiles
+# of 256 cost as much as 152 of 128), of 192 (76 tiles of 192 beat 114 of 128)
+# and of 128 (few tiles).
+WIDTH_SHAPES = [(16, 19456, 128), (40, 14592, 192), (290, 512, 1024)]
 
 
 @pytest.mark.parametrize("m,n,k", TC_SHAPES)
@@ -84,9 +89,16 @@ def test_tc_and_mma_engines_agree_at_8b_shapes(torch):
             assert tc[t, r] == oracle.dot_i8(a[t], w[r])
 
 
+@pytest.mark.parametrize("m,n,k", WIDTH_SHAPES)
+def test_tc_acc_bit_exact_every_tile_width(torch, m, n, k):
+    a = synth.uniform_i8(88, m + k, (m, k))
+    w = synth.uniform_i8(88, n + k, (n, k))
+    assert np.array_equal(_acc(torch, TC, a, w), oracle.gemm_i8(a, w))
+
+
+@pytest.mark.parametrize("m,n,k", WIDTH_SHAPES)
 @pytest.mark.parametrize("epi", [pp.PP_EPI_STORE, pp.PP_EPI_RESID])
-def test_tc_epilogue_bit_exact(torch, epi):
-    m, n, k = 290, 512, 1024
+def test_tc_epilogue_bit_exact(torch, epi, m, n, k):
     a = synth.uniform_i8(86, 1, (m, k))
     w = synth.uniform_i8(86, 2, (n, k))
     ws = synth.uniform_f32(86, 3, (n,), 1e-4, 2e-3)
@@ -100,8 +112,8 @@ def test_tc_epilogue_bit_exact(torch, epi):
     assert np.array_equal(bits(host(out)), bits(ref))
 
 
-def test_tc_swiglu(torch):
-    m, F, k = 70, 256, 512
+@pytest.mark.parametrize("m,F,k", [(70, 256, 512), (16, 9728, 128), (40, 7296, 192)])
+def test_tc_swiglu(torch, m, F, k):
     a = synth.uniform_i8(87, 1, (m, k))
     wg = synth.uniform_i8(87, 2, (F, k))
     wu = synth.uniform_i8(87, 3, (F, k))
@@ -129,7 +141,7 @@ def test_tc_shape_errors(torch):
     t16 = empty((1024,), torch.float16)
     acc = empty((1024,), torch.int32)
     with pytest.raises(pp.PPError) as e:
-        pp.pp_op_gemm_acc(TC, t8, t16, t8, 4, 128, 64, acc)  # n % 256 != 0
+        pp.pp_op_gemm_acc(TC, t8, t16, t8, 4, 96, 64, acc)  # n % 128 != 0
     assert e.value.status == pp.PP_ERR_ARG
     with pytest.raises(pp.PPError):
         pp.pp_set_exact_segment(2048)  # would overflow the exact f32 range
