@@ -56,6 +56,13 @@ extern "C" {
 #define PP_MODE_RESIDENT 0  /* every layer resident in HBM */
 #define PP_MODE_STREAMED 1  /* layers in pinned host memory, streamed into a device ring */
 
+/* Loop order of one prefill call ("Batched Prefill" section "The Solution":
+ * chunks of the prompt swept through each layer; "Single-pass prefill":
+ * stream each layer once for the whole prompt). Both give the same bits. */
+#define PP_LOOP_CHUNK_OUTER 0 /* for each chunk, for each layer: scratch for max_chunk rows */
+#define PP_LOOP_LAYER_OUTER 1 /* for each layer, for each chunk: every layer is fetched (streamed mode: copied
+                                 from the host) once per call; keeps the residual stream of max_seq rows */
+
 #define PP_GEMM_AUTO 0      /* fastest engine that passed its self-check on this device */
 #define PP_GEMM_MMA 1       /* warp-level mma.sync s8 x s8 -> s32 */
 #define PP_GEMM_TC 2        /* tcgen05 exact-integer GEMM (fp16 operands, f32 TMEM, int32 drain) */
@@ -92,7 +99,7 @@ typedef struct pp_config {
   int32_t mode;         /* PP_MODE_RESIDENT or PP_MODE_STREAMED */
   int32_t ring_slots;   /* streamed mode: 2 = double-buffer prefetch ring, 1 = synchronous single buffer */
   int32_t gemm_engine;  /* PP_GEMM_* */
-  int32_t use_graphs;   /* resident mode: replay each chunk length's layer loop as a CUDA graph */
+  int32_t loop_order;   /* PP_LOOP_CHUNK_OUTER or PP_LOOP_LAYER_OUTER */
   int32_t profile_kernel; /* PP_KERNEL_* class to time with events around each launch, or PP_KERNEL_NONE */
 } pp_config;
 
@@ -119,10 +126,11 @@ typedef struct pp_stats {
   int64_t tokens;             /* prompt positions processed */
   int64_t weight_bytes_read;  /* int8 weight + scale bytes the kernels fetch by design: every layer once
                                  per chunk, the output projection once per call ("Streamed" bytes) */
-  int64_t h2d_bytes;          /* host-to-device bytes: token ids, and layer copies in streamed mode */
+  int64_t h2d_bytes;          /* host-to-device bytes: token ids, and layer copies in streamed mode (once per
+                                 layer per chunk chunk-outer, once per layer per call layer-outer) */
   int64_t prefetch_hits;      /* streamed mode: layer copy finished before the compute stream needed it */
   int64_t prefetch_misses;    /* streamed mode: compute waited on the copy (includes each call's first layer) */
-  int64_t kernel_launches;    /* kernels this library launched (graph replays count their kernels) */
+  int64_t kernel_launches;    /* kernels this library launched */
   int64_t prof_launches;      /* launches of the profiled kernel class */
   double prof_ms;             /* summed event-timed duration of those launches */
 } pp_stats;

@@ -23,9 +23,11 @@ LIB_PATH = os.path.join(_HERE, "libpp.so")
 PP_OK, PP_ERR_ARG, PP_ERR_CAPACITY, PP_ERR_OOM, PP_ERR_CUDA, PP_ERR_DEVICE_TIMEOUT, PP_ERR_UNSUPPORTED = (
     0, -1, -2, -3, -4, -5, -6)
 PP_MODE_RESIDENT, PP_MODE_STREAMED = 0, 1
+PP_LOOP_CHUNK_OUTER, PP_LOOP_LAYER_OUTER = 0, 1
 PP_GEMM_AUTO, PP_GEMM_MMA, PP_GEMM_TC = 0, 1, 2
 (PP_KERNEL_NONE, PP_KERNEL_GEMM, PP_KERNEL_ATTENTION, PP_KERNEL_NORM_QUANT, PP_KERNEL_ROPE_KV, PP_KERNEL_LM_HEAD,
  PP_KERNEL_EMBED) = (-1, 0, 1, 2, 3, 4, 5)
+PP_KERNEL_COUNT = 6
 KERNEL_NAMES = {0: "gemm", 1: "attention", 2: "norm_quant", 3: "rope_kv", 4: "lm_head", 5: "embed"}
 PP_EPI_STORE, PP_EPI_RESID, PP_EPI_SWIGLU = 0, 1, 2
 
@@ -40,7 +42,7 @@ class pp_config(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_int32) for n in ("dim", "n_layers", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab")]
                 + [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
                 + [(n, ctypes.c_int32) for n in ("max_seq", "max_chunk", "mode", "ring_slots", "gemm_engine",
-                                                  "use_graphs", "profile_kernel")])
+                                                  "loop_order", "profile_kernel")])
 
 
 class pp_weights(ctypes.Structure):
@@ -153,9 +155,9 @@ def _stream(stream) -> int | None:
 # ---------------------------------------------------------------- model API
 def make_config(dim, n_layers, n_heads, n_kv_heads, head_dim, ffn, vocab, rms_eps=1e-5, rope_theta=10000.0,
                 max_seq=4096, max_chunk=512, mode=PP_MODE_RESIDENT, ring_slots=2, gemm_engine=PP_GEMM_AUTO,
-                use_graphs=0, profile_kernel=PP_KERNEL_NONE) -> pp_config:
+                loop_order=PP_LOOP_CHUNK_OUTER, profile_kernel=PP_KERNEL_NONE) -> pp_config:
     return pp_config(dim, n_layers, n_heads, n_kv_heads, head_dim, ffn, vocab, rms_eps, rope_theta, max_seq,
-                     max_chunk, mode, ring_slots, gemm_engine, use_graphs, profile_kernel)
+                     max_chunk, mode, ring_slots, gemm_engine, loop_order, profile_kernel)
 
 
 def make_weights(tok_emb, w, w_scale, attn_norm, ffn_norm, final_norm, w_out, w_out_scale):
@@ -313,12 +315,12 @@ class PrefillModel:
     """A loaded model: owns the pp_model handle (freed on close)."""
 
     def __init__(self, shape, weights, max_seq=4096, max_chunk=512, mode=PP_MODE_RESIDENT, ring_slots=2,
-                 gemm_engine=PP_GEMM_AUTO, use_graphs=0, profile_kernel=PP_KERNEL_NONE):
+                 gemm_engine=PP_GEMM_AUTO, loop_order=PP_LOOP_CHUNK_OUTER, profile_kernel=PP_KERNEL_NONE):
         """shape: any object with the ModelShape fields; weights: any object with
         tok_emb, w, w_scale, attn_norm, ffn_norm, final_norm, w_out, w_out_scale (host arrays)."""
         self.cfg = make_config(shape.dim, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                                shape.vocab, shape.rms_eps, shape.rope_theta, max_seq, max_chunk, mode, ring_slots,
-                               gemm_engine, use_graphs, profile_kernel)
+                               gemm_engine, loop_order, profile_kernel)
         ws, keep = make_weights(weights.tok_emb, weights.w, weights.w_scale, weights.attn_norm, weights.ffn_norm,
                                 weights.final_norm, weights.w_out, weights.w_out_scale)
         self.h = pp_model_load(self.cfg, ws)

@@ -62,7 +62,11 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 //   r = 1 / sqrt(sum(x^2)/k + eps), y = (x * r) * g            (NORM only)
 //   amax = max|y|, inv = 127/amax, q = clamp(rint_even(y*inv), +-127), a_scale = amax/127
 // All f32 with IEEE division and square root; amax == 0 gives q = 0, a_scale = 0.
-template <bool NORM>
+// NV > 0: the thread's NV float4 of the row are loaded once and kept in
+// registers for all three passes (k <= 4 * NV * kRowThreads); NV == 0 streams
+// the row from memory in each pass (any k). Every pass visits the thread's
+// elements in the same order, so both forms give the same bits.
+template <bool NORM, int NV>
 __global__ void __launch_bounds__(kRowThreads)
     k_norm_quant(const float* __restrict__ x, int ldx, const float* __restrict__ g, int k, float eps,
                  float* __restrict__ y_out, int8_t* __restrict__ q8, __half* __restrict__ q16,
@@ -72,34 +76,51 @@ __global__ void __launch_bounds__(kRowThreads)
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
   const float4* g4 = reinterpret_cast<const float4*>(g);
   const int k4 = k >> 2;
+  constexpr int NR = NV > 0 ? NV : 1;
+  float4 xv[NR];
+  if (NV > 0) {
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      const int c = threadIdx.x + j * kRowThreads;
+      if (c < k4) xv[j] = xr[c];
+    }
+  }
+  auto for_each = [&](auto&& f) {  // f(x[4c .. 4c+3], c) for this thread's c in increasing order
+    if (NV > 0) {
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        const int c = threadIdx.x + j * kRowThreads;
+        if (c < k4) f(xv[j], c);
+      }
+    } else {
+      for (int c = threadIdx.x; c < k4; c += kRowThreads) f(xr[c], c);
+    }
+  };
   float r = 1.f;
   if (NORM) {
     float ss = 0.f;
-    for (int c = threadIdx.x; c < k4; c += kRowThreads) {
-      const float4 v = xr[c];
+    for_each([&](const float4& v, int) {
       ss = fmaf(v.x, v.x, ss);
       ss = fmaf(v.y, v.y, ss);
       ss = fmaf(v.z, v.z, ss);
       ss = fmaf(v.w, v.w, ss);
-    }
+    });
     ss = block_sum(ss, red);
     r = 1.0f / sqrtf(ss / (float)k + eps);
   }
-  auto yval = [&](float xv, float gv) { return NORM ? __fmul_rn(__fmul_rn(xv, r), gv) : xv; };
+  auto yval = [&](float xv_, float gv) { return NORM ? __fmul_rn(__fmul_rn(xv_, r), gv) : xv_; };
   float amax = 0.f;
-  for (int c = threadIdx.x; c < k4; c += kRowThreads) {
-    const float4 v = xr[c];
+  for_each([&](const float4& v, int c) {
     const float4 gg = NORM ? g4[c] : make_float4(1.f, 1.f, 1.f, 1.f);
     amax = fmaxf(amax, fabsf(yval(v.x, gg.x)));
     amax = fmaxf(amax, fabsf(yval(v.y, gg.y)));
     amax = fmaxf(amax, fabsf(yval(v.z, gg.z)));
     amax = fmaxf(amax, fabsf(yval(v.w, gg.w)));
-  }
+  });
   amax = block_max(amax, red);
   const bool zero = amax == 0.f;
   const float inv = zero ? 0.f : 127.0f / amax;
-  for (int c = threadIdx.x; c < k4; c += kRowThreads) {
-    const float4 v = xr[c];
+  for_each([&](const float4& v, int c) {
     const float4 gg = NORM ? g4[c] : make_float4(1.f, 1.f, 1.f, 1.f);
     float y[4] = {yval(v.x, gg.x), yval(v.y, gg.y), yval(v.z, gg.z), yval(v.w, gg.w)};
     int qi[4];
@@ -118,7 +139,7 @@ __global__ void __launch_bounds__(kRowThreads)
       reinterpret_cast<__half2*>(q16 + base)[1] = h23;
     }
     if (y_out) reinterpret_cast<float4*>(y_out + base)[0] = make_float4(y[0], y[1], y[2], y[3]);
-  }
+  });
   if (threadIdx.x == 0) a_scale[row] = zero ? 0.f : amax / 127.0f;
 }
 
@@ -220,10 +241,17 @@ cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab,
 
 cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
                               int8_t* q8, __half* q16, float* a_scale, cudaStream_t s) {
-  if (g)
-    k_norm_quant<true><<<rows, kRowThreads, 0, s>>>(x, ldx, g, k, eps, y, q8, q16, a_scale);
-  else
-    k_norm_quant<false><<<rows, kRowThreads, 0, s>>>(x, ldx, g, k, eps, y, q8, q16, a_scale);
+  const int nv = (k / 4 + kRowThreads - 1) / kRowThreads;  // float4 per thread
+  auto go = [&](auto kern) { kern<<<rows, kRowThreads, 0, s>>>(x, ldx, g, k, eps, y, q8, q16, a_scale); };
+  if (g) {
+    if (nv <= 4) go(k_norm_quant<true, 4>);
+    else if (nv <= 16) go(k_norm_quant<true, 16>);
+    else go(k_norm_quant<true, 0>);
+  } else {
+    if (nv <= 4) go(k_norm_quant<false, 4>);
+    else if (nv <= 16) go(k_norm_quant<false, 16>);
+    else go(k_norm_quant<false, 0>);
+  }
   return cudaGetLastError();
 }
 

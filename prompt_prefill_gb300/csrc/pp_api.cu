@@ -313,9 +313,11 @@ int validate_cfg(const pp_config* c) {
                   c->ffn % 64 == 0 && c->vocab > 0 && c->max_seq > 0 && c->max_chunk > 0 &&
                   (c->mode == PP_MODE_RESIDENT || c->mode == PP_MODE_STREAMED) &&
                   (c->mode == PP_MODE_RESIDENT || c->ring_slots == 1 || c->ring_slots == 2) && c->rms_eps >= 0.f &&
-                  c->rope_theta > 0.f && c->profile_kernel >= PP_KERNEL_NONE && c->profile_kernel < PP_KERNEL_COUNT;
+                  c->rope_theta > 0.f && c->profile_kernel >= PP_KERNEL_NONE && c->profile_kernel < PP_KERNEL_COUNT &&
+                  (c->loop_order == PP_LOOP_CHUNK_OUTER || c->loop_order == PP_LOOP_LAYER_OUTER);
   if (!ok) {
-    set_err("invalid pp_config (dim%%64, head_dim in {64,128}, 64 %% (H/Hkv), ffn%%64, sizes > 0, mode, ring_slots)");
+    set_err("invalid pp_config (dim%%64, head_dim in {64,128}, 64 %% (H/Hkv), ffn%%64, sizes > 0, mode, ring_slots, "
+            "loop_order)");
     return PP_ERR_ARG;
   }
   return PP_OK;
@@ -363,7 +365,8 @@ int load_impl(pp_model* m, const pp_weights* w) {
 
   // scratch
   const size_t KMAX = std::max(std::max(D, QD), F);
-  PP_TRY(dalloc(m, &m->x, MC * D));
+  // residual stream: max_chunk rows chunk-outer, every position of a call layer-outer
+  PP_TRY(dalloc(m, &m->x, (c.loop_order == PP_LOOP_LAYER_OUTER ? std::max(MC, (size_t)c.max_seq) : MC) * D));
   PP_TRY(dalloc(m, &m->qkv, MC * QKV));
   PP_TRY(dalloc(m, &m->qr, MC * QD));
   PP_TRY(dalloc(m, &m->o, MC * QD));
@@ -523,19 +526,91 @@ int trace_codes(pp_model* m, cudaStream_t cs, int layer, int point, int pos0, in
   return PP_OK;
 }
 
-int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
-                 cudaStream_t st) {
+// One layer over the C rows of a chunk at positions pos0.. (residual rows x):
+// attention block then FFN block, every projection an int8 GEMM over the chunk.
+int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base, float* x, int C, int pos0) {
   const pp_config& c = m->cfg;
   const int D = c.dim, H = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim, F = c.ffn;
   const int QD = H * hd, QKV = (H + 2 * Hkv) * hd;
   const size_t kvl = (size_t)c.max_seq * Hkv * hd;
+  __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
+  if (m->trace)
+    PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)l * m->trace_pos + pos0) * D, x, sizeof(float) * C * D,
+                            cudaMemcpyDeviceToDevice, cs));
+  const LayerPtrs L = layer_ptrs(m->lay, base);
+  float* kcl = m->kc + kvl * l;
+  float* vcl = m->vc + kvl * l;
+  // attention block
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+    return launch_norm_quant(x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
+  }));
+  PP_TRY(trace_codes(m, cs, l, 0, pos0, C, D));
+  PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
+  PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
+    return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
+  }));
+  PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
+    return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
+  }));
+  if (attention_workspace_bytes(C, pos0, H, Hkv, hd)) m->stats.kernel_launches += 1;  // the range merge
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+    return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, q16, m->as, cs);
+  }));
+  PP_TRY(trace_codes(m, cs, l, 1, pos0, C, QD));
+  PP_TRY(gemm(m, cs, EPI_RESID, mg, 1, L.so, L.wo, C, D, QD, x, D));
+  // FFN block
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+    return launch_norm_quant(x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
+  }));
+  PP_TRY(trace_codes(m, cs, l, 2, pos0, C, D));
+  PP_TRY(gemm(m, cs, EPI_SWIGLU, mg, 2, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+    return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, q16, m->as, cs);
+  }));
+  PP_TRY(trace_codes(m, cs, l, 3, pos0, C, F));
+  PP_TRY(gemm(m, cs, EPI_RESID, mg, 3, L.sd, L.wd, C, D, F, x, D));
+  return PP_OK;
+}
+
+// The weights of layer l for visit v: resident block, or (streamed) the ring
+// slot its copy lands in, with the compute stream made to wait for that copy.
+int layer_weights(pp_model* m, cudaStream_t cs, int l, int v, int n_visits, const uint8_t** base, int* mg) {
+  if (m->cfg.mode == PP_MODE_STREAMED) {
+    *mg = v % m->cfg.ring_slots;
+    return stream_layer(m, cs, v, n_visits, base);
+  }
+  *mg = l;
+  *base = m->d_layers + m->lay.bytes * l;
+  return PP_OK;
+}
+
+// Final RMSNorm -> quantise -> output projection of the last position's row.
+int head(pp_model* m, cudaStream_t cs, const float* xlast, float* d_logits) {
+  const pp_config& c = m->cfg;
+  const int D = c.dim;
+  __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
+    return launch_norm_quant(xlast, D, m->final_norm, 1, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
+  }));
+  PP_TRY(launch(m, PP_KERNEL_LM_HEAD, cs, [&] {
+    return launch_lm_head(m->a8, m->as, m->w_out, m->s_out, c.vocab, D, d_logits, cs);
+  }));
+  return PP_OK;
+}
+
+int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
+                 cudaStream_t st) {
+  const pp_config& c = m->cfg;
+  const int D = c.dim;
+  const bool streamed = c.mode == PP_MODE_STREAMED;
+  const bool layer_outer = c.loop_order == PP_LOOP_LAYER_OUTER;
   const int n_chunks = (n + chunk - 1) / chunk;
-  const int n_visits = n_chunks * c.n_layers;
-  int visit = 0;
+  // streamed: one layer copy per (chunk, layer) chunk-outer, per layer layer-outer
+  const int n_visits = layer_outer ? c.n_layers : n_chunks * c.n_layers;
   // The model's scratch, K/V cache and ring are shared by every call: order
   // this call after the previous one, whichever stream that one ran on.
   PP_CUDA(cudaStreamWaitEvent(st, m->done, 0));
-  if (c.mode == PP_MODE_STREAMED && st != m->stream) {
+  if (streamed && st != m->stream) {
     // keep the ring's events on one compute stream
     cudaEvent_t e;
     PP_TRY(ev_get(m, &e));
@@ -543,72 +618,44 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     PP_CUDA(cudaStreamWaitEvent(m->stream, e, 0));
     m->ev_pool.push_back(e);
   }
-  cudaStream_t cs = c.mode == PP_MODE_STREAMED ? m->stream : st;
-  __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
-  for (int c0 = 0; c0 < n; c0 += chunk) {
-    const int C = std::min(chunk, n - c0);
-    const int pos0 = start_pos + c0;
-    PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, cs); }));
-    for (int l = 0; l < c.n_layers; ++l, ++visit) {
-      if (m->trace)
-        PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)l * m->trace_pos + pos0) * D, m->x, sizeof(float) * C * D,
-                                cudaMemcpyDeviceToDevice, cs));
-      const uint8_t* base;
-      const int mg = c.mode == PP_MODE_STREAMED ? visit % c.ring_slots : l;
-      if (c.mode == PP_MODE_STREAMED) {
-        PP_TRY(stream_layer(m, cs, visit, n_visits, &base));
-      } else {
-        base = m->d_layers + m->lay.bytes * l;
+  cudaStream_t cs = streamed ? m->stream : st;
+  if (!layer_outer) {
+    // "Batched Prefill": for each chunk, every layer over the chunk's rows
+    int visit = 0;
+    for (int c0 = 0; c0 < n; c0 += chunk) {
+      const int C = std::min(chunk, n - c0);
+      const int pos0 = start_pos + c0;
+      PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, cs); }));
+      for (int l = 0; l < c.n_layers; ++l, ++visit) {
+        const uint8_t* base;
+        int mg;
+        PP_TRY(layer_weights(m, cs, l, visit, n_visits, &base, &mg));
+        PP_TRY(layer_block(m, cs, l, mg, base, m->x, C, pos0));
+        if (streamed) PP_CUDA(cudaEventRecord(m->ring_free[visit % c.ring_slots], cs));
       }
-      const LayerPtrs L = layer_ptrs(m->lay, base);
-      float* kcl = m->kc + kvl * l;
-      float* vcl = m->vc + kvl * l;
-      // attention block
-      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
-      }));
-      PP_TRY(trace_codes(m, cs, l, 0, pos0, C, D));
-      PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
-      PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
-        return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
-      }));
-      PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
-        return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
-      }));
-      if (attention_workspace_bytes(C, pos0, H, Hkv, hd)) m->stats.kernel_launches += 1;  // the range merge
-      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, q16, m->as, cs);
-      }));
-      PP_TRY(trace_codes(m, cs, l, 1, pos0, C, QD));
-      PP_TRY(gemm(m, cs, EPI_RESID, mg, 1, L.so, L.wo, C, D, QD, m->x, D));
-      // FFN block
-      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
-      }));
-      PP_TRY(trace_codes(m, cs, l, 2, pos0, C, D));
-      PP_TRY(gemm(m, cs, EPI_SWIGLU, mg, 2, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
-      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, q16, m->as, cs);
-      }));
-      PP_TRY(trace_codes(m, cs, l, 3, pos0, C, F));
-      PP_TRY(gemm(m, cs, EPI_RESID, mg, 3, L.sd, L.wd, C, D, F, m->x, D));
-      if (c.mode == PP_MODE_STREAMED) PP_CUDA(cudaEventRecord(m->ring_free[visit % c.ring_slots], cs));
+      if (m->trace)
+        PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)c.n_layers * m->trace_pos + pos0) * D, m->x,
+                                sizeof(float) * C * D, cudaMemcpyDeviceToDevice, cs));
+      if (c0 + C == n) PP_TRY(head(m, cs, m->x + (size_t)(C - 1) * D, d_logits));
+    }
+  } else {
+    // "Single-pass prefill": for each layer, every chunk of the call; the
+    // residual rows of all n positions stay in m->x between layers
+    PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok, n, m->emb, c.vocab, D, m->x, m->status, cs); }));
+    for (int l = 0; l < c.n_layers; ++l) {
+      const uint8_t* base;
+      int mg;
+      PP_TRY(layer_weights(m, cs, l, l, n_visits, &base, &mg));
+      for (int c0 = 0; c0 < n; c0 += chunk)
+        PP_TRY(layer_block(m, cs, l, mg, base, m->x + (size_t)c0 * D, std::min(chunk, n - c0), start_pos + c0));
+      if (streamed) PP_CUDA(cudaEventRecord(m->ring_free[l % c.ring_slots], cs));
     }
     if (m->trace)
-      PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)c.n_layers * m->trace_pos + pos0) * D, m->x,
-                              sizeof(float) * C * D, cudaMemcpyDeviceToDevice, cs));
-    if (c0 + C == n) {
-      // last position only: final RMSNorm -> quantise -> output projection
-      PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-        return launch_norm_quant(m->x + (size_t)(C - 1) * D, D, m->final_norm, 1, D, c.rms_eps, nullptr, m->a8,
-                                 q16, m->as, cs);
-      }));
-      PP_TRY(launch(m, PP_KERNEL_LM_HEAD, cs, [&] {
-        return launch_lm_head(m->a8, m->as, m->w_out, m->s_out, c.vocab, D, d_logits, cs);
-      }));
-    }
+      PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)c.n_layers * m->trace_pos + start_pos) * D, m->x,
+                              sizeof(float) * n * D, cudaMemcpyDeviceToDevice, cs));
+    PP_TRY(head(m, cs, m->x + (size_t)(n - 1) * D, d_logits));
   }
-  if (c.mode == PP_MODE_STREAMED && st != m->stream) {
+  if (streamed && st != m->stream) {
     cudaEvent_t e;
     PP_TRY(ev_get(m, &e));
     PP_CUDA(cudaEventRecord(e, m->stream));

@@ -77,6 +77,18 @@ def test_host_side_validation_needs_no_device(libpp):
     bad = pp.make_config(100, 1, 4, 4, 64, 256, 10)  # dim % 64 != 0
     h = ctypes.c_void_p()
     assert libpp.pp_model_load(ctypes.byref(bad), None, ctypes.byref(h)) == pp.PP_ERR_ARG
+    bad = pp.make_config(128, 1, 4, 4, 64, 256, 10, loop_order=2)  # no such loop order
+    assert libpp.pp_model_load(ctypes.byref(bad), None, ctypes.byref(h)) == pp.PP_ERR_ARG
+
+
+def test_header_constants_match_binding():
+    import prompt_prefill_gb300 as pp
+
+    text = open(HEADER).read()
+    defs = {k: int(v) for k, v in re.findall(r"#define\s+(PP_[A-Z0-9_]+)\s+(-?\d+)", text)}
+    assert defs, "no constants found"
+    for name, value in defs.items():
+        assert getattr(pp, name) == value, name
 
 
 def test_no_cpu_fallback_without_a_device(libpp):
