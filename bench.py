@@ -416,7 +416,9 @@ def h2d_bandwidth_gbs(nbytes: int = 1 << 30) -> float:
 def run_streamed(args, cfg, world, rank, local, pg):
     """Weights in pinned host memory, streamed into a device ring ("Predictive
     prefetch"): tok/s per prompt length for the 2-slot ring and the 1-slot
-    synchronous loader, host-to-device bytes, prefetch hits and misses."""
+    synchronous loader (chunk-outer: each layer copied once per chunk), and for
+    the layer-outer loop (each layer copied once per call), host-to-device
+    bytes, prefetch hits and misses."""
     import torch
 
     import prompt_prefill_gb300 as pp
@@ -429,9 +431,10 @@ def run_streamed(args, cfg, world, rank, local, pg):
     bw = h2d_bandwidth_gbs()
     layer_block = None
     results = {}
-    for slots in (2, 1):
+    for slots, order in ((2, pp.PP_LOOP_CHUNK_OUTER), (1, pp.PP_LOOP_CHUNK_OUTER), (2, pp.PP_LOOP_LAYER_OUTER)):
         g = pp.PrefillModel(cfg, model, max_seq=max(lens), max_chunk=chunk, mode=pp.PP_MODE_STREAMED,
-                            ring_slots=slots, gemm_engine=args.engine)
+                            ring_slots=slots, gemm_engine=args.engine, loop_order=order)
+        tag = "" if order == pp.PP_LOOP_CHUNK_OUTER else "_layer_outer"
         stream = torch.cuda.current_stream()
         for P in lens:
             toks = synth.prompt(cfg, P)
@@ -451,9 +454,10 @@ def run_streamed(args, cfg, world, rank, local, pg):
             st = g.stats()
             h2d = st["h2d_bytes"] / args.steps
             n_chunks = -(-P // chunk)
-            layer_block = h2d / (n_chunks * cfg.n_layers)
-            results[f"{P}_slots{slots}"] = {
-                "prompt": P, "ring_slots": slots, "tok_per_s": P / (ms / 1000), "ms": ms,
+            layer_block = h2d / ((1 if order == pp.PP_LOOP_LAYER_OUTER else n_chunks) * cfg.n_layers)
+            results[f"{P}_slots{slots}{tag}"] = {
+                "prompt": P, "ring_slots": slots, "loop": "layer-outer" if tag else "chunk-outer",
+                "tok_per_s": P / (ms / 1000), "ms": ms,
                 "h2d_bytes_per_prompt": h2d, "h2d_bytes_naive_per_prompt": layer_block * cfg.n_layers * P,
                 "prefetch_hits": st["prefetch_hits"] // args.steps, "prefetch_misses": st["prefetch_misses"] // args.steps,
                 "h2d_bound_tok_per_s": P / (h2d / (bw * 1e9)), "frac_of_h2d_bound": (h2d / (bw * 1e9)) / (ms / 1000)}
