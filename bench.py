@@ -431,6 +431,7 @@ def run_streamed(args, cfg, world, rank, local, pg):
     bw = h2d_bandwidth_gbs()
     layer_block = None
     results = {}
+    layer_profiles = {}
     for slots, order in ((2, pp.PP_LOOP_CHUNK_OUTER), (1, pp.PP_LOOP_CHUNK_OUTER), (2, pp.PP_LOOP_LAYER_OUTER)):
         g = pp.PrefillModel(cfg, model, max_seq=max(lens), max_chunk=chunk, mode=pp.PP_MODE_STREAMED,
                             ring_slots=slots, gemm_engine=args.engine, loop_order=order)
@@ -461,6 +462,19 @@ def run_streamed(args, cfg, world, rank, local, pg):
                 "h2d_bytes_per_prompt": h2d, "h2d_bytes_naive_per_prompt": layer_block * cfg.n_layers * P,
                 "prefetch_hits": st["prefetch_hits"] // args.steps, "prefetch_misses": st["prefetch_misses"] // args.steps,
                 "h2d_bound_tok_per_s": P / (h2d / (bw * 1e9)), "frac_of_h2d_bound": (h2d / (bw * 1e9)) / (ms / 1000)}
+        # per-layer profile (an extra, untimed call with the profiler on): sync vs async loader per layer
+        P = lens[-1]
+        toks = synth.prompt(cfg, P)
+        d_tok = torch.from_numpy(toks).cuda()
+        g.set_layer_profile(True)
+        g.reset_stats()
+        g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)
+        prof = g.layer_profile()
+        g.set_layer_profile(False)
+        v = sum(p["visits"] for p in prof)
+        layer_profiles[f"{P}_slots{slots}{tag}"] = {
+            "per_visit_ms": {k: sum(p[k] for p in prof) / v for k in ("compute_ms", "io_ms", "wait_ms")},
+            "visits": v, "wait_ms_by_layer": [round(p["wait_ms"], 3) for p in prof]}
         g.close()
     main = results[f"{lens[-1]}_slots2"]
     line = {"metric": "prefill tok/s, 8B-shaped int8 decoder, weights streamed from pinned host memory",
@@ -468,7 +482,7 @@ def run_streamed(args, cfg, world, rank, local, pg):
             "ms_per_step": main["ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic", "config": {"workload": f"8B-shaped int8 decoder, weights streamed (2-slot ring), "
                                                     f"prompts {lens}, chunk {chunk}"},
-            "h2d_gbs_measured": bw, "per_prompt": results}
+            "h2d_gbs_measured": bw, "per_prompt": results, "layer_profile": layer_profiles}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -197,6 +197,26 @@ int pp_reset_stats(pp_model* m);
  * and summed duration appear in pp_stats (prof_launches, prof_ms). */
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
+/* Per-layer stage profile ("Single-pass prefill", the per-layer profiler of
+ * I/O and compute; "Predictive prefetch", the sync vs async loader A/B),
+ * summed over every visit of the layer (one per chunk chunk-outer, one per
+ * call layer-outer) since the last pp_reset_stats. */
+typedef struct pp_layer_profile {
+  double compute_ms;  /* first kernel of the visit to its last kernel, on the compute stream */
+  double io_ms;       /* streamed mode: the layer's host-to-device copy on the copy stream */
+  double wait_ms;     /* streamed mode: time the compute stream waited for that copy (prefetch misses) */
+  int64_t visits;
+} pp_layer_profile;
+
+/* Turn the per-layer profile on (1) or off (0). It brackets every layer visit
+ * with CUDA events (and every layer copy in streamed mode), which costs a few
+ * microseconds per visit: keep it off in timed runs. */
+int pp_set_layer_profile(pp_model* m, int32_t enable);
+
+/* Copy the per-layer profile of the model's n_layers layers to out
+ * [n_layers] (synchronises the model's streams first). */
+int pp_get_layer_profile(const pp_model* m, pp_layer_profile* out, int32_t n_layers);
+
 /* Record the residual stream at every layer boundary and the int8 codes at
  * every quantisation point (for layer-by-layer verification). While set,
  * each prefill call writes, for its positions p < max_pos:

@@ -61,6 +61,11 @@ class pp_stats(ctypes.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class pp_layer_profile(ctypes.Structure):
+    _fields_ = [("compute_ms", ctypes.c_double), ("io_ms", ctypes.c_double), ("wait_ms", ctypes.c_double),
+                ("visits", ctypes.c_int64)]
+
+
 # Exported symbols and their ctypes signatures (same names as include/pp.h).
 _vp, _i32, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
 SIGNATURES = {
@@ -76,6 +81,8 @@ SIGNATURES = {
     "pp_reset_stats": ([_vp], ctypes.c_int),
     "pp_model_gemm_engine": ([_vp], ctypes.c_int),
     "pp_set_profile_kernel": ([_vp, _i32], ctypes.c_int),
+    "pp_set_layer_profile": ([_vp, _i32], ctypes.c_int),
+    "pp_get_layer_profile": ([_vp, ctypes.POINTER(pp_layer_profile), _i32], ctypes.c_int),
     "pp_set_trace": ([_vp, _vp, _vp, _vp, _i32], ctypes.c_int),
     "pp_status_str": ([ctypes.c_int], ctypes.c_char_p),
     "pp_last_error": ([], ctypes.c_char_p),
@@ -238,6 +245,16 @@ def pp_set_profile_kernel(h: int, kernel_class: int):
     _check(lib().pp_set_profile_kernel(h, kernel_class), "pp_set_profile_kernel")
 
 
+def pp_set_layer_profile(h: int, enable: bool):
+    _check(lib().pp_set_layer_profile(h, 1 if enable else 0), "pp_set_layer_profile")
+
+
+def pp_get_layer_profile(h: int, n_layers: int) -> list:
+    arr = (pp_layer_profile * n_layers)()
+    _check(lib().pp_get_layer_profile(h, arr, n_layers), "pp_get_layer_profile")
+    return [{n: getattr(x, n) for n, _ in pp_layer_profile._fields_} for x in arr]
+
+
 def pp_set_trace(h: int, d_x, d_codes, d_scales, max_pos: int):
     _check(lib().pp_set_trace(h, _ptr(d_x), _ptr(d_codes), _ptr(d_scales), max_pos), "pp_set_trace")
 
@@ -362,6 +379,12 @@ class PrefillModel:
 
     def set_profile_kernel(self, kernel_class):
         pp_set_profile_kernel(self.h, kernel_class)
+
+    def set_layer_profile(self, enable=True):
+        pp_set_layer_profile(self.h, enable)
+
+    def layer_profile(self):
+        return pp_get_layer_profile(self.h, self.cfg.n_layers)
 
     def set_trace(self, d_x, d_codes, d_scales, max_pos):
         pp_set_trace(self.h, d_x, d_codes, d_scales, max_pos)

@@ -137,6 +137,12 @@ struct EventPair {
   cudaEvent_t a, b;
 };
 
+// Events of one profiled layer visit: compute (a..b) and, streamed, the copy (c..d).
+struct LayerVisitEv {
+  int layer;
+  cudaEvent_t a, b, c, d;
+};
+
 }  // namespace
 
 struct pp_model {
@@ -183,6 +189,12 @@ struct pp_model {
   std::vector<cudaEvent_t> ev_pool;
   std::vector<EventPair> prof_pending;                 // profiled kernel launches
   std::vector<EventPair> prefetch_pending;             // (copy_done, needed) per layer visit
+  std::vector<int> prefetch_layer;                     // the layer of each prefetch_pending entry
+  // per-layer profile (opt-in)
+  bool layer_prof = false;
+  std::vector<pp_layer_profile> lprof;
+  std::vector<LayerVisitEv> lprof_pending;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> copy_ev;  // copy start/end of each visit of the current call
   std::vector<void*> allocations;
 };
 
@@ -218,17 +230,37 @@ int collect(pp_model* m) {
     m->ev_pool.push_back(p.b);
   }
   m->prof_pending.clear();
-  for (auto& p : m->prefetch_pending) {
+  for (size_t i = 0; i < m->prefetch_pending.size(); ++i) {
+    const EventPair& p = m->prefetch_pending[i];
     float ms = 0.f;  // time from the copy's completion to the moment compute needed it
     PP_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
     if (ms >= 0.f)
       m->stats.prefetch_hits += 1;
     else
       m->stats.prefetch_misses += 1;
+    if (m->layer_prof && i < m->prefetch_layer.size() && ms < 0.f)
+      m->lprof[m->prefetch_layer[i]].wait_ms += -ms;
     m->ev_pool.push_back(p.a);
     m->ev_pool.push_back(p.b);
   }
   m->prefetch_pending.clear();
+  m->prefetch_layer.clear();
+  for (auto& v : m->lprof_pending) {
+    float ms = 0.f;
+    PP_CUDA(cudaEventElapsedTime(&ms, v.a, v.b));
+    pp_layer_profile& lp = m->lprof[v.layer];
+    lp.compute_ms += ms;
+    lp.visits += 1;
+    m->ev_pool.push_back(v.a);
+    m->ev_pool.push_back(v.b);
+    if (v.c) {
+      PP_CUDA(cudaEventElapsedTime(&ms, v.c, v.d));
+      lp.io_ms += ms;
+      m->ev_pool.push_back(v.c);
+      m->ev_pool.push_back(v.d);
+    }
+  }
+  m->lprof_pending.clear();
   return PP_OK;
 }
 
@@ -456,6 +488,13 @@ void free_impl(pp_model* m) {
   }
   for (auto& p : m->prof_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
   for (auto& p : m->prefetch_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  for (auto& v : m->lprof_pending) {
+    cudaEventDestroy(v.a);
+    cudaEventDestroy(v.b);
+    if (v.c) { cudaEventDestroy(v.c); cudaEventDestroy(v.d); }
+  }
+  for (auto& e : m->copy_ev)
+    if (e.first) { cudaEventDestroy(e.first); cudaEventDestroy(e.second); }
   for (auto e : m->ev_pool) cudaEventDestroy(e);
   for (int s = 0; s < 2; ++s) {
     if (m->ring_ready[s]) cudaEventDestroy(m->ring_ready[s]);
@@ -493,8 +532,19 @@ int stream_layer(pp_model* m, cudaStream_t st, int v, int n_visits, const uint8_
     const int slot = visit % S;
     const int layer = visit % c.n_layers;
     PP_CUDA(cudaStreamWaitEvent(m->copy_stream, m->ring_free[slot], 0));
+    cudaEvent_t c0 = nullptr, c1 = nullptr;
+    if (m->layer_prof) {
+      PP_TRY(ev_get(m, &c0));
+      PP_TRY(ev_get(m, &c1));
+      PP_CUDA(cudaEventRecord(c0, m->copy_stream));
+    }
     PP_CUDA(cudaMemcpyAsync(m->ring[slot], m->h_layers + stride * layer, stride, cudaMemcpyHostToDevice,
                             m->copy_stream));
+    if (m->layer_prof) {
+      PP_CUDA(cudaEventRecord(c1, m->copy_stream));
+      if ((int)m->copy_ev.size() <= visit) m->copy_ev.resize(visit + 1, {nullptr, nullptr});
+      m->copy_ev[visit] = {c0, c1};
+    }
     PP_CUDA(cudaEventRecord(m->ring_ready[slot], m->copy_stream));
     m->stats.h2d_bytes += (int64_t)stride;
     return PP_OK;
@@ -511,6 +561,7 @@ int stream_layer(pp_model* m, cudaStream_t st, int v, int n_visits, const uint8_
   PP_CUDA(cudaStreamWaitEvent(st, m->ring_ready[slot], 0));
   if (S == 2 && v + 1 < n_visits) PP_TRY(issue_copy(v + 1));
   m->prefetch_pending.push_back(hp);
+  m->prefetch_layer.push_back(v % c.n_layers);
   *base = m->ring[slot];
   return PP_OK;
 }
@@ -619,6 +670,29 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     m->ev_pool.push_back(e);
   }
   cudaStream_t cs = streamed ? m->stream : st;
+  // per-layer profile: events around every layer visit (compute) and its copy
+  if (m->layer_prof) m->copy_ev.assign(n_visits, {nullptr, nullptr});
+  auto visit_begin = [&](cudaEvent_t* a) -> int {
+    *a = nullptr;
+    if (!m->layer_prof) return PP_OK;
+    PP_TRY(ev_get(m, a));
+    PP_CUDA(cudaEventRecord(*a, cs));
+    return PP_OK;
+  };
+  auto visit_end = [&](int l, int v, cudaEvent_t a) -> int {
+    if (!m->layer_prof) return PP_OK;
+    cudaEvent_t b;
+    PP_TRY(ev_get(m, &b));
+    PP_CUDA(cudaEventRecord(b, cs));
+    LayerVisitEv e{l, a, b, nullptr, nullptr};
+    if (streamed && v < (int)m->copy_ev.size()) {
+      e.c = m->copy_ev[v].first;
+      e.d = m->copy_ev[v].second;
+      m->copy_ev[v] = {nullptr, nullptr};
+    }
+    m->lprof_pending.push_back(e);
+    return PP_OK;
+  };
   if (!layer_outer) {
     // "Batched Prefill": for each chunk, every layer over the chunk's rows
     int visit = 0;
@@ -630,7 +704,10 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
         const uint8_t* base;
         int mg;
         PP_TRY(layer_weights(m, cs, l, visit, n_visits, &base, &mg));
+        cudaEvent_t ev;
+        PP_TRY(visit_begin(&ev));
         PP_TRY(layer_block(m, cs, l, mg, base, m->x, C, pos0));
+        PP_TRY(visit_end(l, visit, ev));
         if (streamed) PP_CUDA(cudaEventRecord(m->ring_free[visit % c.ring_slots], cs));
       }
       if (m->trace)
@@ -646,8 +723,11 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       const uint8_t* base;
       int mg;
       PP_TRY(layer_weights(m, cs, l, l, n_visits, &base, &mg));
+      cudaEvent_t ev;
+      PP_TRY(visit_begin(&ev));
       for (int c0 = 0; c0 < n; c0 += chunk)
         PP_TRY(layer_block(m, cs, l, mg, base, m->x + (size_t)c0 * D, std::min(chunk, n - c0), start_pos + c0));
+      PP_TRY(visit_end(l, l, ev));
       if (streamed) PP_CUDA(cudaEventRecord(m->ring_free[l % c.ring_slots], cs));
     }
     if (m->trace)
@@ -810,6 +890,32 @@ int pp_reset_stats(pp_model* m) {
   PP_TRY(sync_model(m));
   PP_TRY(collect(m));
   m->stats = pp_stats{};
+  m->lprof.assign(m->cfg.n_layers, pp_layer_profile{});
+  return PP_OK;
+}
+
+int pp_set_layer_profile(pp_model* m, int32_t enable) {
+  if (!m || (enable != 0 && enable != 1)) {
+    set_err("bad pp_set_layer_profile arguments");
+    return PP_ERR_ARG;
+  }
+  PP_TRY(sync_model(m));
+  PP_TRY(collect(m));
+  if ((int)m->lprof.size() != m->cfg.n_layers) m->lprof.assign(m->cfg.n_layers, pp_layer_profile{});
+  m->layer_prof = enable != 0;
+  return PP_OK;
+}
+
+int pp_get_layer_profile(const pp_model* cm, pp_layer_profile* out, int32_t n_layers) {
+  if (!cm || !out || n_layers != cm->cfg.n_layers) {
+    set_err("bad pp_get_layer_profile arguments (n_layers must equal the model's)");
+    return PP_ERR_ARG;
+  }
+  pp_model* m = const_cast<pp_model*>(cm);
+  PP_TRY(sync_model(m));
+  PP_TRY(collect(m));
+  if ((int)m->lprof.size() != m->cfg.n_layers) m->lprof.assign(m->cfg.n_layers, pp_layer_profile{});
+  for (int l = 0; l < n_layers; ++l) out[l] = m->lprof[l];
   return PP_OK;
 }
 

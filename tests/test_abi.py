@@ -57,6 +57,11 @@ def test_struct_layouts_match_header():
     sbody = re.sub(r"/\*.*?\*/", "", sbody, flags=re.S)
     sfields = re.findall(r"\b(int64_t|double)\s+(\w+);", sbody)
     assert [n for _, n in sfields] == [n for n, _ in pp.pp_stats._fields_]
+    lbody = re.search(r"typedef struct pp_layer_profile \{(.*?)\} pp_layer_profile;", text, re.S).group(1)
+    lbody = re.sub(r"/\*.*?\*/", "", lbody, flags=re.S)
+    lfields = re.findall(r"\b(int64_t|double)\s+(\w+);", lbody)
+    assert [n for _, n in lfields] == [n for n, _ in pp.pp_layer_profile._fields_]
+    assert ctypes.sizeof(pp.pp_layer_profile) == 8 * len(lfields)
 
 
 def test_status_strings(libpp):

@@ -83,3 +83,50 @@ def test_layer_outer_streamed_copies_each_layer_once(m1b, slots):
     layer_w = c.layer_bytes() + 4 * (c.qkv_rows + c.dim + 2 * c.ffn + c.dim)
     # the GEMMs still read every layer's weights once per chunk (from the ring slot)
     assert s["weight_bytes_read"] == n_chunks * c.n_layers * layer_w + c.vocab * c.dim + 4 * c.vocab
+
+
+def test_layer_profile_resident(m350):
+    """The per-layer profile: one visit per layer per chunk, compute time for
+    every layer, no copy or wait in resident mode; profiling changes no bits."""
+    c = m350.cfg
+    toks = synth.prompt(c)[:200]
+    g = load(m350, max_seq=1024, max_chunk=64)
+    ref = g.prefill(toks, 0, 64)
+    g.kv_reset()
+    g.set_layer_profile(True)
+    g.reset_stats()
+    got = g.prefill(toks, 0, 64)
+    prof = g.layer_profile()
+    g.close()
+    assert np.array_equal(bits(got), bits(ref))
+    assert len(prof) == c.n_layers
+    for p in prof:
+        assert p["visits"] == 4  # 200 tokens in chunks of 64
+        assert p["compute_ms"] > 0 and p["io_ms"] == 0 and p["wait_ms"] == 0
+
+
+@pytest.mark.parametrize("slots,order", [(2, pp.PP_LOOP_CHUNK_OUTER), (1, pp.PP_LOOP_CHUNK_OUTER),
+                                         (2, pp.PP_LOOP_LAYER_OUTER)])
+def test_layer_profile_streamed(m1b, slots, order):
+    """Streamed: every visit has a copy; with one slot the copy of a layer can
+    only start once the previous layer's compute has freed the slot, so every
+    layer after the first waits for its copy."""
+    c = m1b.cfg
+    P, chunk = 384, 128
+    toks = synth.prompt(c, P)
+    g = load(m1b, max_seq=1024, max_chunk=chunk, mode=pp.PP_MODE_STREAMED, ring_slots=slots, loop_order=order)
+    ref = g.prefill(toks, 0, chunk)
+    g.set_layer_profile(True)
+    g.reset_stats()
+    g.kv_reset()
+    got = g.prefill(toks, 0, chunk)
+    prof = g.layer_profile()
+    s = g.stats()
+    g.close()
+    assert np.array_equal(bits(got), bits(ref))
+    visits = 1 if order == pp.PP_LOOP_LAYER_OUTER else -(-P // chunk)
+    assert all(p["visits"] == visits for p in prof)
+    assert all(p["compute_ms"] > 0 and p["io_ms"] > 0 for p in prof)
+    if slots == 1:
+        assert all(p["wait_ms"] > 0 for p in prof[1:])
+    assert s["prefetch_hits"] + s["prefetch_misses"] == visits * c.n_layers
