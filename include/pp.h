@@ -101,6 +101,10 @@ typedef struct pp_config {
   int32_t gemm_engine;  /* PP_GEMM_* */
   int32_t loop_order;   /* PP_LOOP_CHUNK_OUTER or PP_LOOP_LAYER_OUTER */
   int32_t profile_kernel; /* PP_KERNEL_* class to time with events around each launch, or PP_KERNEL_NONE */
+  int32_t kv_grow;      /* 0: the K/V cache for max_seq positions is allocated at load; 1: only its address
+                           range is reserved and device memory is mapped as calls write positions
+                           ("Single-pass prefill": grow-on-demand KV), in steps of the device's allocation
+                           granularity, and released by pp_kv_reset */
 } pp_config;
 
 /* Host weights (the pages' WeightSource seam: the math sees only these).
@@ -133,6 +137,7 @@ typedef struct pp_stats {
   int64_t kernel_launches;    /* kernels this library launched */
   int64_t prof_launches;      /* launches of the profiled kernel class */
   double prof_ms;             /* summed event-timed duration of those launches */
+  int64_t kv_bytes;           /* device memory backing the K/V cache now (a level, not a counter) */
 } pp_stats;
 
 typedef struct pp_model pp_model;

@@ -42,7 +42,7 @@ class pp_config(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_int32) for n in ("dim", "n_layers", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab")]
                 + [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
                 + [(n, ctypes.c_int32) for n in ("max_seq", "max_chunk", "mode", "ring_slots", "gemm_engine",
-                                                  "loop_order", "profile_kernel")])
+                                                  "loop_order", "profile_kernel", "kv_grow")])
 
 
 class pp_weights(ctypes.Structure):
@@ -55,7 +55,8 @@ class pp_weights(ctypes.Structure):
 class pp_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("calls", "chunks", "tokens", "weight_bytes_read", "h2d_bytes",
                                                "prefetch_hits", "prefetch_misses", "kernel_launches",
-                                               "prof_launches")] + [("prof_ms", ctypes.c_double)]
+                                               "prof_launches")] + [("prof_ms", ctypes.c_double),
+                                                                    ("kv_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -162,9 +163,9 @@ def _stream(stream) -> int | None:
 # ---------------------------------------------------------------- model API
 def make_config(dim, n_layers, n_heads, n_kv_heads, head_dim, ffn, vocab, rms_eps=1e-5, rope_theta=10000.0,
                 max_seq=4096, max_chunk=512, mode=PP_MODE_RESIDENT, ring_slots=2, gemm_engine=PP_GEMM_AUTO,
-                loop_order=PP_LOOP_CHUNK_OUTER, profile_kernel=PP_KERNEL_NONE) -> pp_config:
+                loop_order=PP_LOOP_CHUNK_OUTER, profile_kernel=PP_KERNEL_NONE, kv_grow=0) -> pp_config:
     return pp_config(dim, n_layers, n_heads, n_kv_heads, head_dim, ffn, vocab, rms_eps, rope_theta, max_seq,
-                     max_chunk, mode, ring_slots, gemm_engine, loop_order, profile_kernel)
+                     max_chunk, mode, ring_slots, gemm_engine, loop_order, profile_kernel, kv_grow)
 
 
 def make_weights(tok_emb, w, w_scale, attn_norm, ffn_norm, final_norm, w_out, w_out_scale):
@@ -332,12 +333,12 @@ class PrefillModel:
     """A loaded model: owns the pp_model handle (freed on close)."""
 
     def __init__(self, shape, weights, max_seq=4096, max_chunk=512, mode=PP_MODE_RESIDENT, ring_slots=2,
-                 gemm_engine=PP_GEMM_AUTO, loop_order=PP_LOOP_CHUNK_OUTER, profile_kernel=PP_KERNEL_NONE):
+                 gemm_engine=PP_GEMM_AUTO, loop_order=PP_LOOP_CHUNK_OUTER, profile_kernel=PP_KERNEL_NONE, kv_grow=0):
         """shape: any object with the ModelShape fields; weights: any object with
         tok_emb, w, w_scale, attn_norm, ffn_norm, final_norm, w_out, w_out_scale (host arrays)."""
         self.cfg = make_config(shape.dim, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                                shape.vocab, shape.rms_eps, shape.rope_theta, max_seq, max_chunk, mode, ring_slots,
-                               gemm_engine, loop_order, profile_kernel)
+                               gemm_engine, loop_order, profile_kernel, kv_grow)
         ws, keep = make_weights(weights.tok_emb, weights.w, weights.w_scale, weights.attn_norm, weights.ffn_norm,
                                 weights.final_norm, weights.w_out, weights.w_out_scale)
         self.h = pp_model_load(self.cfg, ws)

@@ -166,6 +166,8 @@ struct pp_model {
   float* rope = nullptr;
   float* kc = nullptr;
   float* vc = nullptr;
+  size_t kv_layer_floats = 0;  // floats from one layer's K (or V) rows to the next layer's
+  KvSpace kvs;                 // kv_grow: reserved range, mapped as positions are written
   // scratch
   float *x = nullptr, *qkv = nullptr, *qr = nullptr, *o = nullptr, *h = nullptr, *as = nullptr, *logits = nullptr;
   int8_t* a8 = nullptr;
@@ -385,14 +387,30 @@ int load_impl(pp_model* m, const pp_weights* w) {
   PP_TRY(dalloc(m, &m->w_out, V * D));
   PP_TRY(dalloc(m, &m->s_out, V));
   PP_TRY(dalloc(m, &m->rope, (size_t)c.max_seq * c.head_dim));
-  PP_TRY(dalloc(m, &m->kc, KVE));
-  PP_TRY(dalloc(m, &m->vc, KVE));
+  const size_t kv_row = (size_t)c.n_kv_heads * c.head_dim;  // floats per position per layer
+  if (c.kv_grow) {
+    // K regions 0..L-1 then V regions L..2L-1, each padded to the mapping granularity
+    cudaError_t e = kv_space_reserve(&m->kvs, m->device, 2 * c.n_layers, (size_t)c.max_seq * kv_row * sizeof(float));
+    if (e != cudaSuccess) {
+      set_err("reserving the K/V address range failed: %s", cudaGetErrorString(e));
+      return e == cudaErrorMemoryAllocation ? PP_ERR_OOM : PP_ERR_UNSUPPORTED;
+    }
+    m->kv_layer_floats = m->kvs.region_bytes / sizeof(float);
+    m->kc = reinterpret_cast<float*>(m->kvs.base);
+    m->vc = m->kc + (size_t)c.n_layers * m->kv_layer_floats;
+  } else {
+    PP_TRY(dalloc(m, &m->kc, KVE));
+    PP_TRY(dalloc(m, &m->vc, KVE));
+    m->kv_layer_floats = (size_t)c.max_seq * kv_row;
+  }
   PP_CUDA(cudaMemcpy(m->emb, w->tok_emb, V * D * 4, cudaMemcpyHostToDevice));
   PP_CUDA(cudaMemcpy(m->final_norm, w->final_norm, D * 4, cudaMemcpyHostToDevice));
   PP_CUDA(cudaMemcpy(m->w_out, w->w_out, V * D, cudaMemcpyHostToDevice));
   PP_CUDA(cudaMemcpy(m->s_out, w->w_out_scale, V * 4, cudaMemcpyHostToDevice));
-  PP_CUDA(cudaMemsetAsync(m->kc, 0, KVE * 4, m->stream));
-  PP_CUDA(cudaMemsetAsync(m->vc, 0, KVE * 4, m->stream));
+  if (!c.kv_grow) {
+    PP_CUDA(cudaMemsetAsync(m->kc, 0, KVE * 4, m->stream));
+    PP_CUDA(cudaMemsetAsync(m->vc, 0, KVE * 4, m->stream));
+  }
   PP_CUDA(launch_rope_table(c.max_seq, c.head_dim, c.rope_theta, m->rope, m->stream));
 
   // scratch
@@ -501,6 +519,7 @@ void free_impl(pp_model* m) {
     if (m->ring_free[s]) cudaEventDestroy(m->ring_free[s]);
   }
   for (void* p : m->allocations) cudaFree(p);
+  if (m->kvs.base) kv_space_free(&m->kvs);
   if (m->h_layers) cudaFreeHost(m->h_layers);
   if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
   if (m->stream) cudaStreamDestroy(m->stream);
@@ -583,7 +602,7 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
   const pp_config& c = m->cfg;
   const int D = c.dim, H = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim, F = c.ffn;
   const int QD = H * hd, QKV = (H + 2 * Hkv) * hd;
-  const size_t kvl = (size_t)c.max_seq * Hkv * hd;
+  const size_t kvl = m->kv_layer_floats;
   __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
   if (m->trace)
     PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)l * m->trace_pos + pos0) * D, x, sizeof(float) * C * D,
@@ -658,6 +677,15 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   const int n_chunks = (n + chunk - 1) / chunk;
   // streamed: one layer copy per (chunk, layer) chunk-outer, per layer layer-outer
   const int n_visits = layer_outer ? c.n_layers : n_chunks * c.n_layers;
+  if (c.kv_grow) {
+    // back the K/V rows this call writes (positions < start_pos + n) with device memory
+    const size_t need = ((size_t)start_pos + n) * c.n_kv_heads * c.head_dim * sizeof(float);
+    cudaError_t e = kv_space_grow(&m->kvs, need);
+    if (e != cudaSuccess) {
+      set_err("growing the K/V cache to %lld positions failed: %s", (long long)start_pos + n, cudaGetErrorString(e));
+      return e == cudaErrorMemoryAllocation ? PP_ERR_OOM : PP_ERR_CUDA;
+    }
+  }
   // The model's scratch, K/V cache and ring are shared by every call: order
   // this call after the previous one, whichever stream that one ran on.
   PP_CUDA(cudaStreamWaitEvent(st, m->done, 0));
@@ -856,6 +884,10 @@ int pp_kv_reset(pp_model* m) {
   const pp_config& c = m->cfg;
   const size_t KVE = (size_t)c.n_layers * c.max_seq * c.n_kv_heads * c.head_dim;
   PP_TRY(sync_model(m));
+  if (c.kv_grow) {  // give the device memory back; the next call maps what it writes
+    kv_space_release(&m->kvs);
+    return PP_OK;
+  }
   PP_CUDA(cudaMemsetAsync(m->kc, 0, KVE * 4, m->stream));
   PP_CUDA(cudaMemsetAsync(m->vc, 0, KVE * 4, m->stream));
   PP_CUDA(cudaStreamSynchronize(m->stream));
@@ -870,7 +902,11 @@ int pp_kv_read(pp_model* m, int32_t layer, int32_t which, int32_t pos0, int32_t 
   }
   const pp_config& c = m->cfg;
   const size_t row = (size_t)c.n_kv_heads * c.head_dim;
-  const float* src = (which ? m->vc : m->kc) + (size_t)layer * c.max_seq * row + (size_t)pos0 * row;
+  if (c.kv_grow && ((size_t)pos0 + n_pos) * row * sizeof(float) > m->kvs.mapped) {
+    set_err("pp_kv_read: positions [%d, %d) were never written since the last reset", pos0, pos0 + n_pos);
+    return PP_ERR_ARG;
+  }
+  const float* src = (which ? m->vc : m->kc) + (size_t)layer * m->kv_layer_floats + (size_t)pos0 * row;
   PP_TRY(sync_model(m));
   PP_CUDA(cudaMemcpy(out, src, sizeof(float) * row * n_pos, cudaMemcpyDeviceToHost));
   return PP_OK;
@@ -882,6 +918,9 @@ int pp_get_stats(const pp_model* cm, pp_stats* out) {
   PP_TRY(sync_model(m));
   PP_TRY(collect(m));
   *out = m->stats;
+  const pp_config& c = m->cfg;
+  out->kv_bytes = c.kv_grow ? (int64_t)m->kvs.mapped * m->kvs.n_regions
+                            : (int64_t)2 * c.n_layers * c.max_seq * c.n_kv_heads * c.head_dim * (int64_t)sizeof(float);
   return PP_OK;
 }
 

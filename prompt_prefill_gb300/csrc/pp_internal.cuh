@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <vector>
 
 #include <cstdint>
 
@@ -68,6 +69,25 @@ constexpr int kAttnRange = 512;
 size_t attention_workspace_bytes(int rows, int start_pos, int H, int Hkv, int hd);
 cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,
                              int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s);
+
+// ---- grow-on-demand K/V memory (kv_space.cu): n_regions regions of region_bytes
+// in one reserved virtual range; the first `mapped` bytes of every region are
+// backed by device memory. The caller synchronises before kv_space_release.
+struct KvSpace {
+  unsigned long long base = 0;  // CUdeviceptr of the reserved range
+  size_t gran = 0, region_bytes = 0, mapped = 0;
+  int n_regions = 0, device = 0;
+  struct Map {
+    unsigned long long ptr;
+    size_t size;
+    unsigned long long handle;
+  };
+  std::vector<Map> maps;
+};
+cudaError_t kv_space_reserve(KvSpace* s, int device, int n_regions, size_t region_min_bytes);
+cudaError_t kv_space_grow(KvSpace* s, size_t region_bytes_needed);
+void kv_space_release(KvSpace* s);
+void kv_space_free(KvSpace* s);
 
 // Rows of the interleaved gate/up matrix: blocks of 16 gate rows then 16 up rows.
 constexpr int kSwiGluBlock = 16;
