@@ -285,6 +285,31 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
  * shorter segments only add drains. Errors: PP_ERR_ARG out of range. */
 int pp_set_exact_segment(int32_t seg_k);
 
+/* ---------------------------------------------------------------- test hooks
+ * Failure paths made on purpose without faulting the GPU (the pages' only
+ * failure handling is graceful degradation: a prefetch miss blocks until the
+ * copy is ready, "Predictive prefetch"). */
+
+/* Run the tcgen05 GEMM (int32 result into acc, as pp_op_gemm_acc) with its MMA
+ * issuer held back and every mbarrier wait bounded by wait_us microseconds:
+ * nothing completes the accumulators, so every other role's bounded wait runs
+ * out, records the timeout, lets its copies land, frees its tensor memory and
+ * exits. Synchronous. Returns PP_ERR_DEVICE_TIMEOUT when the kernel reported
+ * the timeout (the expected result), PP_OK if it did not, or an argument /
+ * CUDA error. The device stays usable afterwards. */
+int pp_debug_gemm_stall(int32_t wait_us, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n, int32_t k,
+                        int32_t* acc);
+
+/* Streamed-mode loader fault: 0 none; 1 the ring issues no prefetch, so every
+ * layer copy starts only when its visit begins (every visit a miss; results
+ * unchanged). Errors: PP_ERR_ARG. */
+int pp_debug_loader_fault(pp_model* m, int32_t fault);
+
+/* Process-wide cap on the device bytes one model may hold (its allocations at
+ * load plus the grown K/V cache); 0 removes the cap. A load or a K/V growth
+ * that would pass it fails with PP_ERR_OOM and leaks nothing. */
+int pp_debug_alloc_cap(int64_t bytes);
+
 /* The tcgen05 GEMM of pp_op_gemm (engine PP_GEMM_TC) without any device
  * allocation, for callers that may not allocate device memory while they run
  * (an application whose device memory is all held by its own pool allocator,

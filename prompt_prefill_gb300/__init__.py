@@ -97,6 +97,9 @@ SIGNATURES = {
     "pp_op_rope_table": ([_i32, _i32, _f32, _vp, _vp], ctypes.c_int),
     "pp_op_attention": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp], ctypes.c_int),
     "pp_op_lm_head": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp], ctypes.c_int),
+    "pp_debug_gemm_stall": ([_i32, _vp, _vp, _i32, _i32, _i32, _vp], ctypes.c_int),
+    "pp_debug_loader_fault": ([_vp, _i32], ctypes.c_int),
+    "pp_debug_alloc_cap": ([ctypes.c_int64], ctypes.c_int),
 }
 
 _lock = threading.Lock()
@@ -254,6 +257,19 @@ def pp_get_layer_profile(h: int, n_layers: int) -> list:
     arr = (pp_layer_profile * n_layers)()
     _check(lib().pp_get_layer_profile(h, arr, n_layers), "pp_get_layer_profile")
     return [{n: getattr(x, n) for n, _ in pp_layer_profile._fields_} for x in arr]
+
+
+def pp_debug_gemm_stall(wait_us: int, a16, w, m: int, n: int, k: int, acc) -> int:
+    """Status of a tcgen05 GEMM run with its MMA issuer held back (test hook)."""
+    return int(lib().pp_debug_gemm_stall(wait_us, _ptr(a16), _ptr(w), m, n, k, _ptr(acc)))
+
+
+def pp_debug_loader_fault(h: int, fault: int):
+    _check(lib().pp_debug_loader_fault(h, fault), "pp_debug_loader_fault")
+
+
+def pp_debug_alloc_cap(nbytes: int):
+    _check(lib().pp_debug_alloc_cap(nbytes), "pp_debug_alloc_cap")
 
 
 def pp_set_trace(h: int, d_x, d_codes, d_scales, max_pos: int):

@@ -53,7 +53,6 @@ constexpr int MAX_SEG_KB = 16;      // 16 x 64 = 1024 products per exact f32 seg
 constexpr int MIN_SK_KB = 64;       // stream-K only when each cluster owns >= 64 k-blocks (measured: fixups
                                     // cost more than they recover at ~30-40 k-blocks per cluster)
 constexpr int STAGE_BUDGET = 204 * 1024;  // shared memory for the pipeline stages
-constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 
 // Per-tile-width constants.
 template <int BN>
@@ -86,6 +85,8 @@ struct TcParams {
   int max_slots;
   int32_t* part;
   int* cnt;
+  long long wait_cycles;  // bound of every mbarrier wait (clock64 cycles)
+  int hold_mma;           // test hook: the MMA issuer issues nothing, so every other role's wait runs out
 };
 
 // The units (tile, k-block range) a cluster works on, in order.
@@ -143,9 +144,9 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false after ~2 s without the phase completing.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit) {
   if (mbar_try(a, parity)) return true;
-  const long long end = clock64() + WAIT_CYCLES;
+  const long long end = clock64() + limit;
   while (!mbar_try(a, parity))
     if (clock64() > end) return false;
   return true;
@@ -298,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int m_row = (t % p.num_m_tiles) * 2 * BM + (int)rank * BM;
         const int n_row = (t / p.num_m_tiles) * BN + (int)rank * (BN / 2);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(empty_b(s), ph ^ 1)) { fail(); break; }
+          if (!mbar_wait(empty_b(s), ph ^ 1, p.wait_cycles)) { fail(); break; }
           mbar_expect_tx(full_b(s), A_BYTES + C::W_BYTES);
           tma_load_2d(sA(s), &tmA, kb * BK, m_row, full_b(s));
           tma_load_2d(sW(s), &tmW, kb * BK, n_row, full_b(s));
@@ -311,14 +312,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int i = 0; i < STAGES; ++i) {
           const int st = (s + i) % STAGES;
           const uint32_t sph = (s + i >= STAGES) ? ph ^ 1 : ph;
-          if (issued[st]) mbar_wait(full_b(st), sph ^ 1);
+          if (issued[st]) mbar_wait(full_b(st), sph ^ 1, p.wait_cycles);
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (leader CTA)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_ROLE));
-    if (rank == 0 && lane == 0) {
+    if (rank == 0 && lane == 0 && !p.hold_mma) {
       const uint32_t idesc = idesc_f16(2 * BM, BN);
       int s = 0;
       uint32_t ph = 0;
@@ -330,12 +331,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         sc.unit(u, t, ukb0, ukb1);
         for (int seg_k0 = ukb0; seg_k0 < ukb1 && ok; seg_k0 += p.seg_kb, ++g) {
           const int buf = g & 1;
-          if (!mbar_wait(acce_b(buf), ((g >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+          if (!mbar_wait(acce_b(buf), ((g >> 1) & 1) ^ 1, p.wait_cycles)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + buf * BN;
           const int kb0 = seg_k0, kb1 = min(ukb1, seg_k0 + p.seg_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(ready_b(s), ph)) { fail(); ok = false; break; }
+            if (!mbar_wait(ready_b(s), ph, p.wait_cycles)) { fail(); ok = false; break; }
             tc_fence_after();
             const uint64_t da = umma_desc(sA(s)), db = umma_desc(sB(s));
 #pragma unroll
@@ -351,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // let issued MMAs finish before the accumulator memory is released
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(done_b)
                      : "memory");
-        mbar_wait(done_b, 0);
+        mbar_wait(done_b, 0, p.wait_cycles);
       }
     }
   } else if (warp < CONV_WARP0) {
@@ -370,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int s = 0;
     uint32_t ph = 0;
     for (int kb = 0; kb < total_kb; ++kb) {
-      if (*abort_flag || !mbar_wait(full_b(s), ph)) { fail(); break; }
+      if (*abort_flag || !mbar_wait(full_b(s), ph, p.wait_cycles)) { fail(); break; }
       // widen this CTA's BN/2 weight rows x 64 k of int8 to fp16, UMMA layout
       uint8_t* bt = gbase + (sB(s) - base);
       const uint8_t* wt = gbase + (sW(s) - base);
@@ -532,7 +533,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const float ws_r = (EPI != EPI_ACC && et < BN && ncol < p.N) ? __ldg(p.ws + ncol) : 0.f;
       const float as_r = (EPI != EPI_ACC && row < p.M) ? __ldg(p.as + row) : 0.f;
       for (int k0 = kb0; k0 < kb1; k0 += p.seg_kb, ++g) {
-        if (*abort_flag || !mbar_wait(accf_b(g & 1), (g >> 1) & 1)) { fail(); ok = false; break; }
+        if (*abort_flag || !mbar_wait(accf_b(g & 1), (g >> 1) & 1, p.wait_cycles)) { fail(); ok = false; break; }
         drain(g, k0 == kb0);
       }
       if (!ok) break;
@@ -713,8 +714,10 @@ void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters
 
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
-                           int* status, const TcWorkspace& wsp, cudaStream_t s) {
+                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits) {
   TcParams p{};
+  p.wait_cycles = waits.cycles;
+  p.hold_mma = waits.hold_mma;
   p.M = m;
   p.N = n;
   p.K = k;

@@ -167,6 +167,8 @@ struct pp_model {
   float* kc = nullptr;
   float* vc = nullptr;
   size_t kv_layer_floats = 0;  // floats from one layer's K (or V) rows to the next layer's
+  size_t alloc_bytes = 0;      // device bytes this model allocated (test cap, pp_debug_alloc_cap)
+  int loader_fault = 0;        // pp_debug_loader_fault
   KvSpace kvs;                 // kv_grow: reserved range, mapped as positions are written
   // scratch
   float *x = nullptr, *qkv = nullptr, *qr = nullptr, *o = nullptr, *h = nullptr, *as = nullptr, *logits = nullptr;
@@ -326,8 +328,17 @@ int make_weight_maps(pp_model* m, const uint8_t* block) {
   return PP_OK;
 }
 
+std::atomic<long long> g_alloc_cap{0};
+
 template <class T>
 int dalloc(pp_model* m, T** p, size_t n) {
+  const size_t bytes = std::max<size_t>(n * sizeof(T), 256);
+  const long long cap = g_alloc_cap.load();
+  if (cap > 0 && (long long)(m->alloc_bytes + bytes) > cap) {
+    set_err("device allocation of %zu bytes would pass the test cap of %lld bytes", bytes, cap);
+    return PP_ERR_OOM;
+  }
+  m->alloc_bytes += bytes;
   void* v = nullptr;
   cudaError_t e = cudaMalloc(&v, std::max<size_t>(n * sizeof(T), 256));
   if (e != cudaSuccess) {
@@ -571,14 +582,15 @@ int stream_layer(pp_model* m, cudaStream_t st, int v, int n_visits, const uint8_
   EventPair hp{};
   PP_TRY(ev_get(m, &hp.a));
   PP_TRY(ev_get(m, &hp.b));
-  if (v == 0 || S == 1) PP_TRY(issue_copy(v));
+  const bool prefetch = S == 2 && m->loader_fault == 0;
+  if (v == 0 || !prefetch) PP_TRY(issue_copy(v));
   // The copy of visit v is now the newest work on the copy stream (with two
   // slots it was issued at visit v-1 and the copy of v+1 is issued below).
   PP_CUDA(cudaEventRecord(hp.a, m->copy_stream));  // copy of visit v done
   PP_CUDA(cudaEventRecord(hp.b, st));              // the compute stream reached layer v
   const int slot = v % S;
   PP_CUDA(cudaStreamWaitEvent(st, m->ring_ready[slot], 0));
-  if (S == 2 && v + 1 < n_visits) PP_TRY(issue_copy(v + 1));
+  if (prefetch && v + 1 < n_visits) PP_TRY(issue_copy(v + 1));
   m->prefetch_pending.push_back(hp);
   m->prefetch_layer.push_back(v % c.n_layers);
   *base = m->ring[slot];
@@ -680,6 +692,13 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   if (c.kv_grow) {
     // back the K/V rows this call writes (positions < start_pos + n) with device memory
     const size_t need = ((size_t)start_pos + n) * c.n_kv_heads * c.head_dim * sizeof(float);
+    const long long cap = g_alloc_cap.load();
+    const size_t grown = (need + m->kvs.gran - 1) / m->kvs.gran * m->kvs.gran * (size_t)m->kvs.n_regions;
+    if (cap > 0 && grown > (size_t)m->kvs.mapped * m->kvs.n_regions &&
+        (long long)(m->alloc_bytes + grown) > cap) {
+      set_err("growing the K/V cache to %zu bytes would pass the test cap of %lld bytes", grown, cap);
+      return PP_ERR_OOM;
+    }
     cudaError_t e = kv_space_grow(&m->kvs, need);
     if (e != cudaSuccess) {
       set_err("growing the K/V cache to %lld positions failed: %s", (long long)start_pos + n, cudaGetErrorString(e));
@@ -1190,6 +1209,63 @@ int pp_set_exact_segment(int32_t seg_k) {
     return PP_ERR_ARG;
   }
   g_tc_seg.store(seg_k);
+  return PP_OK;
+}
+
+int pp_debug_gemm_stall(int32_t wait_us, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n, int32_t k,
+                        int32_t* acc) {
+  if (wait_us <= 0 || !acc) {
+    set_err("bad pp_debug_gemm_stall arguments");
+    return PP_ERR_ARG;
+  }
+  PP_TRY(check_gemm(PP_GEMM_TC, nullptr, a16, w, m, n, k));
+  int dev = 0, khz = 0;
+  PP_CUDA(cudaGetDevice(&dev));
+  PP_CUDA(cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev));
+  CUtensorMap ma, mw;
+  PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
+  const int bn = tc_bn(m, n, k);
+  PP_CUDA(make_tmap_w(&mw, w, n, k, bn));
+  int* status = nullptr;
+  PP_CUDA(cudaMalloc(&status, sizeof(int)));
+  cudaError_t e = cudaMemset(status, 0, sizeof(int));
+  TcWaits waits;
+  waits.cycles = (long long)wait_us * (khz > 0 ? khz : 2000000) / 1000;  // kHz -> cycles per microsecond
+  waits.hold_mma = 1;
+  if (e == cudaSuccess)  // no stream-K workspace: whole tiles, no counters left behind
+    e = launch_gemm_tc(EPI_ACC, ma, mw, bn, nullptr, nullptr, m, n, k, nullptr, n, acc, g_tc_seg.load(), status,
+                       TcWorkspace{}, nullptr, waits);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  int st = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(status);
+  if (e != cudaSuccess) {
+    set_err("pp_debug_gemm_stall: %s", cudaGetErrorString(e));
+    return PP_ERR_CUDA;
+  }
+  if (st == DEV_TIMEOUT) {
+    set_err("a bounded device wait gave up (held-back MMA issuer)");
+    return PP_ERR_DEVICE_TIMEOUT;
+  }
+  return PP_OK;
+}
+
+int pp_debug_loader_fault(pp_model* m, int32_t fault) {
+  if (!m || (fault != 0 && fault != 1)) {
+    set_err("bad pp_debug_loader_fault arguments");
+    return PP_ERR_ARG;
+  }
+  PP_TRY(sync_model(m));
+  m->loader_fault = fault;
+  return PP_OK;
+}
+
+int pp_debug_alloc_cap(int64_t bytes) {
+  if (bytes < 0) {
+    set_err("bad pp_debug_alloc_cap arguments");
+    return PP_ERR_ARG;
+  }
+  g_alloc_cap.store(bytes);
   return PP_OK;
 }
 

@@ -57,9 +57,15 @@ struct TcWorkspace {
 };
 // Workspace a GEMM of this shape uses (0 when it runs whole tiles).
 void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters);
+// Bound of every mbarrier wait in the tcgen05 GEMM (on expiry: DEV_TIMEOUT in the status word, the kernel
+// lets its copies and MMAs land, frees its TMEM and exits), and a test hook that holds back the MMA issuer.
+struct TcWaits {
+  long long cycles = 4000000000LL;  // ~2 s at 2 GHz
+  int hold_mma = 0;
+};
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
-                           int* status, const TcWorkspace& wsp, cudaStream_t s);
+                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits = TcWaits{});
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)

@@ -1,0 +1,89 @@
+"""Failure paths, made on purpose without faulting the GPU.
+
+* A bounded device wait that runs out: the tcgen05 GEMM with its MMA issuer
+  held back (nothing ever completes an accumulator), every wait bounded to a
+  few milliseconds. Each role must record the timeout, let its copies land,
+  free its tensor memory and exit; the host reads PP_ERR_DEVICE_TIMEOUT and the
+  device stays usable (a normal GEMM right after is exact).
+* A loader that never prefetches ("Predictive prefetch": a miss blocks until
+  the copy is ready): results unchanged, every layer visit a miss.
+* An allocation cap: a load or a K/V growth past it fails with PP_ERR_OOM,
+  leaks nothing, and the K/V rows written before stay intact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import prompt_prefill_gb300 as pp
+import synth
+from tests.gpu_util import bits, dev, empty, host, load, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_runs_out_and_the_device_stays_usable():
+    torch = torch_cuda()
+    m, n, k = 256, 512, 1024
+    a = synth.uniform_i8(91, 1, (m, k))
+    w = synth.uniform_i8(91, 2, (n, k))
+    a16, dw = dev(a.astype(np.float16)), dev(w)
+    acc = empty((m, n), torch.int32)
+    assert pp.pp_debug_gemm_stall(20000, a16, dw, m, n, k, acc) == pp.PP_ERR_DEVICE_TIMEOUT
+    assert "bounded device wait" in pp.last_error()
+    pp.pp_op_gemm_acc(pp.PP_GEMM_TC, dev(a), a16, dw, m, n, k, acc)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(acc), oracle.gemm_i8(a, w))
+
+
+def test_loader_without_prefetch_changes_nothing():
+    torch_cuda()
+    mod = synth.make_model(synth.CONFIGS["1b"])
+    c = mod.cfg
+    toks = synth.prompt(c, 300)
+    g = load(mod, max_seq=1024, max_chunk=128, mode=pp.PP_MODE_STREAMED, ring_slots=2)
+    ref = g.prefill(toks, 0, 128)
+    pp.pp_debug_loader_fault(g.h, 1)
+    g.kv_reset()
+    g.reset_stats()
+    got = g.prefill(toks, 0, 128)
+    s = g.stats()
+    pp.pp_debug_loader_fault(g.h, 0)
+    g.close()
+    assert np.array_equal(bits(got), bits(ref))
+    assert s["prefetch_hits"] == 0 and s["prefetch_misses"] == 3 * c.n_layers
+
+
+def test_allocation_cap_gives_oom_without_damage():
+    torch_cuda()
+    mod = synth.make_model(synth.CONFIGS["350m"])
+    c = mod.cfg
+    row = c.n_kv_heads * c.head_dim * 4
+    try:
+        pp.pp_debug_alloc_cap(1 << 20)  # far below the 350M model's weights
+        with pytest.raises(pp.PPError) as e:
+            load(mod, max_seq=1024, max_chunk=32)
+        assert e.value.status == pp.PP_ERR_OOM
+        pp.pp_debug_alloc_cap(0)
+        g = load(mod, max_seq=8192, max_chunk=32, kv_grow=1)
+        g.prefill(synth.prompt(c, 1), 0, 32)
+        per_step = g.stats()["kv_bytes"] // (2 * c.n_layers) // row  # positions one growth step maps
+        g.kv_reset()
+        if per_step + 40 > 8192:
+            pytest.skip(f"allocation granularity of {per_step} positions leaves no second step to refuse")
+        n1 = per_step - 10  # the second call crosses into the next step
+        toks = synth.prompt(c, n1 + 40)
+        ref_g = load(mod, max_seq=8192, max_chunk=32)
+        ref_g.prefill(toks[:n1], 0, 32)
+        ref = ref_g.prefill(toks[n1:], n1, 32)
+        ref_g.close()
+        g.prefill(toks[:n1], 0, 32)
+        kv_before = g.kv(3, 0, 0, n1)
+        pp.pp_debug_alloc_cap(1)  # any further growth is over the cap
+        assert pp.pp_prefill_rc(g.h, toks[n1:], n1, 32, c.vocab) == pp.PP_ERR_OOM
+        assert np.array_equal(bits(g.kv(3, 0, 0, n1)), bits(kv_before))  # earlier rows intact
+        pp.pp_debug_alloc_cap(0)
+        got = g.prefill(toks[n1:], n1, 32)
+        g.close()
+        assert np.array_equal(bits(got), bits(ref))
+    finally:
+        pp.pp_debug_alloc_cap(0)
