@@ -40,9 +40,10 @@ FP32_LANES = 128
 # valid only while the kernel's source file hashes to the value recorded with
 # it. profiles/ holds the capture summaries and commands.
 KERNEL_TRAFFIC = {
-    # mean over the 8 launches of one layer (chunk starts 0, 512, ..., 3584)
-    "attention": {"bytes_per_launch": 27298912.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
-                  "sha256": "493452c1e36fca3af09a1c178d5f2c59dabd0c0338aca9392365b3b1deead3d2"},
+    # k_attention, mean over the 8 launches of one layer (chunk starts 0, 512, ..., 3584); the range merge
+    # kernel's own bytes are listed in its profile summary
+    "attention": {"bytes_per_launch": 33064000.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
+                  "sha256": "b935ce7261b90c797190b3acd3c863bef673db8026cc438b0f54527e85b9319e"},
 }
 
 
