@@ -53,6 +53,7 @@ constexpr int MAX_SEG_KB = 16;      // 16 x 64 = 1024 products per exact f32 seg
 constexpr int MIN_SK_KB = 64;       // stream-K only when each cluster owns >= 64 k-blocks (measured: fixups
                                     // cost more than they recover at ~30-40 k-blocks per cluster)
 constexpr int STAGE_BUDGET = 204 * 1024;  // shared memory for the pipeline stages
+constexpr int EPI_LD = 20;  // floats per row of a drain warp's epilogue staging (16 + 4: conflict-free writes)
 
 // Per-tile-width constants.
 template <int BN>
@@ -62,7 +63,9 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + W_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES;  // 5 (256), 6 (192), 7 (128)
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 2 * BN * 4 /*w_scale*/;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + 2 * BN * 4 /*w_scale*/ +
+                                    N_DRAIN_WARPS * 32 * EPI_LD * 4 /*epilogue staging*/;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static constexpr int COLS = BN / 2;                 // accumulator columns per drain warp
   static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0, "stage buffers keep the 1024-byte swizzle alignment");
 };
@@ -245,6 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t tmem_slot = bars + 8 * (3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (tmem_slot + 8 - base));
   float* const ws_s = reinterpret_cast<float*>(gbase + STAGES * C::STAGE_BYTES + 256);  // [2][BN] weight scales
+  float* const epi_s = ws_s + 2 * BN;  // [drain warps][32 rows][EPI_LD] epilogue staging
   auto sA = [&](int s) { return base + s * C::STAGE_BYTES; };
   auto sB = [&](int s) { return base + s * C::STAGE_BYTES + A_BYTES; };
   auto sW = [&](int s) { return base + s * C::STAGE_BYTES + A_BYTES + C::B_BYTES; };
@@ -462,9 +466,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // columns for SwiGLU): (float(acc) * w_scale) * a_scale, then store,
     // residual add or SwiGLU. Rows past M are skipped. wsv: this warp's COLS
     // weight scales in shared memory; a_s: the row's activation scale.
-    auto epilogue = [&](int row, int n0, const float* wsv, float a_s) {
-      if (row >= p.M) return;
+    // The warp's 32 rows x 16 output columns of a chunk go through its own
+    // slice of shared memory and leave as 8 rows x 64 bytes per store
+    // instruction (16 full 32-byte sectors), instead of one 16-byte piece of
+    // each of 32 rows; residual rows are loaded in the same pattern.
+    float* const stg = epi_s + (warp - DRAIN_WARP0) * (32 * EPI_LD);
+    auto epilogue = [&](int row0, int n0, const float* wsv, float a_s) {  // row0: the warp's first row
+      const int row = row0 + lane;
       if (EPI == EPI_ACC) {
+        if (row >= p.M) return;
 #pragma unroll
         for (int c = 0; c < COLS / 16; ++c) {
           int4* dst = reinterpret_cast<int4*>(p.acc_out + (size_t)row * p.N + n0 + 16 * c);
@@ -474,49 +484,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         return;
       }
-      if (EPI == EPI_SWIGLU) {
-        // accumulator columns come in blocks of 16 gate rows then 16 up rows
+      constexpr int CHUNKS = EPI == EPI_SWIGLU ? COLS / 32 : COLS / 16;
+      const int ocol0 = EPI == EPI_SWIGLU ? n0 / 2 : n0;  // first output column of the warp
 #pragma unroll
-        for (int c = 0; c < COLS / 32; ++c) {
-          float v[16];
+      for (int c = 0; c < CHUNKS; ++c) {
+        float v[16];
+        if (EPI == EPI_SWIGLU) {
+          // accumulator columns come in blocks of 16 gate rows then 16 up rows
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int cg = 32 * c + i;
             v[i] = ppdev::silu_mul(ppdev::dequant(run[cg], wsv[cg], a_s), ppdev::dequant(run[cg + 16], wsv[cg + 16], a_s));
           }
-          float4* dst = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + n0 / 2 + 16 * c);
+        } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          for (int i = 0; i < 16; ++i) v[i] = ppdev::dequant(run[16 * c + i], wsv[16 * c + i], a_s);
         }
-        return;
-      }
-      float4* rowp = reinterpret_cast<float4*>(p.out + (size_t)row * p.ldo + n0);
-      float4 xr[4];
-      if (EPI == EPI_RESID) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) xr[k] = rowp[k];
-      }
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<float4*>(stg + lane * EPI_LD + 4 * k) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        __syncwarp();
+        // lane -> row it*8 + lane/4, 16 bytes at column 4*(lane%4) of the chunk
+        const int rq = lane >> 2, cq = lane & 3;
+        float4 o[4], x[4];
 #pragma unroll
-      for (int c = 0; c < COLS / 16; ++c) {
-        float4 xn[4];
-        if (EPI == EPI_RESID && c + 1 < COLS / 16) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) xn[k] = rowp[4 * (c + 1) + k];  // next chunk's residual, loaded ahead
+        for (int it = 0; it < 4; ++it) {
+          const int r = 8 * it + rq;
+          o[it] = *reinterpret_cast<const float4*>(stg + r * EPI_LD + 4 * cq);
+          if (EPI == EPI_RESID && row0 + r < p.M)
+            x[it] = *reinterpret_cast<const float4*>(p.out + (size_t)(row0 + r) * p.ldo + ocol0 + 16 * c + 4 * cq);
         }
-        float v[16];
+        __syncwarp();  // the slice is free for the next chunk
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = ppdev::dequant(run[16 * c + i], wsv[16 * c + i], a_s);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        for (int it = 0; it < 4; ++it) {
+          const int r = 8 * it + rq;
+          if (row0 + r >= p.M) continue;
+          float4 w = o[it];
           if (EPI == EPI_RESID)
-            o = make_float4(__fadd_rn(xr[k].x, o.x), __fadd_rn(xr[k].y, o.y), __fadd_rn(xr[k].z, o.z),
-                            __fadd_rn(xr[k].w, o.w));
-          rowp[4 * c + k] = o;
-        }
-        if (EPI == EPI_RESID && c + 1 < COLS / 16) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) xr[k] = xn[k];
+            w = make_float4(__fadd_rn(x[it].x, w.x), __fadd_rn(x[it].y, w.y), __fadd_rn(x[it].z, w.z), __fadd_rn(x[it].w, w.w));
+          *reinterpret_cast<float4*>(p.out + (size_t)(row0 + r) * p.ldo + ocol0 + 16 * c + 4 * cq) = w;
         }
       }
     };
@@ -541,7 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (et < BN) wsb[et] = ws_r;
       asm volatile("bar.sync 2, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
       const bool whole = kb0 == 0 && kb1 == nkb;
-      if (whole || finish_partial(t)) epilogue(row, (t / p.num_m_tiles) * BN + colq * COLS, wsb + colq * COLS, as_r);
+      if (whole || finish_partial(t)) epilogue(row - lane, (t / p.num_m_tiles) * BN + colq * COLS, wsb + colq * COLS, as_r);
     }
   }
 
