@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                 int start_pos, int H, int Hkv, float* __restrict__ o, float qscale, float* __restrict__ part,
                 int n_ranges) {
   extern __shared__ __align__(16) float sm[];
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
   float* Qs = sm;              // [ROWS][HD] swizzled
   float* Ks = Qs + ROWS * HD;  // [KB][HD] swizzled
   float* Vs = Ks + KB * HD;    // [KB][HD]
@@ -279,6 +281,8 @@ template <int HD>
 __global__ void __launch_bounds__(256)
     k_attention_merge(int C, int start_pos, int H, int Hkv, float* __restrict__ o, const float* __restrict__ part,
                       int n_ranges) {
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
   constexpr int F4 = HD / 4;
   constexpr int CTAS_PER_TILE = ROWS * F4 / 256;
   const int G = H / Hkv;
@@ -336,12 +340,12 @@ cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows,
   if (n_ranges > 1 && (!part || part_bytes < attention_workspace_bytes(rows, start_pos, H, Hkv, HD)))
     return cudaErrorInvalidValue;
   const float qscale = (float)(1.4426950408889634 / sqrt((double)HD));
-  k_attention<HD><<<n_tiles * Hkv * n_ranges, THREADS, smem, s>>>(q, kc, vc, rows, start_pos, H, Hkv, o, qscale,
-                                                                  part, n_ranges);
-  if (n_ranges > 1)
-    k_attention_merge<HD><<<n_tiles * Hkv * (ROWS * HD / 4 / 256), 256, 0, s>>>(rows, start_pos, H, Hkv, o, part,
-                                                                                  n_ranges);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(k_attention<HD>, dim3(n_tiles * Hkv * n_ranges), dim3(THREADS), (size_t)smem, s, q, kc,
+                             vc, rows, start_pos, H, Hkv, o, qscale, part, n_ranges);
+  if (e == cudaSuccess && n_ranges > 1)
+    e = launch_pdl(k_attention_merge<HD>, dim3(n_tiles * Hkv * (ROWS * HD / 4 / 256)), dim3(256), 0, s, rows,
+                   start_pos, H, Hkv, o, (const float*)part, n_ranges);
+  return e;
 }
 
 }  // namespace

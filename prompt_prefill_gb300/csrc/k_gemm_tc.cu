@@ -283,6 +283,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
+  // the prologue above overlaps the previous kernel's tail; its results are read from here on
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -606,8 +609,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParam
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_tc<EPI, BN><<<2 * clusters, THREADS, C::SMEM_BYTES, s>>>(ma, mw, p);
-  return cudaGetLastError();
+  return launch_pdl(k_gemm_tc<EPI, BN>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, ma, mw, p);
 }
 
 template <int EPI>

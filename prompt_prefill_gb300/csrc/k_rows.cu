@@ -15,6 +15,8 @@ constexpr int kRowThreads = 256;
 // the device status word.
 __global__ void __launch_bounds__(kRowThreads) k_embed(const int32_t* __restrict__ tok, const float* __restrict__ emb,
                                                      int vocab, int dim, float* __restrict__ x, int* status) {
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
   const int i = blockIdx.x;
   const int t = tok[i];
   const bool ok = t >= 0 && t < vocab;
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(kRowThreads)
     k_norm_quant(const float* __restrict__ x, int ldx, const float* __restrict__ g, int k, float eps,
                  float* __restrict__ y_out, int8_t* __restrict__ q8, __half* __restrict__ q16,
                  float* __restrict__ a_scale) {
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
   __shared__ float red[kRowThreads / 32 + 1];
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
@@ -161,6 +165,8 @@ __global__ void k_rope_table(int max_pos, int hd, double theta, float2* __restri
 __global__ void __launch_bounds__(kRowThreads)
     k_rope_kv(const float* __restrict__ qkv, int start_pos, int H, int Hkv, int hd, const float2* __restrict__ table,
               float* __restrict__ q_out, float* __restrict__ k_cache, float* __restrict__ v_cache) {
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
   const int i = blockIdx.x;
   const int pos = start_pos + i;
   const int half = hd / 2;
@@ -195,6 +201,8 @@ __global__ void __launch_bounds__(kRowThreads)
 __global__ void __launch_bounds__(kRowThreads)
     k_lm_head(const int8_t* __restrict__ q8, const float* __restrict__ a_scale, const int8_t* __restrict__ w,
               const float* __restrict__ ws, int vocab, int dim, float* __restrict__ logits) {
+  ppdev::pdl_trigger();
+  ppdev::pdl_wait();
   extern __shared__ int4 qs[];
   const int n16 = dim / 16;
   for (int c = threadIdx.x; c < n16; c += kRowThreads) qs[c] = reinterpret_cast<const int4*>(q8)[c];
@@ -235,14 +243,14 @@ int sm_count() {
 
 cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab, int dim, float* x, int* status,
                          cudaStream_t s) {
-  k_embed<<<n, kRowThreads, 0, s>>>(tok, emb, vocab, dim, x, status);
-  return cudaGetLastError();
+  return launch_pdl(k_embed, dim3(n), dim3(kRowThreads), 0, s, tok, emb, vocab, dim, x, status);
 }
 
 cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
                               int8_t* q8, __half* q16, float* a_scale, cudaStream_t s) {
   const int nv = (k / 4 + kRowThreads - 1) / kRowThreads;  // float4 per thread
-  auto go = [&](auto kern) { kern<<<rows, kRowThreads, 0, s>>>(x, ldx, g, k, eps, y, q8, q16, a_scale); };
+  cudaError_t e = cudaSuccess;
+  auto go = [&](auto kern) { e = launch_pdl(kern, dim3(rows), dim3(kRowThreads), 0, s, x, ldx, g, k, eps, y, q8, q16, a_scale); };
   if (g) {
     if (nv <= 4) go(k_norm_quant<true, 4>);
     else if (nv <= 16) go(k_norm_quant<true, 16>);
@@ -252,7 +260,7 @@ cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows,
     else if (nv <= 16) go(k_norm_quant<false, 16>);
     else go(k_norm_quant<false, 0>);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s) {
@@ -262,16 +270,14 @@ cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cu
 
 cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
                            float* q_out, float* k_cache, float* v_cache, cudaStream_t s) {
-  k_rope_kv<<<rows, kRowThreads, 0, s>>>(qkv, start_pos, H, Hkv, hd, reinterpret_cast<const float2*>(table), q_out,
-                                         k_cache, v_cache);
-  return cudaGetLastError();
+  return launch_pdl(k_rope_kv, dim3(rows), dim3(kRowThreads), 0, s, qkv, start_pos, H, Hkv, hd,
+                    reinterpret_cast<const float2*>(table), q_out, k_cache, v_cache);
 }
 
 cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,
                            int dim, float* logits, cudaStream_t s) {
   const int blocks = sm_count() * 4;
-  k_lm_head<<<blocks, kRowThreads, dim, s>>>(q8, a_scale, w, ws, vocab, dim, logits);
-  return cudaGetLastError();
+  return launch_pdl(k_lm_head, dim3(blocks), dim3(kRowThreads), (size_t)dim, s, q8, a_scale, w, ws, vocab, dim, logits);
 }
 
 }  // namespace pp

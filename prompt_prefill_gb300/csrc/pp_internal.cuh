@@ -98,10 +98,36 @@ void kv_space_free(KvSpace* s);
 // Rows of the interleaved gate/up matrix: blocks of 16 gate rows then 16 up rows.
 constexpr int kSwiGluBlock = 16;
 
+// Launch kern<<<grid, block, smem, s>>>(args...) with programmatic dependent
+// launch allowed (the kernel calls ppdev::pdl_wait before using its inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace pp
 
 // ---------------------------------------------------------------- PTX helpers
 namespace ppdev {
+
+// Programmatic dependent launch: a kernel launched with launch_pdl may start
+// while the previous kernel of its stream is still running. pdl_trigger lets
+// this kernel's own dependents be scheduled; pdl_wait blocks until every
+// earlier kernel of the stream has finished and its writes are visible, and
+// must come before the first read of their results (and the first write of
+// anything they read). Both are no-ops for a kernel launched without it.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
