@@ -32,6 +32,17 @@ constexpr int KB = 64;        // keys per block
 constexpr int THREADS = 128;  // 16 row groups (ty) x 8 lanes (tx)
 constexpr int PS = 68;        // padded stride of the P tile, [key][4 ty + a]
 static_assert(kAttnRange % KB == 0, "a key range is a whole number of key blocks");
+// A row's reference maximum is raised only when a block's maximum exceeds it
+// by more than this (base-2 units), so unnormalised p stays below 2^kLazy.
+constexpr float kLazy = 8.f;
+
+// 2^x by the hardware approximation (relative error ~2^-22; 2^-inf = 0, and
+// results below 2^-126 flush to 0, which no sum here can notice).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // XOR swizzle of 16-byte chunks within a row of the Q and K tiles: rows r and
 // r' with r = r' (mod 8) never share a bank group when read at the same d.
@@ -99,6 +110,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (i > C - 1) i = C - 1;
     pos[a] = start_pos + i;
   }
+  const int pos_lo = start_pos + i0;  // the tile's first position: no key below it is masked
 
   constexpr int ND = HD / 32;  // float4 groups of dims per thread
   float O[4][ND][4];
@@ -136,12 +148,13 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int key0 = kb * KB;
     const bool more = kb + 1 < kb_end;
 
-    // S = Q K^T for rows ty+16a, keys tx+8b, in d order (one d for all 32 sums at a time).
-    float S[4][8];
+    // S = Q K^T for rows ty+16a, keys tx+8b. Packed f32 FMA over pairs of d:
+    // Sp[a][b].x sums the even d, .y the odd d (in d order); S = .x + .y.
+    float2 Sp[4][8];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 8; ++b) S[a][b] = 0.f;
+      for (int b = 0; b < 8; ++b) Sp[a][b] = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int d = 0; d < HD; d += 4) {
       float4 qv[4], kv[8];
@@ -152,56 +165,72 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].x, kv[b].x, S[a][b]);
+        for (int b = 0; b < 8; ++b)
+          Sp[a][b] = __ffma2_rn(make_float2(qv[a].x, qv[a].y), make_float2(kv[b].x, kv[b].y), Sp[a][b]);
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].y, kv[b].y, S[a][b]);
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].z, kv[b].z, S[a][b]);
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) S[a][b] = fmaf(qv[a].w, kv[b].w, S[a][b]);
+        for (int b = 0; b < 8; ++b)
+          Sp[a][b] = __ffma2_rn(make_float2(qv[a].z, qv[a].w), make_float2(kv[b].z, kv[b].w), Sp[a][b]);
     }
+    float S[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) S[a][b] = Sp[a][b].x + Sp[a][b].y;
     __syncthreads();  // every warp is done with Ks
     if (more) load_tile(Ks, kc, key0 + KB, true);
     else ppdev::cp_async_commit();
 
-    // Causal mask, online softmax (base 2). A row that has seen no key of this
-    // range yet (m = -inf) keeps m = -inf, l = 0, O = 0 through masked blocks.
+    // Causal mask (only in a block that crosses the tile's first position),
+    // then online softmax in base 2. The reference maximum m of a row moves
+    // only when a block's maximum exceeds it by more than kLazy, so p stays
+    // below 2^kLazy and the O rescale is skipped by every warp whose rows all
+    // kept their m. A row that has seen no key of this range yet (m = -inf)
+    // keeps m = -inf, l = 0, O = 0 through masked blocks.
+    if (key0 + KB - 1 > pos_lo) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          if (key0 + tx + 8 * b > pos[a]) S[a][b] = -INFINITY;
+    }
+    float alpha[4];
+    bool rescale = false;
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      float mb = -INFINITY;
+      float mb = S[a][0];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (key0 + tx + 8 * b > pos[a]) S[a][b] = -INFINITY;
-        mb = fmaxf(mb, S[a][b]);
-      }
+      for (int b = 1; b < 8; ++b) mb = fmaxf(mb, S[a][b]);
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-      const float mn = fmaxf(m[a], mb);
-      const float alpha = (mn == m[a]) ? 1.f : exp2f(m[a] - mn);
-      const float mref = (mn == -INFINITY) ? 0.f : mn;
+      alpha[a] = 1.f;
+      if (mb > m[a] + kLazy) {  // false for mb = -inf; true for the first finite block of a row
+        alpha[a] = ex2(m[a] - mb);
+        m[a] = mb;
+        rescale = true;
+      }
+      const float mref = (m[a] == -INFINITY) ? 0.f : m[a];
       float ls = 0.f;
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
-        const float p = exp2f(S[a][b] - mref);
+        const float p = ex2(S[a][b] - mref);
         ls += p;
         S[a][b] = p;
       }
       ls += __shfl_xor_sync(0xffffffffu, ls, 1);
       ls += __shfl_xor_sync(0xffffffffu, ls, 2);
       ls += __shfl_xor_sync(0xffffffffu, ls, 4);
-      l[a] = l[a] * alpha + ls;
-      m[a] = mn;
+      l[a] = fmaf(l[a], alpha[a], ls);
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-      for (int i = 0; i < ND; ++i)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) O[a][i][e] *= alpha;
+        for (int i = 0; i < ND; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) O[a][i][e] *= alpha[a];
     }
     // P -> smem, the thread's 4 rows of one key as one 16-byte store
 #pragma unroll
@@ -211,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     __syncthreads();
 
     // O += P V, keys in order.
-#pragma unroll 4
+#pragma unroll 8
     for (int j = 0; j < KB; ++j) {
       const float4 p4 = *reinterpret_cast<const float4*>(&Ps[j * PS + 4 * ty]);
       const float p[4] = {p4.x, p4.y, p4.z, p4.w};
