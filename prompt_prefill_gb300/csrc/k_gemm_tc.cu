@@ -81,7 +81,7 @@ struct TcParams {
   int32_t* acc_out;
   int* status;
   // stream-K: cluster c owns iterations [c*ipc, (c+1)*ipc) of the (tile, k-block)
-  // space; partial tiles meet in `part` (int32 [tile][slot][cta][128][BN]) and the
+  // space; partial tiles meet in `part` (int32, BM x BN per tile, slot and CTA) and the
   // last contributor, counted in `cnt` ([tile][cta], zero between launches), adds
   // the partial sums and runs the epilogue. ipc == 0: whole tiles round robin.
   int ipc;
@@ -436,13 +436,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int c_first = (int)(((long long)tile * nkb) / p.ipc);
       const int c_last = (int)((((long long)tile + 1) * nkb - 1) / p.ipc);
       const int n_contrib = c_last - c_first + 1;
-      const int row = quarter * 32 + lane;
+      // slot layout [tile][slot][cta][drain warp][COLS/4][32 lanes] of int4: the j-th
+      // store (or load) of a warp covers 512 contiguous bytes
+      const int dw = warp - DRAIN_WARP0;
       auto slot_ptr = [&](int slot) {
-        return p.part + ((((size_t)tile * p.max_slots + slot) * 2 + rank) * BM + row) * BN + colq * COLS;
+        return reinterpret_cast<int4*>(p.part) +
+               ((((size_t)tile * p.max_slots + slot) * 2 + rank) * N_DRAIN_WARPS + dw) * (COLS / 4) * 32 + lane;
       };
-      int4* mine = reinterpret_cast<int4*>(slot_ptr(cluster - c_first));
+      int4* mine = slot_ptr(cluster - c_first);
 #pragma unroll
-      for (int j = 0; j < COLS / 4; ++j) mine[j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
+      for (int j = 0; j < COLS / 4; ++j)
+        mine[32 * j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
       if (et == 0) *last_flag = atomicAdd(p.cnt + 2 * tile + rank, 1) == n_contrib - 1;
@@ -451,10 +455,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __threadfence();
       for (int sl = 0; sl < n_contrib; ++sl) {
         if (sl == cluster - c_first) continue;
-        const int4* other = reinterpret_cast<const int4*>(slot_ptr(sl));
+        const int4* other = slot_ptr(sl);
 #pragma unroll
         for (int j = 0; j < COLS / 4; ++j) {
-          const int4 v = __ldcg(other + j);
+          const int4 v = __ldcg(other + 32 * j);
           run[4 * j] += v.x;
           run[4 * j + 1] += v.y;
           run[4 * j + 2] += v.z;
@@ -658,13 +662,24 @@ cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k, int bn)
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tile width for an m x n x k GEMM: among the widths that divide n, the one
-// whose waves of tiles over the CTA pairs cost the fewest weight columns per
-// pair (ceil(tiles / pairs) x width); ties go to the wider tile. Shapes that
-// stream-K covers (few tiles, long k) keep the widest tile.
+// Tile width for an m x n x k GEMM. A shape with too few tiles to fill the CTA
+// pairs but enough k-blocks for stream-K (at least MIN_SK_KB per pair at width
+// 256) runs stream-K at width 256. The mainloop is bound by shared-memory
+// bandwidth (per k-block and CTA: TMA writes, the converter's int8 read and
+// fp16 write, the tensor core's reads of the 16 KB activation tile and of both
+// weight halves: 64 / 80 / 96 KB at widths 128 / 192 / 256, against 128 bytes
+// per clock); the activation tile costs the same at every width, so a 256-row
+// tile runs at the tensor core's rate while a 128-row tile reaches ~68% of it.
+// Otherwise the width whose waves of tiles over the pairs cost the fewest
+// weight columns per pair (ceil(tiles / pairs) x width); ties go to the wider
+// tile.
 int tc_bn(int m, int n, int k) {
   const int mc = max_clusters();
   const int nmt = (m + 2 * BM - 1) / (2 * BM);
+  if (n % 256 == 0) {
+    const long long tiles = (long long)nmt * (n / 256), total = tiles * (k / BK);
+    if (tiles < 2 * mc && total >= 2 * mc && (total + mc - 1) / mc >= MIN_SK_KB) return 256;
+  }
   int best = 0;
   long long best_cost = 0;
   for (int bn : {256, 192, 128}) {
