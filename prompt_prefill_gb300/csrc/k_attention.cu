@@ -29,6 +29,8 @@ namespace {
 
 constexpr int ROWS = 64;      // query rows per CTA
 constexpr int KB = 64;        // keys per block
+constexpr int NB = KB / 8;    // keys per thread in a block (tx + 8b)
+constexpr int CTAS_PER_SM = 2;
 constexpr int THREADS = 128;  // 16 row groups (ty) x 8 lanes (tx)
 constexpr int PS = 68;        // padded stride of the P tile, [key][4 ty + a]
 static_assert(kAttnRange % KB == 0, "a key range is a whole number of key blocks");
@@ -66,7 +68,7 @@ __device__ __forceinline__ Tile tile_of(int j, int n_tiles, int Hkv, int bq, int
 }
 
 template <int HD>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     k_attention(const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int C,
                 int start_pos, int H, int Hkv, float* __restrict__ o, float qscale, float* __restrict__ part,
                 int n_ranges) {
@@ -150,34 +152,34 @@ __global__ void __launch_bounds__(THREADS, 2)
 
     // S = Q K^T for rows ty+16a, keys tx+8b. Packed f32 FMA over pairs of d:
     // Sp[a][b].x sums the even d, .y the odd d (in d order); S = .x + .y.
-    float2 Sp[4][8];
+    float2 Sp[4][NB];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 8; ++b) Sp[a][b] = make_float2(0.f, 0.f);
+      for (int b = 0; b < NB; ++b) Sp[a][b] = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int d = 0; d < HD; d += 4) {
-      float4 qv[4], kv[8];
+      float4 qv[4], kv[NB];
 #pragma unroll
       for (int a = 0; a < 4; ++a) qv[a] = *reinterpret_cast<const float4*>(&Qs[swz<HD>(ty + 16 * a, d)]);
 #pragma unroll
-      for (int b = 0; b < 8; ++b) kv[b] = *reinterpret_cast<const float4*>(&Ks[swz<HD>(tx + 8 * b, d)]);
+      for (int b = 0; b < NB; ++b) kv[b] = *reinterpret_cast<const float4*>(&Ks[swz<HD>(tx + 8 * b, d)]);
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
+        for (int b = 0; b < NB; ++b)
           Sp[a][b] = __ffma2_rn(make_float2(qv[a].x, qv[a].y), make_float2(kv[b].x, kv[b].y), Sp[a][b]);
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
+        for (int b = 0; b < NB; ++b)
           Sp[a][b] = __ffma2_rn(make_float2(qv[a].z, qv[a].w), make_float2(kv[b].z, kv[b].w), Sp[a][b]);
     }
-    float S[4][8];
+    float S[4][NB];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 8; ++b) S[a][b] = Sp[a][b].x + Sp[a][b].y;
+      for (int b = 0; b < NB; ++b) S[a][b] = Sp[a][b].x + Sp[a][b].y;
     __syncthreads();  // every warp is done with Ks
     if (more) load_tile(Ks, kc, key0 + KB, true);
     else ppdev::cp_async_commit();
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
+        for (int b = 0; b < NB; ++b)
           if (key0 + tx + 8 * b > pos[a]) S[a][b] = -INFINITY;
     }
     float alpha[4];
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int a = 0; a < 4; ++a) {
       float mb = S[a][0];
 #pragma unroll
-      for (int b = 1; b < 8; ++b) mb = fmaxf(mb, S[a][b]);
+      for (int b = 1; b < NB; ++b) mb = fmaxf(mb, S[a][b]);
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       const float mref = (m[a] == -INFINITY) ? 0.f : m[a];
       float ls = 0.f;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
+      for (int b = 0; b < NB; ++b) {
         const float p = ex2(S[a][b] - mref);
         ls += p;
         S[a][b] = p;
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     // P -> smem, the thread's 4 rows of one key as one 16-byte store
 #pragma unroll
-    for (int b = 0; b < 8; ++b)
+    for (int b = 0; b < NB; ++b)
       *reinterpret_cast<float4*>(&Ps[(tx + 8 * b) * PS + 4 * ty]) = make_float4(S[0][b], S[1][b], S[2][b], S[3][b]);
     ppdev::cp_async_wait<1>();  // V of this block (the K prefetch may still be in flight)
     __syncthreads();

@@ -67,7 +67,8 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 // NV > 0: the thread's NV float4 of the row are loaded once and kept in
 // registers for all three passes (k <= 4 * NV * kRowThreads); NV == 0 streams
 // the row from memory in each pass (any k). Every pass visits the thread's
-// elements in the same order, so both forms give the same bits.
+// elements in the same order, so both forms give the same bits. q8 or q16 may
+// be null (that copy of the codes is not written).
 template <bool NORM, int NV>
 __global__ void __launch_bounds__(kRowThreads)
     k_norm_quant(const float* __restrict__ x, int ldx, const float* __restrict__ g, int k, float eps,
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     const size_t base = (size_t)row * k + 4 * (size_t)c;
     char4 p = make_char4((signed char)qi[0], (signed char)qi[1], (signed char)qi[2], (signed char)qi[3]);
-    *reinterpret_cast<char4*>(q8 + base) = p;
+    if (q8) *reinterpret_cast<char4*>(q8 + base) = p;
     if (q16) {
       __half2 h01 = __halves2half2(__int2half_rn(qi[0]), __int2half_rn(qi[1]));
       __half2 h23 = __halves2half2(__int2half_rn(qi[2]), __int2half_rn(qi[3]));

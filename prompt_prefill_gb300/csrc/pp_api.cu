@@ -616,6 +616,9 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
   const int QD = H * hd, QKV = (H + 2 * Hkv) * hd;
   const size_t kvl = m->kv_layer_floats;
   __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
+  // the tcgen05 GEMMs read only the fp16 codes: the int8 copy is written for the
+  // mma.sync engine and for the code trace
+  int8_t* q8 = (m->engine == PP_GEMM_TC && !m->trace_codes) ? nullptr : m->a8;
   if (m->trace)
     PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)l * m->trace_pos + pos0) * D, x, sizeof(float) * C * D,
                             cudaMemcpyDeviceToDevice, cs));
@@ -624,7 +627,7 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
   float* vcl = m->vc + kvl * l;
   // attention block
   PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(x, D, L.attn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
+    return launch_norm_quant(x, D, L.attn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs);
   }));
   PP_TRY(trace_codes(m, cs, l, 0, pos0, C, D));
   PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
@@ -636,18 +639,18 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
   }));
   if (attention_workspace_bytes(C, pos0, H, Hkv, hd)) m->stats.kernel_launches += 1;  // the range merge
   PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, m->a8, q16, m->as, cs);
+    return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, q8, q16, m->as, cs);
   }));
   PP_TRY(trace_codes(m, cs, l, 1, pos0, C, QD));
   PP_TRY(gemm(m, cs, EPI_RESID, mg, 1, L.so, L.wo, C, D, QD, x, D));
   // FFN block
   PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
+    return launch_norm_quant(x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs);
   }));
   PP_TRY(trace_codes(m, cs, l, 2, pos0, C, D));
   PP_TRY(gemm(m, cs, EPI_SWIGLU, mg, 2, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
   PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, m->a8, q16, m->as, cs);
+    return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, q8, q16, m->as, cs);
   }));
   PP_TRY(trace_codes(m, cs, l, 3, pos0, C, F));
   PP_TRY(gemm(m, cs, EPI_RESID, mg, 3, L.sd, L.wd, C, D, F, x, D));
