@@ -42,8 +42,8 @@ FP32_LANES = 128
 KERNEL_TRAFFIC = {
     # k_attention, mean over the 8 launches of one layer (chunk starts 0, 512, ..., 3584); the range merge
     # kernel's own bytes are listed in its profile summary
-    "attention": {"bytes_per_launch": 33064000.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
-                  "sha256": "b935ce7261b90c797190b3acd3c863bef673db8026cc438b0f54527e85b9319e"},
+    "attention": {"bytes_per_launch": 33111904.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
+                  "sha256": "1e155502dc2c759ef4d16023bb51f0bcd25131bdb98551d0241089dff6988c74"},
 }
 
 

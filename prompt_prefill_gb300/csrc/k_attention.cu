@@ -128,8 +128,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   }
 
   // K/V tiles stream through shared memory with cp.async: K of block kb+1
-  // loads while P V of block kb runs, V of block kb+1 while S of block kb+1
-  // runs. Keys past the tile's last position are zero-filled.
+  // loads while softmax and P V of block kb run, V of block kb+1 while S of
+  // block kb+1 runs. Two CTA barriers per block: before each, every thread
+  // waits for its own copies in flight (V of the block before the first, K of
+  // the next block before the second), so each barrier both frees a buffer
+  // and publishes the copy that lands in the other. P is private to a warp
+  // (a thread reads only the rows of its own ty), so it needs only __syncwarp.
+  // Keys past the tile's last position are zero-filled.
   auto load_tile = [&](float* dst, const float* src, int key0, bool swizzle) {
     for (int e = tid; e < KB * C4; e += THREADS) {
       const int j = e / C4, c = e % C4;
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   };
   load_tile(Ks, kc, kb_begin * KB, true);
   load_tile(Vs, vc, kb_begin * KB, false);
-  ppdev::cp_async_wait<1>();  // K of the first block
+  ppdev::cp_async_wait<1>();  // K of the first block (V may still be in flight)
   __syncthreads();
 
   for (int kb = kb_begin; kb < kb_end; ++kb) {
@@ -180,9 +185,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int b = 0; b < NB; ++b) S[a][b] = Sp[a][b].x + Sp[a][b].y;
-    __syncthreads();  // every warp is done with Ks
+    ppdev::cp_async_wait<0>();  // V of this block
+    __syncthreads();            // every warp is done with Ks; V of this block visible
     if (more) load_tile(Ks, kc, key0 + KB, true);
-    else ppdev::cp_async_commit();
 
     // Causal mask (only in a block that crosses the tile's first position),
     // then online softmax in base 2. The reference maximum m of a row moves
@@ -238,8 +243,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 #pragma unroll
     for (int b = 0; b < NB; ++b)
       *reinterpret_cast<float4*>(&Ps[(tx + 8 * b) * PS + 4 * ty]) = make_float4(S[0][b], S[1][b], S[2][b], S[3][b]);
-    ppdev::cp_async_wait<1>();  // V of this block (the K prefetch may still be in flight)
-    __syncthreads();
+    __syncwarp();  // the warp's P rows are written
 
     // O += P V, keys in order.
 #pragma unroll 8
@@ -264,11 +268,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         }
       }
     }
-    __syncthreads();  // every warp is done with Vs and Ps
+    ppdev::cp_async_wait<0>();  // K of the next block
+    __syncthreads();            // every warp is done with Vs; K of the next block visible
     if (more) load_tile(Vs, vc, key0 + KB, false);
-    else ppdev::cp_async_commit();
-    ppdev::cp_async_wait<1>();  // K of the next block
-    __syncthreads();
   }
   ppdev::cp_async_wait<0>();
 
