@@ -88,6 +88,7 @@ struct TcParams {
   int max_slots;
   int32_t* part;
   int* cnt;
+  TcRope rope;            // EPI_ROPE destinations
   long long wait_cycles;  // bound of every mbarrier wait (clock64 cycles)
   int hold_mma;           // test hook: the MMA issuer issues nothing, so every other role's wait runs out
 };
@@ -491,6 +492,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         return;
       }
+      if (EPI == EPI_ROPE) {
+        // RoPE + K/V write. A 16-column chunk starts at a multiple of 16, so it lies
+        // in one head; in a q or k head its columns are the pairs (j, j + hd/2) for
+        // 8 consecutive j. The warp's 32 rows x 16 columns go through its staging
+        // slice; lane (rq, cq) then rotates 2 pairs of row 8 it + rq and stores them
+        // as 8 bytes at dims j and j + hd/2 (8 rows x 32 bytes per instruction).
+        const TcRope& rp = p.rope;
+        const int hd = rp.hd, half = hd >> 1, nqk = (rp.H + rp.Hkv) * hd;
+        const int rq = lane >> 2, cq = lane & 3;
+        // (cos, sin) of the lane's 2 pairs in each of its 4 rows, read one chunk
+        // ahead through the read-only path (rows past M read the last row's entries)
+        auto load_tab = [&](int c, float4 (&t)[4]) {
+          const int col = n0 + 16 * c;
+          if (col >= nqk) return;
+          const int j = ((col % hd) >> 1) + 2 * cq;
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int pos = rp.pos0 + min(row0 + 8 * it + rq, p.M - 1);
+            t[it] = __ldg(reinterpret_cast<const float4*>(rp.table + ((size_t)pos * half + j) * 2));
+          }
+        };
+        float4 tnext[4];
+        load_tab(0, tnext);
+#pragma unroll
+        for (int c = 0; c < COLS / 16; ++c) {
+          float4 tc[4];
+#pragma unroll
+          for (int it = 0; it < 4; ++it) tc[it] = tnext[it];
+          if (c + 1 < COLS / 16) load_tab(c + 1, tnext);
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = ppdev::dequant(run[16 * c + i], wsv[16 * c + i], a_s);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4*>(stg + lane * EPI_LD + 4 * k) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          __syncwarp();
+          const int col = n0 + 16 * c;
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int r = 8 * it + rq, row_r = row0 + r;
+            const float4 x = *reinterpret_cast<const float4*>(stg + r * EPI_LD + 4 * cq);
+            if (row_r >= p.M) continue;
+            const int pos = rp.pos0 + row_r;
+            if (col < nqk) {
+              const int head = col / hd, j = ((col % hd) >> 1) + 2 * cq;
+              const float4 t = tc[it];
+              const float2 r0 = ppdev::rope_rot(x.x, x.y, make_float2(t.x, t.y));
+              const float2 r1 = ppdev::rope_rot(x.z, x.w, make_float2(t.z, t.w));
+              float* dst = head < rp.H ? rp.q_out + ((size_t)row_r * rp.H + head) * hd
+                                       : rp.k_cache + ((size_t)pos * rp.Hkv + (head - rp.H)) * hd;
+              *reinterpret_cast<float2*>(dst + j) = make_float2(r0.x, r1.x);
+              *reinterpret_cast<float2*>(dst + j + half) = make_float2(r0.y, r1.y);
+            } else {
+              *reinterpret_cast<float4*>(rp.v_cache + (size_t)pos * rp.Hkv * hd + (col - nqk) + 4 * cq) = x;
+            }
+          }
+          __syncwarp();  // the slice is free for the next chunk
+        }
+        return;
+      }
       constexpr int CHUNKS = EPI == EPI_SWIGLU ? COLS / 32 : COLS / 16;
       const int ocol0 = EPI == EPI_SWIGLU ? n0 / 2 : n0;  // first output column of the warp
 #pragma unroll
@@ -737,7 +798,8 @@ void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters
 
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
-                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits) {
+                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits,
+                           const TcRope& rope) {
   TcParams p{};
   p.wait_cycles = waits.cycles;
   p.hold_mma = waits.hold_mma;
@@ -752,6 +814,7 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
   p.ldo = ldo;
   p.acc_out = acc;
   p.status = status;
+  p.rope = rope;
   Plan pl = plan(m, n, k);
   if (!pl.bn || pl.bn != bn) return cudaErrorInvalidValue;  // the weight map was made for another tile width
   p.num_tiles = pl.num_tiles;
@@ -769,6 +832,11 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
     case EPI_RESID: return launch_bn<EPI_RESID>(bn, ma, mw, p, pl.clusters, s);
     case EPI_SWIGLU: return launch_bn<EPI_SWIGLU>(bn, ma, mw, p, pl.clusters, s);
     case EPI_ACC: return launch_bn<EPI_ACC>(bn, ma, mw, p, pl.clusters, s);
+    case EPI_ROPE:
+      if (!rope.table || !rope.q_out || !rope.k_cache || !rope.v_cache || rope.hd % 16 ||
+          n != (rope.H + 2 * rope.Hkv) * rope.hd)
+        return cudaErrorInvalidValue;
+      return launch_bn<EPI_ROPE>(bn, ma, mw, p, pl.clusters, s);
     default: return cudaErrorInvalidValue;
   }
 }

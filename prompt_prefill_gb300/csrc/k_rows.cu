@@ -162,7 +162,9 @@ __global__ void k_rope_table(int max_pos, int hd, double theta, float2* __restri
 }
 
 // RoPE + K/V write ("Single-pass prefill": K/V history written position by
-// position). qkv row = [q heads | k heads | v heads]; pairs (j, j + hd/2).
+// position). qkv row = [q heads | k heads | v heads]; pairs (j, j + hd/2), read
+// from columns j and j + hd/2 of the head, or (PAIRED) 2j and 2j + 1.
+template <bool PAIRED>
 __global__ void __launch_bounds__(kRowThreads)
     k_rope_kv(const float* __restrict__ qkv, int start_pos, int H, int Hkv, int hd, const float2* __restrict__ table,
               float* __restrict__ q_out, float* __restrict__ k_cache, float* __restrict__ v_cache) {
@@ -178,9 +180,10 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int e = threadIdx.x; e < n_rot; e += kRowThreads) {
     const int head = e / half, j = e % half;
     const float2 cs = tab[j];
-    const float a = row[head * hd + j], b = row[head * hd + j + half];
-    const float ra = a * cs.x - b * cs.y;
-    const float rb = a * cs.y + b * cs.x;
+    const float a = PAIRED ? row[head * hd + 2 * j] : row[head * hd + j];
+    const float b = PAIRED ? row[head * hd + 2 * j + 1] : row[head * hd + j + half];
+    const float2 r2 = ppdev::rope_rot(a, b, cs);
+    const float ra = r2.x, rb = r2.y;
     if (head < H) {
       float* dst = q_out + ((size_t)i * H + head) * hd;
       dst[j] = ra;
@@ -270,9 +273,9 @@ cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cu
 }
 
 cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
-                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s) {
-  return launch_pdl(k_rope_kv, dim3(rows), dim3(kRowThreads), 0, s, qkv, start_pos, H, Hkv, hd,
-                    reinterpret_cast<const float2*>(table), q_out, k_cache, v_cache);
+                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s, bool paired) {
+  return launch_pdl(paired ? k_rope_kv<true> : k_rope_kv<false>, dim3(rows), dim3(kRowThreads), 0, s, qkv, start_pos,
+                    H, Hkv, hd, reinterpret_cast<const float2*>(table), q_out, k_cache, v_cache);
 }
 
 cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,

@@ -80,21 +80,29 @@ LayerLayout make_layout(const pp_config& c) {
 }
 
 // Repack layer `l` of the caller's weights into `dst` (host memory):
-// wq|wk|wv rows fused into one QKV matrix; gate and up rows interleaved in
-// blocks of 16 (16 gate rows, then the same 16 up rows) so that one GEMM tile
-// holds both operands of SwiGLU.
+// wq|wk|wv rows fused into one QKV matrix, the rows of every q and k head in
+// RoPE pair order (row 2j + e of the head is its row j + e * hd/2, so the two
+// members of a rotated pair are adjacent output columns); gate and up rows
+// interleaved in blocks of 16 (16 gate rows, then the same 16 up rows) so that
+// one GEMM tile holds both operands of SwiGLU.
 void pack_layer(const pp_config& c, const LayerLayout& lay, const pp_weights& w, int l, uint8_t* dst) {
-  const size_t D = c.dim, hd = c.head_dim, F = c.ffn;
+  const size_t D = c.dim, hd = c.head_dim, F = c.ffn, half = hd / 2;
   const size_t qr = c.n_heads * hd, kr = c.n_kv_heads * hd;
   const int8_t* const* W = w.w + 7 * l;
   const float* const* S = w.w_scale + 7 * l;
   uint8_t* p = dst + lay.wqkv;
-  memcpy(p, W[0], qr * D);
-  memcpy(p + qr * D, W[1], kr * D);
-  memcpy(p + (qr + kr) * D, W[2], kr * D);
   float* s = reinterpret_cast<float*>(dst + lay.sqkv);
-  memcpy(s, S[0], qr * 4);
-  memcpy(s + qr, S[1], kr * 4);
+  auto pair_rows = [&](const int8_t* src, const float* ssrc, size_t heads, int8_t* out, float* sout) {
+    for (size_t h = 0; h < heads; ++h)
+      for (size_t r = 0; r < hd; ++r) {
+        const size_t from = h * hd + (r >> 1) + (r & 1) * half;
+        memcpy(out + (h * hd + r) * D, src + from * D, D);
+        sout[h * hd + r] = ssrc[from];
+      }
+  };
+  pair_rows(W[0], S[0], c.n_heads, reinterpret_cast<int8_t*>(p), s);
+  pair_rows(W[1], S[1], c.n_kv_heads, reinterpret_cast<int8_t*>(p + qr * D), s + qr);
+  memcpy(p + (qr + kr) * D, W[2], kr * D);
   memcpy(s + qr + kr, S[2], kr * 4);
   memcpy(dst + lay.wo, W[3], D * qr);
   memcpy(dst + lay.so, S[3], D * 4);
@@ -297,14 +305,14 @@ int tc_segment() { return g_tc_seg.load(); }
 // One projection GEMM of the layer whose weight block sits at map group `mg`
 // (matrix `which`: 0 qkv, 1 o, 2 gate/up, 3 down).
 int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* ws, const int8_t* w, int M, int N,
-         int K, float* out, int ldo) {
+         int K, float* out, int ldo, const TcRope& rope = TcRope{}) {
   if (m->engine == PP_GEMM_TC) {
     const int bi = tc_bn_index(M, N, K);
     const CUtensorMap& wm = m->wmap[((size_t)mg * 4 + which) * 3 + bi];
     const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
     return launch(m, PP_KERNEL_GEMM, st, [&] {
       return launch_gemm_tc(epi, am, wm, kTcBn[bi], ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
-                            st);
+                            st, TcWaits{}, rope);
     });
   }
   return launch(m, PP_KERNEL_GEMM, st, [&] {
@@ -630,10 +638,24 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
     return launch_norm_quant(x, D, L.attn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs);
   }));
   PP_TRY(trace_codes(m, cs, l, 0, pos0, C, D));
-  PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
-  PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
-    return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs);
-  }));
+  if (m->engine == PP_GEMM_TC) {
+    // QKV projection with RoPE and the K/V write in its epilogue
+    TcRope rp;
+    rp.table = m->rope;
+    rp.pos0 = pos0;
+    rp.H = H;
+    rp.Hkv = Hkv;
+    rp.hd = hd;
+    rp.q_out = m->qr;
+    rp.k_cache = kcl;
+    rp.v_cache = vcl;
+    PP_TRY(gemm(m, cs, EPI_ROPE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, nullptr, QKV, rp));
+  } else {
+    PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
+    PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
+      return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs, true);
+    }));
+  }
   PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
     return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
   }));

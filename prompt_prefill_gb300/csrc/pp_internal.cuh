@@ -15,7 +15,9 @@
 namespace pp {
 
 // Epilogue selector of the GEMM kernels (PP_EPI_* plus the raw int32 form).
-enum Epi : int { EPI_STORE = PP_EPI_STORE, EPI_RESID = PP_EPI_RESID, EPI_SWIGLU = PP_EPI_SWIGLU, EPI_ACC = 3 };
+// EPI_ROPE (tcgen05 engine only): RoPE + K/V write of a QKV projection whose q and k
+// head rows are in pair order (see TcRope).
+enum Epi : int { EPI_STORE = PP_EPI_STORE, EPI_RESID = PP_EPI_RESID, EPI_SWIGLU = PP_EPI_SWIGLU, EPI_ACC = 3, EPI_ROPE = 4 };
 
 // Device status word values (written by kernels, read by pp_device_status).
 enum : int { DEV_OK = 0, DEV_BAD_TOKEN = 1, DEV_TIMEOUT = 2 };
@@ -26,8 +28,10 @@ cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab,
 cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
                               int8_t* q8, __half* q16, float* a_scale, cudaStream_t s);
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s);
+// paired: the q and k head columns of qkv are in pair order (dims j and j + hd/2 at
+// columns 2j and 2j + 1 of the head), as the model's packed QKV weights produce them.
 cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
-                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s);
+                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s, bool paired = false);
 cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,
                            int dim, float* logits, cudaStream_t s);
 
@@ -63,9 +67,19 @@ struct TcWaits {
   long long cycles = 4000000000LL;  // ~2 s at 2 GHz
   int hold_mma = 0;
 };
+// EPI_ROPE destinations: the GEMM's n = (H + 2 Hkv) hd columns are q heads, k heads, v heads,
+// with the rows of every q and k head in pair order; row r of the GEMM is position pos0 + r.
+struct TcRope {
+  const float* table = nullptr;  // [max_pos][hd/2] (cos, sin)
+  int pos0 = 0, H = 0, Hkv = 0, hd = 0;
+  float* q_out = nullptr;    // [m][H][hd]
+  float* k_cache = nullptr;  // [pos][Hkv][hd]
+  float* v_cache = nullptr;  // [pos][Hkv][hd]
+};
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
-                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits = TcWaits{});
+                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits = TcWaits{},
+                           const TcRope& rope = TcRope{});
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)
@@ -163,6 +177,13 @@ __device__ __forceinline__ void mma_s8_16832(int32_t (&d)[4], const uint32_t (&a
 // each product rounded to nearest (no contraction).
 __device__ __forceinline__ float dequant(int32_t acc, float ws, float as) {
   return __fmul_rn(__fmul_rn(__int2float_rn(acc), ws), as);
+}
+
+// RoPE rotation of the pair (a, b) = (x_j, x_{j + hd/2}) by (c, s) = (cos, sin):
+// (a c - b s, a s + b c), each a fused multiply-add of one rounded product, in
+// this fixed form wherever the model rotates (the GEMM epilogue and the RoPE kernel).
+__device__ __forceinline__ float2 rope_rot(float a, float b, float2 cs) {
+  return make_float2(__fmaf_rn(a, cs.x, -__fmul_rn(b, cs.y)), __fmaf_rn(a, cs.y, __fmul_rn(b, cs.x)));
 }
 
 // SwiGLU gate: silu(g) * u = g / (1 + exp(-g)) * u with the fast exponential and
