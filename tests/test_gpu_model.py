@@ -255,3 +255,34 @@ def test_engines_give_identical_logits():
         out[eng] = g.prefill(toks, 0, 8)
         g.close()
     assert np.array_equal(bits(out[pp.PP_GEMM_MMA]), bits(out[pp.PP_GEMM_TC]))
+
+
+def test_head_dim_128_fused_rope_engines_and_oracle():
+    # The 8B head layout (head_dim 128, 4 query heads per KV head, theta 5e5) on a 2-layer model. The
+    # tcgen05 path applies RoPE and writes K/V in its QKV GEMM epilogue; the mma.sync path runs the RoPE
+    # kernel on the same pair-ordered columns: logits and K/V rows agree bit for bit, the chunked prefill
+    # equals the per-token one, and layer by layer (codes forced at tie decisions) the tcgen05 path matches
+    # the oracle, as for the 350M and 1B classes.
+    torch_cuda()
+    cfg = synth.ModelConfig("hd128", 1024, 2, 8, 2, 128, 2048, 2048, rope_theta=500000.0, max_seq=256,
+                            seed=4321, prompt_len=200, chunk=64)
+    m = synth.make_model(cfg)
+    toks = synth.prompt(cfg)
+    out, kv = {}, {}
+    for eng in (pp.PP_GEMM_MMA, pp.PP_GEMM_TC):
+        g = load(m, max_seq=256, max_chunk=64, gemm_engine=eng)
+        try:
+            out[eng] = g.prefill(toks, 0, 64)
+            kv[eng] = [g.kv(L, which, 0, len(toks)) for L in range(cfg.n_layers) for which in (0, 1)]
+            if eng == pp.PP_GEMM_TC:
+                g.kv_reset()
+                assert np.array_equal(bits(g.prefill(toks, 0, 1)), bits(out[eng]))
+                got, ref, report = layerwise_forced(m, g, toks, 64)
+                assert np.array_equal(bits(got), bits(out[eng]))
+        finally:
+            g.close()
+    assert np.array_equal(bits(out[pp.PP_GEMM_MMA]), bits(out[pp.PP_GEMM_TC]))
+    for a, b in zip(kv[pp.PP_GEMM_MMA], kv[pp.PP_GEMM_TC]):
+        assert np.array_equal(bits(a), bits(b))
+    print("hd128 per-layer (tie decisions, max margin):", _summary(report))
+    _assert_e2e(got, ref, "hd128 final")
