@@ -284,9 +284,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
-  // the prologue above overlaps the previous kernel's tail; its results are read from here on
+  // The prologue above overlaps the previous kernel's tail; its results are read
+  // from here on. The producer first issues the weight loads of the stages it
+  // can fill without waiting (no kernel of the stream writes the weights; a
+  // streamed layer's copy is waited for before the layer's first kernel) and
+  // only then waits.
   ppdev::pdl_trigger();
-  ppdev::pdl_wait();
+  if (warp != 0) ppdev::pdl_wait();
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -301,17 +305,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t ph = 0;
       int issued[STAGES] = {0};
       const Sched sc(p, cluster, n_clusters);
+      // weights of the first STAGES k-blocks (every stage starts empty), then the wait
+      int pre = 0;
+      for (int u = 0; u < sc.units() && pre < STAGES; ++u) {
+        int t, kb0, kb1;
+        sc.unit(u, t, kb0, kb1);
+        const int n_row = (t / p.num_m_tiles) * BN + (int)rank * (BN / 2);
+        for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
+          mbar_expect_tx(full_b(pre), A_BYTES + C::W_BYTES);
+          tma_load_2d(sW(pre), &tmW, kb * BK, n_row, full_b(pre));
+          issued[pre] = 1;
+        }
+      }
+      ppdev::pdl_wait();
+      int g = 0;  // k-blocks issued so far (the first `pre` have their weights in flight)
       for (int u = 0; u < sc.units() && !*abort_flag; ++u) {
         int t, kb0, kb1;
         sc.unit(u, t, kb0, kb1);
         const int m_row = (t % p.num_m_tiles) * 2 * BM + (int)rank * BM;
         const int n_row = (t / p.num_m_tiles) * BN + (int)rank * (BN / 2);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(empty_b(s), ph ^ 1, p.wait_cycles)) { fail(); break; }
-          mbar_expect_tx(full_b(s), A_BYTES + C::W_BYTES);
-          tma_load_2d(sA(s), &tmA, kb * BK, m_row, full_b(s));
-          tma_load_2d(sW(s), &tmW, kb * BK, n_row, full_b(s));
-          issued[s] = 1;
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+          if (g < pre) {
+            tma_load_2d(sA(s), &tmA, kb * BK, m_row, full_b(s));
+          } else {
+            if (!mbar_wait(empty_b(s), ph ^ 1, p.wait_cycles)) { fail(); break; }
+            mbar_expect_tx(full_b(s), A_BYTES + C::W_BYTES);
+            tma_load_2d(sA(s), &tmA, kb * BK, m_row, full_b(s));
+            tma_load_2d(sW(s), &tmW, kb * BK, n_row, full_b(s));
+            issued[s] = 1;
+          }
           if (++s == STAGES) { s = 0; ph ^= 1; }
         }
       }

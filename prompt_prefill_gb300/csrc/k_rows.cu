@@ -27,35 +27,26 @@ __global__ void __launch_bounds__(kRowThreads) k_embed(const int32_t* __restrict
 }
 
 // Fixed-order block reductions: per-thread partials, xor butterfly within a
-// warp, then warp 0 folds the 8 warp results in index order.
+// warp, then every thread folds the warp results in index order (one barrier;
+// each reduction of a kernel uses its own `red` array, so none is reused).
 __device__ __forceinline__ float block_sum(float v, float* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) red[w] = v;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   float s = 0.f;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kRowThreads / 32; ++i) s += red[i];
-    red[kRowThreads / 32] = s;
-  }
-  __syncthreads();
-  return red[kRowThreads / 32];
+#pragma unroll
+  for (int i = 0; i < kRowThreads / 32; ++i) s += red[i];
+  return s;
 }
 
 __device__ __forceinline__ float block_max(float v, float* red) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (l == 0) red[w] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = 0.f;
-    for (int i = 0; i < kRowThreads / 32; ++i) m = fmaxf(m, red[i]);
-    red[kRowThreads / 32] = m;
-  }
-  __syncthreads();
-  return red[kRowThreads / 32];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowThreads / 32; ++i) m = fmaxf(m, red[i]);
+  return m;
 }
 
 // RMSNorm (optional) then the per-token absmax quantiser ("Batched Prefill",
@@ -76,7 +67,7 @@ __global__ void __launch_bounds__(kRowThreads)
                  float* __restrict__ a_scale) {
   ppdev::pdl_trigger();
   ppdev::pdl_wait();
-  __shared__ float red[kRowThreads / 32 + 1];
+  __shared__ float red_sum[kRowThreads / 32], red_max[kRowThreads / 32];
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
   const float4* g4 = reinterpret_cast<const float4*>(g);
@@ -110,7 +101,7 @@ __global__ void __launch_bounds__(kRowThreads)
       ss = fmaf(v.z, v.z, ss);
       ss = fmaf(v.w, v.w, ss);
     });
-    ss = block_sum(ss, red);
+    ss = block_sum(ss, red_sum);
     r = 1.0f / sqrtf(ss / (float)k + eps);
   }
   auto yval = [&](float xv_, float gv) { return NORM ? __fmul_rn(__fmul_rn(xv_, r), gv) : xv_; };
@@ -122,7 +113,7 @@ __global__ void __launch_bounds__(kRowThreads)
     amax = fmaxf(amax, fabsf(yval(v.z, gg.z)));
     amax = fmaxf(amax, fabsf(yval(v.w, gg.w)));
   });
-  amax = block_max(amax, red);
+  amax = block_max(amax, red_max);
   const bool zero = amax == 0.f;
   const float inv = zero ? 0.f : 127.0f / amax;
   for_each([&](const float4& v, int c) {
