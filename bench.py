@@ -221,6 +221,13 @@ def max_over_ranks(pg, value: float) -> float:
     return float(t.item())
 
 
+def replica_tok_per_s(world: int, tokens_per_rank: int, steps: int, seconds_max: float) -> float:
+    """Whole-job throughput of N replicas: every rank prefills its own
+    `tokens_per_rank`-token prompt `steps` times; the job takes as long as the
+    slowest rank (`seconds_max`, the max over ranks)."""
+    return world * tokens_per_rank * steps / seconds_max
+
+
 # ----------------------------------------------------------------------------- CPU oracle leg
 def oracle_sample(model, cfg, sample_tokens: int, toks) -> tuple[float, int, float]:
     """Time the oracle (as it stands) prefilling the first `sample_tokens`
@@ -347,8 +354,8 @@ def run_ours(args, cfg, world, rank, local, pg):
     t_e2e = max_over_ranks(pg, t_e2e)
     assert np.array_equal(host_logits.view(np.uint32), logits.view(np.uint32)), "host and device paths differ"
 
-    value = world * P * args.steps / (ms_max / 1000.0)
-    e2e_value = world * P * args.steps / t_e2e
+    value = replica_tok_per_s(world, P, args.steps, ms_max / 1000.0)
+    e2e_value = replica_tok_per_s(world, P, args.steps, t_e2e)
     work = algorithmic_work(cfg, P, chunk)[dominant]
     achieved_ms = stats["prof_ms"] / max(1, stats["prof_launches"])
     per_launch = work["work"] / max(1, stats["prof_launches"] // args.steps)
