@@ -385,6 +385,12 @@ def run_ours(args, cfg, world, rank, local, pg):
                      "unit": work["unit"], "frac": achieved / peak,
                      "traffic": kernel_traffic(dominant, "8b" if (args.workload, args.prompt, args.chunk) == ("8b", None, 512) else ""),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)", "peak_source": peak_src},
+        # the projection GEMMs as one class: the step's int8 GEMM work over their summed launch times (each
+        # launch bracketed by CUDA events in a profiled step), against the measured dense f16/bf16 rate (the
+        # tensor path they run on; sm_103a has no integer MMA kind)
+        "gemm_roofline": {"bound": "tensor", "achieved": gemm_ops / (class_ms["gemm"] / 1000.0) / 1e12,
+                          "peak": peak_for("tensor", peaks)[0], "unit": "TFLOP/s",
+                          "frac": gemm_ops / (class_ms["gemm"] / 1000.0) / 1e12 / peak_for("tensor", peaks)[0]},
         "kernel_ms_per_step": {k: v for k, v in class_ms.items()},
         "weight_bytes_read_per_step": weight_bytes_read(cfg, P, chunk),
         "weight_bytes_naive_per_step": layer_weight_bytes(cfg) * cfg.n_layers * P + cfg.vocab * cfg.dim + 4 * cfg.vocab,
