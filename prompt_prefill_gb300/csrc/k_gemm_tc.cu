@@ -453,9 +453,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(acce_b(buf), 0);
     };
 
+    // After the CTA's last unit is drained its pipeline stages are idle. There
+    // the other contributors' partial sums and the epilogue's residual rows are
+    // brought in with cp.async, every copy of a batch in flight at once, instead
+    // of register loads that wait on L2 chunk by chunk. Each drain warp owns one
+    // region, used by its partial slots and then by its residual rows.
+    constexpr int XLD = COLS + 4;  // padded row of a warp's staged residual rows
+    constexpr int PARK_BYTES = (COLS * 128 > 32 * XLD * 4) ? COLS * 128 : 32 * XLD * 4;
+    static_assert(N_DRAIN_WARPS * PARK_BYTES <= STAGES * C::STAGE_BYTES, "parking fits in the stages");
+    uint8_t* const park = gbase + (size_t)(warp - DRAIN_WARP0) * PARK_BYTES;
+    int4* const park_i4 = reinterpret_cast<int4*>(park);  // [COLS/4][32 lanes]
+    float* const park_x = reinterpret_cast<float*>(park);  // [32 rows][XLD]
+
     // Stream-K: this CTA's partial sums of `tile` meet the other contributors'.
     // Returns true for the last contributor, whose run[] then holds the totals.
-    auto finish_partial = [&](int tile) -> bool {
+    // parked: this is the CTA's last unit (the stages are free).
+    auto finish_partial = [&](int tile, bool parked) -> bool {
       const int c_first = (int)(((long long)tile * nkb) / p.ipc);
       const int c_last = (int)((((long long)tile + 1) * nkb - 1) / p.ipc);
       const int n_contrib = c_last - c_first + 1;
@@ -479,9 +492,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int sl = 0; sl < n_contrib; ++sl) {
         if (sl == cluster - c_first) continue;
         const int4* other = slot_ptr(sl);
+        if (parked) {
+          // each lane copies and then reads back only its own 16-byte pieces
+#pragma unroll 8
+          for (int j = 0; j < COLS / 4; ++j) ppdev::cp_async16(park_i4 + 32 * j + lane, other + 32 * j, 16);
+          ppdev::cp_async_commit();
+          ppdev::cp_async_wait<0>();
+        }
 #pragma unroll
         for (int j = 0; j < COLS / 4; ++j) {
-          const int4 v = __ldcg(other + 32 * j);
+          const int4 v = parked ? park_i4[32 * j + lane] : __ldcg(other + 32 * j);
           run[4 * j] += v.x;
           run[4 * j + 1] += v.y;
           run[4 * j + 2] += v.z;
@@ -501,7 +521,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // instruction (16 full 32-byte sectors), instead of one 16-byte piece of
     // each of 32 rows; residual rows are loaded in the same pattern.
     float* const stg = epi_s + (warp - DRAIN_WARP0) * (32 * EPI_LD);
-    auto epilogue = [&](int row0, int n0, const float* wsv, float a_s) {  // row0: the warp's first row
+    auto epilogue = [&](int row0, int n0, const float* wsv, float a_s, bool parked) {  // row0: the warp's first row
       const int row = row0 + lane;
       if (EPI == EPI_ACC) {
         if (row >= p.M) return;
@@ -576,6 +596,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       constexpr int CHUNKS = EPI == EPI_SWIGLU ? COLS / 32 : COLS / 16;
       const int ocol0 = EPI == EPI_SWIGLU ? n0 / 2 : n0;  // first output column of the warp
+      // (only for wide tiles: with 4 chunks or fewer the one-chunk-ahead loads measured as fast)
+      parked = parked && COLS >= 128;
+      if (EPI == EPI_RESID && parked) {
+        // the warp's 32 rows x COLS residual columns in one batch (rows past M are zero-filled)
+        __syncwarp();  // every lane is done with the partial slots in this region
+        for (int e = lane; e < 32 * (COLS / 4); e += 32) {
+          const int r = e / (COLS / 4), c4 = e % (COLS / 4);
+          const bool in = row0 + r < p.M;
+          ppdev::cp_async16(park_x + r * XLD + 4 * c4, p.out + (size_t)(in ? row0 + r : row0) * p.ldo + ocol0 + 4 * c4,
+                            in ? 16 : 0);
+        }
+        ppdev::cp_async_commit();
+        ppdev::cp_async_wait<0>();
+        __syncwarp();  // lanes read rows that other lanes copied
+      }
 #pragma unroll
       for (int c = 0; c < CHUNKS; ++c) {
         float v[16];
@@ -602,7 +637,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const int r = 8 * it + rq;
           o[it] = *reinterpret_cast<const float4*>(stg + r * EPI_LD + 4 * cq);
           if (EPI == EPI_RESID && row0 + r < p.M)
-            x[it] = *reinterpret_cast<const float4*>(p.out + (size_t)(row0 + r) * p.ldo + ocol0 + 16 * c + 4 * cq);
+            x[it] = parked ? *reinterpret_cast<const float4*>(park_x + r * XLD + 16 * c + 4 * cq)
+                           : *reinterpret_cast<const float4*>(p.out + (size_t)(row0 + r) * p.ldo + ocol0 + 16 * c + 4 * cq);
         }
         __syncwarp();  // the slice is free for the next chunk
 #pragma unroll
@@ -637,7 +673,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (et < BN) wsb[et] = ws_r;
       asm volatile("bar.sync 2, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
       const bool whole = kb0 == 0 && kb1 == nkb;
-      if (whole || finish_partial(t)) epilogue(row - lane, (t / p.num_m_tiles) * BN + colq * COLS, wsb + colq * COLS, as_r);
+      const bool parked = u == sc.units() - 1;  // every MMA of the cluster is done: the stages are free
+      if (whole || finish_partial(t, parked))
+        epilogue(row - lane, (t / p.num_m_tiles) * BN + colq * COLS, wsb + colq * COLS, as_r, parked);
     }
   }
 
