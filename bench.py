@@ -505,8 +505,9 @@ def run_streamed(args, cfg, world, rank, local, pg):
 # ----------------------------------------------------------------------------- one kernel
 def run_op(args):
     """Time one kernel alone at a given shape (for ncu captures and per-kernel
-    rooflines): --op gemm --engine 1|2 --m --n --k, or --op attention --m
-    (query rows) --start (start position) on the 8B head layout."""
+    rooflines): --op gemm --engine 1|2 --m --n --k, --op attention --m
+    (query rows) --start (start position) on the 8B head layout, or
+    --op quant | norm_quant --m (rows) --k (row length)."""
     import torch
 
     import prompt_prefill_gb300 as pp
@@ -539,6 +540,22 @@ def run_op(args):
             pp.pp_op_attention(q, kc, vc, m, start, H, Hkv, hd, o)
         pairs = sum(start + i + 1 for i in range(m))
         work, unit, bound = 4.0 * hd * H * pairs, "TFLOP/s", "alu"
+    elif args.op in ("quant", "norm_quant"):
+        # per-token quantiser (and RMSNorm before it) over m rows of k; writes int8 and fp16 codes
+        x = torch.randn((m, k), device="cuda")
+        g = 1.0 + 0.02 * torch.randn((k,), device="cuda")
+        q8 = torch.empty((m, k), dtype=torch.int8, device="cuda")
+        q16 = torch.empty((m, k), dtype=torch.float16, device="cuda")
+        asc = torch.empty((m,), device="cuda")
+        if args.op == "norm_quant":
+            def once():
+                pp.pp_op_rmsnorm_quantize(x, g, m, k, 1e-5, None, q8, q16, asc)
+        else:
+            def once():
+                pp.pp_op_quantize(x, m, k, q8, q16, asc)
+        # bytes the kernel must move: f32 rows in, int8 + fp16 codes and the row scale out (+ the gains)
+        work = m * (4 * k + k + 2 * k + 4) + (4 * k if args.op == "norm_quant" else 0)
+        unit, bound = "GB/s", "hbm"
     else:
         raise SystemExit(f"unknown --op {args.op}")
     for _ in range(args.warmup):
@@ -551,7 +568,7 @@ def run_op(args):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    achieved = work / (ms / 1000) / 1e12
+    achieved = work / (ms / 1000) / (1e9 if unit == "GB/s" else 1e12)
     peak, src = peak_for(bound, peaks)
     print(json.dumps({"op": args.op, "m": m, "n": n, "k": k, "start": args.start, "engine": args.engine,
                       "ms": ms, "achieved": achieved, "unit": unit, "peak": peak, "frac": achieved / peak,
@@ -572,7 +589,7 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention")
+    ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention | quant | norm_quant")
     ap.add_argument("--m", type=int, default=512)
     ap.add_argument("--n", type=int, default=28672)
     ap.add_argument("--k", type=int, default=4096)
