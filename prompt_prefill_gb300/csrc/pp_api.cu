@@ -436,7 +436,8 @@ int load_impl(pp_model* m, const pp_weights* w) {
   const size_t KMAX = std::max(std::max(D, QD), F);
   // residual stream: max_chunk rows chunk-outer, every position of a call layer-outer
   PP_TRY(dalloc(m, &m->x, (c.loop_order == PP_LOOP_LAYER_OUTER ? std::max(MC, (size_t)c.max_seq) : MC) * D));
-  PP_TRY(dalloc(m, &m->qkv, MC * QKV));
+  // QKV rows staged for the RoPE kernel (the tcgen05 path rotates in its QKV epilogue instead)
+  if (m->engine != PP_GEMM_TC) PP_TRY(dalloc(m, &m->qkv, MC * QKV));
   PP_TRY(dalloc(m, &m->qr, MC * QD));
   PP_TRY(dalloc(m, &m->o, MC * QD));
   {
