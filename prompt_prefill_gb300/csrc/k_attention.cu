@@ -92,8 +92,32 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const int kb_end = min(pmax, (r + 1) * kAttnRange - 1) / KB + 1;
   const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
 
-  // Query tile (row rr = position-in-tile * G + head-in-group).
   constexpr int C4 = HD / 4;
+  // K/V tiles stream through shared memory with cp.async: K of block kb+1
+  // loads while softmax and P V of block kb run, V of block kb+1 while S of
+  // block kb+1 runs. Two CTA barriers per block: before each, every thread
+  // waits for its own copies in flight (V of the block before the first, K of
+  // the next block before the second), so each barrier both frees a buffer
+  // and publishes the copy that lands in the other. P is private to a warp
+  // (a thread reads only the rows of its own ty), so it needs only __syncwarp.
+  // Keys past the tile's last position are zero-filled.
+  auto load_tile = [&](float* dst, const float* src, int key0, bool swizzle) {
+    for (int e = tid; e < KB * C4; e += THREADS) {
+      const int j = e / C4, c = e % C4;
+      const int kp = key0 + j;
+      const bool ok = kp <= pmax;
+      const float* g = src + ((size_t)(ok ? kp : 0) * Hkv + kvh) * HD + 4 * c;
+      float* d = swizzle ? &dst[swz<HD>(j, 4 * c)] : &dst[j * HD + 4 * c];
+      ppdev::cp_async16(d, g, ok ? 16 : 0);
+    }
+    ppdev::cp_async_commit();
+  };
+  load_tile(Ks, kc, kb_begin * KB, true);
+  load_tile(Vs, vc, kb_begin * KB, false);
+
+  // Query tile (issued after the first K/V copies, so the latencies overlap;
+  // row rr = position-in-tile * G + head-in-group).
+#pragma unroll 8
   for (int e = tid; e < ROWS * C4; e += THREADS) {
     const int rr = e / C4, c = e % C4;
     int i = i0 + rr / G;
@@ -127,27 +151,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       for (int e = 0; e < 4; ++e) O[a][i][e] = 0.f;
   }
 
-  // K/V tiles stream through shared memory with cp.async: K of block kb+1
-  // loads while softmax and P V of block kb run, V of block kb+1 while S of
-  // block kb+1 runs. Two CTA barriers per block: before each, every thread
-  // waits for its own copies in flight (V of the block before the first, K of
-  // the next block before the second), so each barrier both frees a buffer
-  // and publishes the copy that lands in the other. P is private to a warp
-  // (a thread reads only the rows of its own ty), so it needs only __syncwarp.
-  // Keys past the tile's last position are zero-filled.
-  auto load_tile = [&](float* dst, const float* src, int key0, bool swizzle) {
-    for (int e = tid; e < KB * C4; e += THREADS) {
-      const int j = e / C4, c = e % C4;
-      const int kp = key0 + j;
-      const bool ok = kp <= pmax;
-      const float* g = src + ((size_t)(ok ? kp : 0) * Hkv + kvh) * HD + 4 * c;
-      float* d = swizzle ? &dst[swz<HD>(j, 4 * c)] : &dst[j * HD + 4 * c];
-      ppdev::cp_async16(d, g, ok ? 16 : 0);
-    }
-    ppdev::cp_async_commit();
-  };
-  load_tile(Ks, kc, kb_begin * KB, true);
-  load_tile(Vs, vc, kb_begin * KB, false);
   ppdev::cp_async_wait<1>();  // K of the first block (V may still be in flight)
   __syncthreads();
 
