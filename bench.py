@@ -42,8 +42,8 @@ FP32_LANES = 128
 KERNEL_TRAFFIC = {
     # k_attention, mean over the 8 launches of one layer (chunk starts 0, 512, ..., 3584); the range merge
     # kernel's own bytes are listed in its profile summary
-    "attention": {"bytes_per_launch": 33111904.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
-                  "sha256": "1e155502dc2c759ef4d16023bb51f0bcd25131bdb98551d0241089dff6988c74"},
+    "attention": {"bytes_per_launch": 33144640.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
+                  "sha256": "285b18a54d6527342a8f11c64e00a366a2391d47a8505c52fe1409c8fe33f0d1"},
 }
 
 
