@@ -202,6 +202,19 @@ int pp_reset_stats(pp_model* m);
  * and summed duration appear in pp_stats (prof_launches, prof_ms). */
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
+/* Chunk overlap (1 on, 0 off; off after pp_model_load), resident weights and
+ * chunk-outer order only ("Batched Prefill": chunks in order, each swept
+ * through every layer). Consecutive chunks of a call alternate between two
+ * streams, each with its own scratch set; a chunk waits, layer by layer, only
+ * for the previous chunk's K/V rows of that layer before its attention reads
+ * them, so one chunk's kernels can use the SMs another chunk's leave idle.
+ * Results are bit-identical to the serial order. The first call that turns it
+ * on allocates the second scratch set and stream (PP_ERR_OOM if that fails)
+ * after waiting for the model's work. Ignored while a trace or the per-layer
+ * profile is on, and for calls of a single chunk. PP_ERR_UNSUPPORTED for a
+ * streamed-mode model. */
+int pp_set_chunk_overlap(pp_model* m, int32_t enable);
+
 /* Per-layer stage profile ("Single-pass prefill", the per-layer profiler of
  * I/O and compute; "Predictive prefetch", the sync vs async loader A/B),
  * summed over every visit of the layer (one per chunk chunk-outer, one per

@@ -83,6 +83,7 @@ SIGNATURES = {
     "pp_model_gemm_engine": ([_vp], ctypes.c_int),
     "pp_set_profile_kernel": ([_vp, _i32], ctypes.c_int),
     "pp_set_layer_profile": ([_vp, _i32], ctypes.c_int),
+    "pp_set_chunk_overlap": ([_vp, _i32], ctypes.c_int),
     "pp_get_layer_profile": ([_vp, ctypes.POINTER(pp_layer_profile), _i32], ctypes.c_int),
     "pp_set_trace": ([_vp, _vp, _vp, _vp, _i32], ctypes.c_int),
     "pp_status_str": ([ctypes.c_int], ctypes.c_char_p),
@@ -253,6 +254,10 @@ def pp_set_layer_profile(h: int, enable: bool):
     _check(lib().pp_set_layer_profile(h, 1 if enable else 0), "pp_set_layer_profile")
 
 
+def pp_set_chunk_overlap(h: int, enable: bool):
+    _check(lib().pp_set_chunk_overlap(h, 1 if enable else 0), "pp_set_chunk_overlap")
+
+
 def pp_get_layer_profile(h: int, n_layers: int) -> list:
     arr = (pp_layer_profile * n_layers)()
     _check(lib().pp_get_layer_profile(h, arr, n_layers), "pp_get_layer_profile")
@@ -399,6 +404,9 @@ class PrefillModel:
 
     def set_layer_profile(self, enable=True):
         pp_set_layer_profile(self.h, enable)
+
+    def set_chunk_overlap(self, enable=True):
+        pp_set_chunk_overlap(self.h, enable)
 
     def layer_profile(self):
         return pp_get_layer_profile(self.h, self.cfg.n_layers)

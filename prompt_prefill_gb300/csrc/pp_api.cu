@@ -196,6 +196,24 @@ struct pp_model {
   TcWorkspace tcws;  // stream-K partial tiles and counters of the projection GEMMs
   float* attn_part = nullptr;  // per-key-range partial attention state of one chunk
   size_t attn_part_bytes = 0;
+  // chunk overlap (pp_set_chunk_overlap): consecutive chunks alternate between the
+  // compute stream and stream2, each with its own scratch set (the fields above
+  // hold the active one, `alt` the other); chunk k waits for chunk k-1's K/V rows
+  // of a layer (qkv_ev) before its attention at that layer
+  struct Scratch {
+    float *x, *qkv, *qr, *o, *h, *as;
+    int8_t* a8;
+    __half* a16;
+    TcWorkspace tcws;
+    float* attn_part;
+    size_t attn_part_bytes;
+    CUtensorMap amap_d, amap_qd, amap_f;
+  };
+  bool overlap = false;
+  bool alt_ready = false;
+  Scratch alt{};
+  cudaStream_t stream2 = nullptr;
+  std::vector<cudaEvent_t> qkv_ev[2];
   // stats and timing
   pp_stats stats{};
   std::vector<cudaEvent_t> ev_pool;
@@ -376,6 +394,77 @@ int validate_cfg(const pp_config* c) {
   return PP_OK;
 }
 
+// One scratch set (residual rows, activations, codes, attention and stream-K
+// workspaces, the activation tensor maps) into the model's scratch fields.
+int alloc_scratch(pp_model* m) {
+  const pp_config& c = m->cfg;
+  const size_t D = c.dim, QD = (size_t)c.n_heads * c.head_dim,
+               QKV = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn, MC = c.max_chunk;
+  const size_t KMAX = std::max(std::max(D, QD), F);
+  // residual stream: max_chunk rows chunk-outer, every position of a call layer-outer
+  PP_TRY(dalloc(m, &m->x, (c.loop_order == PP_LOOP_LAYER_OUTER ? std::max(MC, (size_t)c.max_seq) : MC) * D));
+  // QKV rows staged for the RoPE kernel (the tcgen05 path rotates in its QKV epilogue instead)
+  if (m->engine != PP_GEMM_TC) PP_TRY(dalloc(m, &m->qkv, MC * QKV));
+  PP_TRY(dalloc(m, &m->qr, MC * QD));
+  PP_TRY(dalloc(m, &m->o, MC * QD));
+  {
+    // largest chunk at the end of the cache: the most tiles times the most key ranges
+    const int rows = (int)std::min<size_t>(MC, (size_t)c.max_seq);
+    m->attn_part_bytes = attention_workspace_bytes(rows, c.max_seq - rows, c.n_heads, c.n_kv_heads, c.head_dim);
+    if (m->attn_part_bytes) PP_TRY(dalloc(m, &m->attn_part, m->attn_part_bytes / sizeof(float)));
+  }
+  PP_TRY(dalloc(m, &m->h, MC * F));
+  PP_TRY(dalloc(m, &m->a8, MC * KMAX));
+  PP_TRY(dalloc(m, &m->a16, MC * KMAX));
+  PP_TRY(dalloc(m, &m->as, MC));
+  PP_CUDA(cudaMemsetAsync(m->a16, 0, MC * KMAX * sizeof(__half), m->stream));
+  if (m->engine == PP_GEMM_TC) {
+    // stream-K workspace: the largest need over every chunk-row count and projection
+    size_t part = 0, cnt = 0;
+    const int shapes[4][2] = {{(int)QKV, (int)D}, {(int)D, (int)QD}, {(int)(2 * F), (int)D}, {(int)D, (int)F}};
+    for (size_t rows = 256; rows < MC + 256; rows += 256)
+      for (auto& sh : shapes) {
+        size_t pb = 0, cc = 0;
+        tc_workspace_need((int)std::min(rows, MC), sh[0], sh[1], &pb, &cc);
+        part = std::max(part, pb);
+        cnt = std::max(cnt, cc);
+      }
+    if (part) {
+      PP_TRY(dalloc(m, &m->tcws.part, part / sizeof(int32_t)));
+      PP_TRY(dalloc(m, &m->tcws.cnt, cnt));
+      PP_CUDA(cudaMemsetAsync(m->tcws.cnt, 0, cnt * sizeof(int), m->stream));
+      m->tcws.part_bytes = part;
+      m->tcws.counters = cnt;
+    }
+    PP_CUDA(make_tmap_a(&m->amap_d, m->a16, (int)MC, (int)D));
+    PP_CUDA(make_tmap_a(&m->amap_qd, m->a16, (int)MC, (int)QD));
+    PP_CUDA(make_tmap_a(&m->amap_f, m->a16, (int)MC, (int)F));
+  }
+  return PP_OK;
+}
+
+// Exchange the active scratch set (the model's fields) with the other one.
+void swap_scratch(pp_model* m) {
+  pp_model::Scratch cur{m->x, m->qkv, m->qr, m->o, m->h, m->as, m->a8, m->a16, m->tcws, m->attn_part,
+                        m->attn_part_bytes, m->amap_d, m->amap_qd, m->amap_f};
+  const pp_model::Scratch& o = m->alt;
+  m->x = o.x;
+  m->qkv = o.qkv;
+  m->qr = o.qr;
+  m->o = o.o;
+  m->h = o.h;
+  m->as = o.as;
+  m->a8 = o.a8;
+  m->a16 = o.a16;
+  m->tcws = o.tcws;
+  m->attn_part = o.attn_part;
+  m->attn_part_bytes = o.attn_part_bytes;
+  m->amap_d = o.amap_d;
+  m->amap_qd = o.amap_qd;
+  m->amap_f = o.amap_f;
+  m->alt = cur;
+}
+
 int load_impl(pp_model* m, const pp_weights* w) {
   const pp_config& c = m->cfg;
   PP_CUDA(cudaGetDevice(&m->device));
@@ -433,50 +522,11 @@ int load_impl(pp_model* m, const pp_weights* w) {
   PP_CUDA(launch_rope_table(c.max_seq, c.head_dim, c.rope_theta, m->rope, m->stream));
 
   // scratch
-  const size_t KMAX = std::max(std::max(D, QD), F);
-  // residual stream: max_chunk rows chunk-outer, every position of a call layer-outer
-  PP_TRY(dalloc(m, &m->x, (c.loop_order == PP_LOOP_LAYER_OUTER ? std::max(MC, (size_t)c.max_seq) : MC) * D));
-  // QKV rows staged for the RoPE kernel (the tcgen05 path rotates in its QKV epilogue instead)
-  if (m->engine != PP_GEMM_TC) PP_TRY(dalloc(m, &m->qkv, MC * QKV));
-  PP_TRY(dalloc(m, &m->qr, MC * QD));
-  PP_TRY(dalloc(m, &m->o, MC * QD));
-  {
-    // largest chunk at the end of the cache: the most tiles times the most key ranges
-    const int rows = (int)std::min<size_t>(MC, (size_t)c.max_seq);
-    m->attn_part_bytes = attention_workspace_bytes(rows, c.max_seq - rows, c.n_heads, c.n_kv_heads, c.head_dim);
-    if (m->attn_part_bytes) PP_TRY(dalloc(m, &m->attn_part, m->attn_part_bytes / sizeof(float)));
-  }
-  PP_TRY(dalloc(m, &m->h, MC * F));
-  PP_TRY(dalloc(m, &m->a8, MC * KMAX));
-  PP_TRY(dalloc(m, &m->a16, MC * KMAX));
-  PP_TRY(dalloc(m, &m->as, MC));
+  PP_TRY(alloc_scratch(m));
   PP_TRY(dalloc(m, &m->logits, V));
   PP_TRY(dalloc(m, &m->tok, (size_t)c.max_seq));
   PP_TRY(dalloc(m, &m->status, 1));
   PP_CUDA(cudaMemsetAsync(m->status, 0, sizeof(int), m->stream));
-  PP_CUDA(cudaMemsetAsync(m->a16, 0, MC * KMAX * sizeof(__half), m->stream));
-  if (m->engine == PP_GEMM_TC) {
-    // stream-K workspace: the largest need over every chunk-row count and projection
-    size_t part = 0, cnt = 0;
-    const int shapes[4][2] = {{(int)QKV, (int)D}, {(int)D, (int)QD}, {(int)(2 * F), (int)D}, {(int)D, (int)F}};
-    for (size_t rows = 256; rows < MC + 256; rows += 256)
-      for (auto& sh : shapes) {
-        size_t pb = 0, cc = 0;
-        tc_workspace_need((int)std::min(rows, MC), sh[0], sh[1], &pb, &cc);
-        part = std::max(part, pb);
-        cnt = std::max(cnt, cc);
-      }
-    if (part) {
-      PP_TRY(dalloc(m, &m->tcws.part, part / sizeof(int32_t)));
-      PP_TRY(dalloc(m, &m->tcws.cnt, cnt));
-      PP_CUDA(cudaMemsetAsync(m->tcws.cnt, 0, cnt * sizeof(int), m->stream));
-      m->tcws.part_bytes = part;
-      m->tcws.counters = cnt;
-    }
-    PP_CUDA(make_tmap_a(&m->amap_d, m->a16, (int)MC, (int)D));
-    PP_CUDA(make_tmap_a(&m->amap_qd, m->a16, (int)MC, (int)QD));
-    PP_CUDA(make_tmap_a(&m->amap_f, m->a16, (int)MC, (int)F));
-  }
 
   // layers
   const size_t stride = m->lay.bytes;
@@ -538,6 +588,9 @@ void free_impl(pp_model* m) {
     if (m->ring_ready[s]) cudaEventDestroy(m->ring_ready[s]);
     if (m->ring_free[s]) cudaEventDestroy(m->ring_free[s]);
   }
+  for (int p = 0; p < 2; ++p)
+    for (auto e : m->qkv_ev[p]) cudaEventDestroy(e);
+  if (m->stream2) cudaStreamDestroy(m->stream2);
   for (void* p : m->allocations) cudaFree(p);
   if (m->kvs.base) kv_space_free(&m->kvs);
   if (m->h_layers) cudaFreeHost(m->h_layers);
@@ -619,7 +672,11 @@ int trace_codes(pp_model* m, cudaStream_t cs, int layer, int point, int pos0, in
 
 // One layer over the C rows of a chunk at positions pos0.. (residual rows x):
 // attention block then FFN block, every projection an int8 GEMM over the chunk.
-int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base, float* x, int C, int pos0) {
+// kv_done: recorded once this chunk's K/V rows of the layer are written;
+// kv_wait: the previous chunk's K/V rows of the layer (chunk overlap), waited
+// for before the attention reads them.
+int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base, float* x, int C, int pos0,
+                cudaEvent_t kv_done = nullptr, cudaEvent_t kv_wait = nullptr) {
   const pp_config& c = m->cfg;
   const int D = c.dim, H = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim, F = c.ffn;
   const int QD = H * hd, QKV = (H + 2 * Hkv) * hd;
@@ -657,6 +714,8 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
       return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs, true);
     }));
   }
+  if (kv_done) PP_CUDA(cudaEventRecord(kv_done, cs));
+  if (kv_wait) PP_CUDA(cudaStreamWaitEvent(cs, kv_wait, 0));
   PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
     return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
   }));
@@ -766,7 +825,45 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     m->lprof_pending.push_back(e);
     return PP_OK;
   };
-  if (!layer_outer) {
+  const bool overlap = m->overlap && !streamed && !layer_outer && !m->trace && !m->layer_prof && n > chunk;
+  if (overlap) {
+    // "Batched Prefill" with consecutive chunks on two streams: chunk k runs on
+    // stream k % 2 with scratch set k % 2 and waits, layer by layer, only for
+    // chunk k-1's K/V rows before its attention (a chunk's other inputs are its
+    // own), so chunk k's layer l can fill the SMs that chunk k-1 leaves idle
+    // between its kernels. Chunk k-2 ran on the same stream: its scratch and its
+    // K/V rows are complete in stream order.
+    cudaStream_t S[2] = {cs, m->stream2};
+    cudaEvent_t e;
+    PP_TRY(ev_get(m, &e));
+    PP_CUDA(cudaEventRecord(e, cs));
+    PP_CUDA(cudaStreamWaitEvent(m->stream2, e, 0));
+    m->ev_pool.push_back(e);
+    int active = 0, rc = PP_OK, k = 0;
+    for (int c0 = 0; c0 < n && rc == PP_OK; c0 += chunk, ++k) {
+      const int p = k & 1;
+      if (p != active) {
+        swap_scratch(m);
+        active = p;
+      }
+      cudaStream_t sk = S[p];
+      const int C = std::min(chunk, n - c0);
+      const int pos0 = start_pos + c0;
+      rc = launch(m, PP_KERNEL_EMBED, sk, [&] {
+        return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, sk);
+      });
+      for (int l = 0; l < c.n_layers && rc == PP_OK; ++l)
+        rc = layer_block(m, sk, l, l, m->d_layers + m->lay.bytes * l, m->x, C, pos0, m->qkv_ev[p][l],
+                         k > 0 ? m->qkv_ev[1 - p][l] : nullptr);
+      if (rc == PP_OK && c0 + C == n) rc = head(m, sk, m->x + (size_t)(C - 1) * D, d_logits);
+    }
+    if (active != 0) swap_scratch(m);  // set 0 is the model's between calls
+    PP_TRY(rc);
+    PP_TRY(ev_get(m, &e));  // the call ends on the caller's stream
+    PP_CUDA(cudaEventRecord(e, m->stream2));
+    PP_CUDA(cudaStreamWaitEvent(cs, e, 0));
+    m->ev_pool.push_back(e);
+  } else if (!layer_outer) {
     // "Batched Prefill": for each chunk, every layer over the chunk's rows
     int visit = 0;
     for (int c0 = 0; c0 < n; c0 += chunk) {
@@ -975,6 +1072,35 @@ int pp_reset_stats(pp_model* m) {
   PP_TRY(collect(m));
   m->stats = pp_stats{};
   m->lprof.assign(m->cfg.n_layers, pp_layer_profile{});
+  return PP_OK;
+}
+
+int pp_set_chunk_overlap(pp_model* m, int32_t enable) {
+  if (!m || (enable != 0 && enable != 1)) {
+    set_err("bad pp_set_chunk_overlap arguments");
+    return PP_ERR_ARG;
+  }
+  if (enable && m->cfg.mode == PP_MODE_STREAMED) {
+    set_err("chunk overlap needs resident weights");
+    return PP_ERR_UNSUPPORTED;
+  }
+  if (enable && !m->alt_ready) {
+    PP_TRY(sync_model(m));
+    swap_scratch(m);  // the fields take the second set while it is allocated
+    const int rc = alloc_scratch(m);
+    swap_scratch(m);
+    if (rc != PP_OK) return rc;  // what was allocated is released with the model
+    PP_CUDA(cudaStreamCreateWithFlags(&m->stream2, cudaStreamNonBlocking));
+    for (int p = 0; p < 2; ++p)
+      for (int l = 0; l < m->cfg.n_layers; ++l) {
+        cudaEvent_t e;
+        PP_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        m->qkv_ev[p].push_back(e);
+      }
+    PP_CUDA(cudaStreamSynchronize(m->stream));  // the new set's initial clears
+    m->alt_ready = true;
+  }
+  m->overlap = enable != 0;
   return PP_OK;
 }
 

@@ -286,3 +286,26 @@ def test_head_dim_128_fused_rope_engines_and_oracle():
         assert np.array_equal(bits(a), bits(b))
     print("hd128 per-layer (tie decisions, max margin):", _summary(report))
     _assert_e2e(got, ref, "hd128 final")
+
+
+def test_1b_chunk_overlap_bit_identical(one_b):
+    # Chunks alternating between two streams (each waits only for the previous chunk's K/V rows of a
+    # layer) give the serial path's bits: logits, K/V rows, ragged chunks and a continuation call.
+    m, g = one_b
+    toks = synth.prompt(m.cfg)  # 2048 tokens
+    g.kv_reset()
+    ref = g.prefill(toks, 0, 256)
+    kv_ref = [g.kv(L, which, 0, len(toks)) for L in (0, m.cfg.n_layers - 1) for which in (0, 1)]
+    g.set_chunk_overlap(True)
+    try:
+        for chunk in (256, 512, 100):
+            g.kv_reset()
+            assert np.array_equal(bits(g.prefill(toks, 0, chunk)), bits(ref)), chunk
+        kv = [g.kv(L, which, 0, len(toks)) for L in (0, m.cfg.n_layers - 1) for which in (0, 1)]
+        for a, b in zip(kv, kv_ref):
+            assert np.array_equal(bits(a), bits(b))
+        g.kv_reset()
+        g.prefill(toks[:1000], 0, 256)
+        assert np.array_equal(bits(g.prefill(toks[1000:], 1000, 256)), bits(ref))
+    finally:
+        g.set_chunk_overlap(False)
