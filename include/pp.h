@@ -204,12 +204,12 @@ int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
 /* Chunk overlap (1 on, 0 off; off after pp_model_load), resident weights and
  * chunk-outer order only ("Batched Prefill": chunks in order, each swept
- * through every layer). Consecutive chunks of a call alternate between two
- * streams, each with its own scratch set; a chunk waits, layer by layer, only
- * for the previous chunk's K/V rows of that layer before its attention reads
- * them, so one chunk's kernels can use the SMs another chunk's leave idle.
- * Results are bit-identical to the serial order. The first call that turns it
- * on allocates the second scratch set and stream (PP_ERR_OOM if that fails)
+ * through every layer). Consecutive chunks of a call rotate over four streams,
+ * each with its own scratch set; a chunk waits, layer by layer, only for the
+ * previous chunk's K/V rows of that layer before its attention reads them, so
+ * one chunk's kernels can use the SMs the others leave idle. Results are
+ * bit-identical to the serial order. The first call that turns it on
+ * allocates three more scratch sets and streams (PP_ERR_OOM if that fails)
  * after waiting for the model's work. Ignored while a trace or the per-layer
  * profile is on, and for calls of a single chunk. PP_ERR_UNSUPPORTED for a
  * streamed-mode model. */

@@ -196,10 +196,11 @@ struct pp_model {
   TcWorkspace tcws;  // stream-K partial tiles and counters of the projection GEMMs
   float* attn_part = nullptr;  // per-key-range partial attention state of one chunk
   size_t attn_part_bytes = 0;
-  // chunk overlap (pp_set_chunk_overlap): consecutive chunks alternate between the
-  // compute stream and stream2, each with its own scratch set (the fields above
-  // hold the active one, `alt` the other); chunk k waits for chunk k-1's K/V rows
-  // of a layer (qkv_ev) before its attention at that layer
+  // chunk overlap (pp_set_chunk_overlap): consecutive chunks rotate over
+  // kOverlap streams (the compute stream and ostream[]), each with its own
+  // scratch set (the fields above hold the active one, sets[] all of them);
+  // chunk k waits for chunk k-1's K/V rows of a layer (qkv_ev) before its
+  // attention at that layer
   struct Scratch {
     float *x, *qkv, *qr, *o, *h, *as;
     int8_t* a8;
@@ -209,11 +210,13 @@ struct pp_model {
     size_t attn_part_bytes;
     CUtensorMap amap_d, amap_qd, amap_f;
   };
+  static constexpr int kOverlap = 4;
   bool overlap = false;
-  bool alt_ready = false;
-  Scratch alt{};
-  cudaStream_t stream2 = nullptr;
-  std::vector<cudaEvent_t> qkv_ev[2];
+  bool sets_ready = false;
+  int active_set = 0;
+  Scratch sets[kOverlap]{};
+  cudaStream_t ostream[kOverlap - 1] = {};
+  std::vector<cudaEvent_t> qkv_ev[kOverlap];
   // stats and timing
   pp_stats stats{};
   std::vector<cudaEvent_t> ev_pool;
@@ -443,11 +446,12 @@ int alloc_scratch(pp_model* m) {
   return PP_OK;
 }
 
-// Exchange the active scratch set (the model's fields) with the other one.
-void swap_scratch(pp_model* m) {
-  pp_model::Scratch cur{m->x, m->qkv, m->qr, m->o, m->h, m->as, m->a8, m->a16, m->tcws, m->attn_part,
-                        m->attn_part_bytes, m->amap_d, m->amap_qd, m->amap_f};
-  const pp_model::Scratch& o = m->alt;
+// Make scratch set j the model's fields (the active set's pointers are kept in sets[]).
+void use_scratch(pp_model* m, int j) {
+  if (j == m->active_set) return;
+  m->sets[m->active_set] = pp_model::Scratch{m->x, m->qkv, m->qr, m->o, m->h, m->as, m->a8, m->a16, m->tcws,
+                                             m->attn_part, m->attn_part_bytes, m->amap_d, m->amap_qd, m->amap_f};
+  const pp_model::Scratch& o = m->sets[j];
   m->x = o.x;
   m->qkv = o.qkv;
   m->qr = o.qr;
@@ -462,7 +466,7 @@ void swap_scratch(pp_model* m) {
   m->amap_d = o.amap_d;
   m->amap_qd = o.amap_qd;
   m->amap_f = o.amap_f;
-  m->alt = cur;
+  m->active_set = j;
 }
 
 int load_impl(pp_model* m, const pp_weights* w) {
@@ -588,9 +592,10 @@ void free_impl(pp_model* m) {
     if (m->ring_ready[s]) cudaEventDestroy(m->ring_ready[s]);
     if (m->ring_free[s]) cudaEventDestroy(m->ring_free[s]);
   }
-  for (int p = 0; p < 2; ++p)
+  for (int p = 0; p < pp_model::kOverlap; ++p)
     for (auto e : m->qkv_ev[p]) cudaEventDestroy(e);
-  if (m->stream2) cudaStreamDestroy(m->stream2);
+  for (auto s : m->ostream)
+    if (s) cudaStreamDestroy(s);
   for (void* p : m->allocations) cudaFree(p);
   if (m->kvs.base) kv_space_free(&m->kvs);
   if (m->h_layers) cudaFreeHost(m->h_layers);
@@ -833,19 +838,21 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     // own), so chunk k's layer l can fill the SMs that chunk k-1 leaves idle
     // between its kernels. Chunk k-2 ran on the same stream: its scratch and its
     // K/V rows are complete in stream order.
-    cudaStream_t S[2] = {cs, m->stream2};
+    constexpr int NS = pp_model::kOverlap;
+    cudaStream_t S[NS];
+    S[0] = cs;
     cudaEvent_t e;
     PP_TRY(ev_get(m, &e));
     PP_CUDA(cudaEventRecord(e, cs));
-    PP_CUDA(cudaStreamWaitEvent(m->stream2, e, 0));
+    for (int i = 1; i < NS; ++i) {
+      S[i] = m->ostream[i - 1];
+      PP_CUDA(cudaStreamWaitEvent(S[i], e, 0));
+    }
     m->ev_pool.push_back(e);
-    int active = 0, rc = PP_OK, k = 0;
+    int rc = PP_OK, k = 0;
     for (int c0 = 0; c0 < n && rc == PP_OK; c0 += chunk, ++k) {
-      const int p = k & 1;
-      if (p != active) {
-        swap_scratch(m);
-        active = p;
-      }
+      const int p = k % NS, prev = (k + NS - 1) % NS;
+      use_scratch(m, p);
       cudaStream_t sk = S[p];
       const int C = std::min(chunk, n - c0);
       const int pos0 = start_pos + c0;
@@ -854,15 +861,17 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       });
       for (int l = 0; l < c.n_layers && rc == PP_OK; ++l)
         rc = layer_block(m, sk, l, l, m->d_layers + m->lay.bytes * l, m->x, C, pos0, m->qkv_ev[p][l],
-                         k > 0 ? m->qkv_ev[1 - p][l] : nullptr);
+                         k > 0 ? m->qkv_ev[prev][l] : nullptr);
       if (rc == PP_OK && c0 + C == n) rc = head(m, sk, m->x + (size_t)(C - 1) * D, d_logits);
     }
-    if (active != 0) swap_scratch(m);  // set 0 is the model's between calls
+    use_scratch(m, 0);  // set 0 is the model's between calls
     PP_TRY(rc);
-    PP_TRY(ev_get(m, &e));  // the call ends on the caller's stream
-    PP_CUDA(cudaEventRecord(e, m->stream2));
-    PP_CUDA(cudaStreamWaitEvent(cs, e, 0));
-    m->ev_pool.push_back(e);
+    for (int i = 1; i < NS; ++i) {  // the call ends on the caller's stream
+      PP_TRY(ev_get(m, &e));
+      PP_CUDA(cudaEventRecord(e, S[i]));
+      PP_CUDA(cudaStreamWaitEvent(cs, e, 0));
+      m->ev_pool.push_back(e);
+    }
   } else if (!layer_outer) {
     // "Batched Prefill": for each chunk, every layer over the chunk's rows
     int visit = 0;
@@ -1084,21 +1093,23 @@ int pp_set_chunk_overlap(pp_model* m, int32_t enable) {
     set_err("chunk overlap needs resident weights");
     return PP_ERR_UNSUPPORTED;
   }
-  if (enable && !m->alt_ready) {
+  if (enable && !m->sets_ready) {
     PP_TRY(sync_model(m));
-    swap_scratch(m);  // the fields take the second set while it is allocated
-    const int rc = alloc_scratch(m);
-    swap_scratch(m);
-    if (rc != PP_OK) return rc;  // what was allocated is released with the model
-    PP_CUDA(cudaStreamCreateWithFlags(&m->stream2, cudaStreamNonBlocking));
-    for (int p = 0; p < 2; ++p)
+    for (int j = 1; j < pp_model::kOverlap; ++j) {
+      use_scratch(m, j);  // empty fields: the set is allocated into them
+      const int rc = alloc_scratch(m);
+      use_scratch(m, 0);
+      if (rc != PP_OK) return rc;  // what was allocated is released with the model
+      PP_CUDA(cudaStreamCreateWithFlags(&m->ostream[j - 1], cudaStreamNonBlocking));
+    }
+    for (int p = 0; p < pp_model::kOverlap; ++p)
       for (int l = 0; l < m->cfg.n_layers; ++l) {
         cudaEvent_t e;
         PP_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
         m->qkv_ev[p].push_back(e);
       }
-    PP_CUDA(cudaStreamSynchronize(m->stream));  // the new set's initial clears
-    m->alt_ready = true;
+    PP_CUDA(cudaStreamSynchronize(m->stream));  // the new sets' initial clears
+    m->sets_ready = true;
   }
   m->overlap = enable != 0;
   return PP_OK;
