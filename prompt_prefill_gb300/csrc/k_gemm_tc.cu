@@ -785,10 +785,16 @@ cudaError_t make_tmap_w(CUtensorMap* map, const int8_t* w, int n, int k, int bn)
 // tile runs at the tensor core's rate while a 128-row tile reaches ~68% of it.
 // Otherwise the width whose waves of tiles over the pairs cost the fewest
 // weight columns per pair (ceil(tiles / pairs) x width); ties go to the wider
-// tile.
-int tc_bn(int m, int n, int k) {
+// tile. `wide` (other streams fill the pairs a launch leaves idle): the widest
+// tile that divides n and no stream-K, the least SM time per GEMM.
+int tc_bn(int m, int n, int k, bool wide) {
   const int mc = max_clusters();
   const int nmt = (m + 2 * BM - 1) / (2 * BM);
+  if (wide) {
+    for (int bn : {256, 192, 128})
+      if (n % bn == 0) return bn;
+    return 0;
+  }
   if (n % 256 == 0) {
     const long long tiles = (long long)nmt * (n / 256), total = tiles * (k / BK);
     if (tiles < 2 * mc && total >= 2 * mc && (total + mc - 1) / mc >= MIN_SK_KB) return 256;
@@ -815,15 +821,15 @@ struct Plan {
   size_t part_elems;
 };
 
-Plan plan(int m, int n, int k) {
+Plan plan(int m, int n, int k, bool wide) {
   Plan pl{};
-  pl.bn = tc_bn(m, n, k);
+  pl.bn = tc_bn(m, n, k, wide);
   if (!pl.bn) return pl;
   const int nmt = (m + 2 * BM - 1) / (2 * BM);
   const int nkb = k / BK;
   pl.num_tiles = nmt * (n / pl.bn);
   const int mc = max_clusters();
-  if (pl.num_tiles >= 2 * mc || pl.num_tiles * nkb < 2 * mc) {
+  if (wide || pl.num_tiles >= 2 * mc || pl.num_tiles * nkb < 2 * mc) {
     pl.clusters = std::min(pl.num_tiles, mc);
     return pl;
   }
@@ -843,7 +849,7 @@ Plan plan(int m, int n, int k) {
 }  // namespace
 
 void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters) {
-  const Plan pl = plan(m, n, k);
+  const Plan pl = plan(m, n, k, false);
   *part_bytes = pl.part_elems * sizeof(int32_t);
   *counters = pl.ipc ? (size_t)pl.num_tiles * 2 : 0;
 }
@@ -851,7 +857,7 @@ void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
                            int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits,
-                           const TcRope& rope) {
+                           const TcRope& rope, bool wide) {
   TcParams p{};
   p.wait_cycles = waits.cycles;
   p.hold_mma = waits.hold_mma;
@@ -867,7 +873,7 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
   p.acc_out = acc;
   p.status = status;
   p.rope = rope;
-  Plan pl = plan(m, n, k);
+  Plan pl = plan(m, n, k, wide);
   if (!pl.bn || pl.bn != bn) return cudaErrorInvalidValue;  // the weight map was made for another tile width
   p.num_tiles = pl.num_tiles;
   if (pl.ipc && wsp.part && wsp.cnt && wsp.part_bytes >= pl.part_elems * sizeof(int32_t) &&

@@ -212,6 +212,7 @@ struct pp_model {
   };
   static constexpr int kOverlap = 4;
   bool overlap = false;
+  bool gemm_wide = false;  // the current call overlaps chunks: widest GEMM tiles, no stream-K
   bool sets_ready = false;
   int active_set = 0;
   Scratch sets[kOverlap]{};
@@ -328,12 +329,12 @@ int tc_segment() { return g_tc_seg.load(); }
 int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* ws, const int8_t* w, int M, int N,
          int K, float* out, int ldo, const TcRope& rope = TcRope{}) {
   if (m->engine == PP_GEMM_TC) {
-    const int bi = tc_bn_index(M, N, K);
+    const int bi = tc_bn_index(M, N, K, m->gemm_wide);
     const CUtensorMap& wm = m->wmap[((size_t)mg * 4 + which) * 3 + bi];
     const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
     return launch(m, PP_KERNEL_GEMM, st, [&] {
       return launch_gemm_tc(epi, am, wm, kTcBn[bi], ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
-                            st, TcWaits{}, rope);
+                            st, TcWaits{}, rope, m->gemm_wide);
     });
   }
   return launch(m, PP_KERNEL_GEMM, st, [&] {
@@ -850,6 +851,9 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     }
     m->ev_pool.push_back(e);
     int rc = PP_OK, k = 0;
+    // the other streams fill the CTA pairs a GEMM leaves idle: each GEMM takes the
+    // least SM time (widest tile, no stream-K) rather than the least latency
+    m->gemm_wide = true;
     for (int c0 = 0; c0 < n && rc == PP_OK; c0 += chunk, ++k) {
       const int p = k % NS, prev = (k + NS - 1) % NS;
       use_scratch(m, p);
@@ -865,6 +869,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       if (rc == PP_OK && c0 + C == n) rc = head(m, sk, m->x + (size_t)(C - 1) * D, d_logits);
     }
     use_scratch(m, 0);  // set 0 is the model's between calls
+    m->gemm_wide = false;
     PP_TRY(rc);
     for (int i = 1; i < NS; ++i) {  // the call ends on the caller's stream
       PP_TRY(ev_get(m, &e));

@@ -45,9 +45,11 @@ cudaError_t launch_gemm_mma(int epi, const int8_t* a8, const int8_t* w, const fl
 // is made for one tile width bn (256, 192 or 128): the one tc_bn(m, n, k) picks for the launch.
 bool tc_available();
 constexpr int kTcBn[3] = {256, 192, 128};
-int tc_bn(int m, int n, int k);
-inline int tc_bn_index(int m, int n, int k) {
-  const int bn = tc_bn(m, n, k);
+// wide: the widest width that divides n and no stream-K (for launches whose idle
+// CTA pairs other streams fill).
+int tc_bn(int m, int n, int k, bool wide = false);
+inline int tc_bn_index(int m, int n, int k, bool wide = false) {
+  const int bn = tc_bn(m, n, k, wide);
   return bn == 256 ? 0 : (bn == 192 ? 1 : 2);
 }
 cudaError_t make_tmap_a(CUtensorMap* map, const __half* a16, int rows, int k);
@@ -79,7 +81,7 @@ struct TcRope {
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
                            int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits = TcWaits{},
-                           const TcRope& rope = TcRope{});
+                           const TcRope& rope = TcRope{}, bool wide = false);
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)
