@@ -678,9 +678,11 @@ int trace_codes(pp_model* m, cudaStream_t cs, int layer, int point, int pos0, in
 
 // One layer over the C rows of a chunk at positions pos0.. (residual rows x):
 // attention block then FFN block, every projection an int8 GEMM over the chunk.
-// kv_done: recorded once this chunk's K/V rows of the layer are written;
-// kv_wait: the previous chunk's K/V rows of the layer (chunk overlap), waited
-// for before the attention reads them.
+// kv_wait: the previous chunk's K/V event of the layer (chunk overlap),
+// waited for before the attention reads the earlier rows; kv_done: recorded
+// after this chunk's K/V rows of the layer are written and after that wait, so
+// it stands for the K/V rows of this chunk and of every earlier chunk (a chunk
+// two or three back runs on another stream and is covered only through it).
 int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base, float* x, int C, int pos0,
                 cudaEvent_t kv_done = nullptr, cudaEvent_t kv_wait = nullptr) {
   const pp_config& c = m->cfg;
@@ -720,8 +722,8 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
       return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs, true);
     }));
   }
-  if (kv_done) PP_CUDA(cudaEventRecord(kv_done, cs));
   if (kv_wait) PP_CUDA(cudaStreamWaitEvent(cs, kv_wait, 0));
+  if (kv_done) PP_CUDA(cudaEventRecord(kv_done, cs));
   PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
     return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
   }));
@@ -833,12 +835,13 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   };
   const bool overlap = m->overlap && !streamed && !layer_outer && !m->trace && !m->layer_prof && n > chunk;
   if (overlap) {
-    // "Batched Prefill" with consecutive chunks on two streams: chunk k runs on
-    // stream k % 2 with scratch set k % 2 and waits, layer by layer, only for
-    // chunk k-1's K/V rows before its attention (a chunk's other inputs are its
-    // own), so chunk k's layer l can fill the SMs that chunk k-1 leaves idle
-    // between its kernels. Chunk k-2 ran on the same stream: its scratch and its
-    // K/V rows are complete in stream order.
+    // "Batched Prefill" with consecutive chunks on NS streams: chunk k runs on
+    // stream k % NS with scratch set k % NS and waits, layer by layer, for the
+    // K/V rows of every earlier chunk before its attention (chunk k-1's event,
+    // recorded after chunk k-1's own wait, covers them all; a chunk's other
+    // inputs are its own), so chunk k's layer l can fill the SMs the others
+    // leave idle between their kernels. Chunk k-NS ran on the same stream: its
+    // scratch set is free in stream order.
     constexpr int NS = pp_model::kOverlap;
     cudaStream_t S[NS];
     S[0] = cs;
