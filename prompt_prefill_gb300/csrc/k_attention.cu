@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(256)
 
 template <int HD>
 cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H, int Hkv,
-                     float* o, float* part, size_t part_bytes, cudaStream_t s) {
+                     float* o, float* part, size_t part_bytes, cudaStream_t s, bool pdl) {
   constexpr int smem = (ROWS * HD + 2 * KB * HD + KB * PS) * (int)sizeof(float);
   static bool attr = false;
   if (!attr) {
@@ -376,8 +376,8 @@ cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows,
   if (n_ranges > 1 && (!part || part_bytes < attention_workspace_bytes(rows, start_pos, H, Hkv, HD)))
     return cudaErrorInvalidValue;
   const float qscale = (float)(1.4426950408889634 / sqrt((double)HD));
-  cudaError_t e = launch_pdl(k_attention<HD>, dim3(n_tiles * Hkv * n_ranges), dim3(THREADS), (size_t)smem, s, q, kc,
-                             vc, rows, start_pos, H, Hkv, o, qscale, part, n_ranges);
+  cudaError_t e = launch_pdl_if(pdl, k_attention<HD>, dim3(n_tiles * Hkv * n_ranges), dim3(THREADS), (size_t)smem, s,
+                                q, kc, vc, rows, start_pos, H, Hkv, o, qscale, part, n_ranges);
   if (e == cudaSuccess && n_ranges > 1)
     e = launch_pdl(k_attention_merge<HD>, dim3(n_tiles * Hkv * (ROWS * HD / 4 / 256)), dim3(256), 0, s, rows,
                    start_pos, H, Hkv, o, (const float*)part, n_ranges);
@@ -395,9 +395,9 @@ size_t attention_workspace_bytes(int rows, int start_pos, int H, int Hkv, int hd
 }
 
 cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,
-                             int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s) {
-  if (hd == 64) return launch_t<64>(q, kc, vc, rows, start_pos, H, Hkv, o, part, part_bytes, s);
-  if (hd == 128) return launch_t<128>(q, kc, vc, rows, start_pos, H, Hkv, o, part, part_bytes, s);
+                             int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s, bool pdl) {
+  if (hd == 64) return launch_t<64>(q, kc, vc, rows, start_pos, H, Hkv, o, part, part_bytes, s, pdl);
+  if (hd == 128) return launch_t<128>(q, kc, vc, rows, start_pos, H, Hkv, o, part, part_bytes, s, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -725,7 +725,9 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
   if (kv_wait) PP_CUDA(cudaStreamWaitEvent(cs, kv_wait, 0));
   if (kv_done) PP_CUDA(cudaEventRecord(kv_done, cs));
   PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
-    return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs);
+    // after another stream's event the launch is plainly stream-ordered
+    return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs,
+                            kv_wait == nullptr);
   }));
   if (attention_workspace_bytes(C, pos0, H, Hkv, hd)) m->stats.kernel_launches += 1;  // the range merge
   PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {

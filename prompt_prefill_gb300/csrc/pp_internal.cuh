@@ -89,8 +89,11 @@ constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of 
 constexpr int kAttnRange = 512;
 // Bytes of per-range partial state a launch of this size needs (0: one range).
 size_t attention_workspace_bytes(int rows, int start_pos, int H, int Hkv, int hd);
+// pdl: allow the launch to start early behind the stream's previous kernel
+// (off when another stream's event must hold it back).
 cudaError_t launch_attention(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H,
-                             int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s);
+                             int Hkv, int hd, float* o, float* part, size_t part_bytes, cudaStream_t s,
+                             bool pdl = true);
 
 // ---- grow-on-demand K/V memory (kv_space.cu): n_regions regions of region_bytes
 // in one reserved virtual range; the first `mapped` bytes of every region are
@@ -115,9 +118,11 @@ void kv_space_free(KvSpace* s);
 constexpr int kSwiGluBlock = 16;
 
 // Launch kern<<<grid, block, smem, s>>>(args...) with programmatic dependent
-// launch allowed (the kernel calls ppdev::pdl_wait before using its inputs).
+// launch allowed (the kernel calls ppdev::pdl_wait before using its inputs),
+// or as a plain stream-ordered launch when pdl is false.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl_if(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -127,8 +132,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  return launch_pdl_if(true, kern, grid, block, smem, s, args...);
 }
 
 }  // namespace pp
