@@ -466,6 +466,9 @@ def run_streamed(args, cfg, world, rank, local, pg):
         g = pp.PrefillModel(cfg, model, max_seq=max(lens), max_chunk=chunk, mode=pp.PP_MODE_STREAMED,
                             ring_slots=slots, gemm_engine=args.engine, loop_order=order)
         tag = "" if order == pp.PP_LOOP_CHUNK_OUTER else "_layer_outer"
+        overlap = bool(args.overlap) and order == pp.PP_LOOP_LAYER_OUTER  # chunk-outer streaming is H2D-bound
+        if overlap:
+            g.set_chunk_overlap(True)
         stream = torch.cuda.current_stream()
         for P in lens:
             toks = synth.prompt(cfg, P)
@@ -488,6 +491,7 @@ def run_streamed(args, cfg, world, rank, local, pg):
             layer_block = h2d / ((1 if order == pp.PP_LOOP_LAYER_OUTER else n_chunks) * cfg.n_layers)
             results[f"{P}_slots{slots}{tag}"] = {
                 "prompt": P, "ring_slots": slots, "loop": "layer-outer" if tag else "chunk-outer",
+                "chunk_overlap": overlap,
                 "tok_per_s": P / (ms / 1000), "ms": ms,
                 "h2d_bytes_per_prompt": h2d, "h2d_bytes_naive_per_prompt": layer_block * cfg.n_layers * P,
                 "prefetch_hits": st["prefetch_hits"] // args.steps, "prefetch_misses": st["prefetch_misses"] // args.steps,

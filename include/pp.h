@@ -202,17 +202,20 @@ int pp_reset_stats(pp_model* m);
  * and summed duration appear in pp_stats (prof_launches, prof_ms). */
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
-/* Chunk overlap (1 on, 0 off; off after pp_model_load), resident weights and
- * chunk-outer order only ("Batched Prefill": chunks in order, each swept
- * through every layer). Consecutive chunks of a call rotate over four streams,
- * each with its own scratch set; a chunk waits, layer by layer, only for the
- * previous chunk's K/V rows of that layer before its attention reads them, so
- * one chunk's kernels can use the SMs the others leave idle. Results are
- * bit-identical to the serial order. The first call that turns it on
+/* Chunk overlap (1 on, 0 off; off after pp_model_load). The chunks of a call
+ * rotate over four streams, each with its own scratch set; a chunk waits, layer
+ * by layer, only for the earlier chunks' K/V rows of that layer before its
+ * attention reads them ("Single-pass prefill": K/V history written position
+ * by position), so one chunk's kernels can use the SMs the others leave idle.
+ * Chunk-outer order ("Batched Prefill") with resident weights: the chunks run
+ * through their layers concurrently. Layer-outer order, resident or streamed:
+ * the chunks of each layer run concurrently (streamed: every stream waits for
+ * the layer's copy, and the ring slot is released after all of them). Results
+ * are bit-identical to the serial order. The first call that turns it on
  * allocates three more scratch sets and streams (PP_ERR_OOM if that fails)
  * after waiting for the model's work. Ignored while a trace or the per-layer
- * profile is on, and for calls of a single chunk. PP_ERR_UNSUPPORTED for a
- * streamed-mode model. */
+ * profile is on, for calls of a single chunk, and for streamed weights in
+ * chunk-outer order. */
 int pp_set_chunk_overlap(pp_model* m, int32_t enable);
 
 /* Per-layer stage profile ("Single-pass prefill", the per-layer profiler of

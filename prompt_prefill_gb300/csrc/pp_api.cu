@@ -906,23 +906,61 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     }
   } else {
     // "Single-pass prefill": for each layer, every chunk of the call; the
-    // residual rows of all n positions stay in m->x between layers
+    // residual rows of all n positions stay in m->x between layers. With chunk
+    // overlap the chunks of a layer rotate over the streams as in chunk-outer
+    // order (their residual rows are disjoint slices of set 0's m->x); with
+    // streamed weights every stream waits for the layer's copy and the ring
+    // slot is freed only after every stream's work on the layer.
+    const bool ovl = m->overlap && !m->trace && !m->layer_prof && n > chunk;
+    constexpr int NS = pp_model::kOverlap;
+    cudaStream_t S[NS];
+    S[0] = cs;
+    for (int i = 1; i < NS; ++i) S[i] = ovl ? m->ostream[i - 1] : cs;
+    auto fan = [&](bool out) -> int {  // out: the others wait for cs; in: cs waits for the others
+      for (int i = 1; i < NS; ++i) {
+        cudaEvent_t e;
+        PP_TRY(ev_get(m, &e));
+        PP_CUDA(cudaEventRecord(e, out ? cs : S[i]));
+        PP_CUDA(cudaStreamWaitEvent(out ? S[i] : cs, e, 0));
+        m->ev_pool.push_back(e);
+      }
+      return PP_OK;
+    };
     PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok, n, m->emb, c.vocab, D, m->x, m->status, cs); }));
-    for (int l = 0; l < c.n_layers; ++l) {
+    float* const x0 = m->x;
+    if (ovl) {
+      PP_TRY(fan(true));
+      m->gemm_wide = true;
+    }
+    int rc = PP_OK;
+    for (int l = 0; l < c.n_layers && rc == PP_OK; ++l) {
       const uint8_t* base;
       int mg;
-      PP_TRY(layer_weights(m, cs, l, l, n_visits, &base, &mg));
-      cudaEvent_t ev;
-      PP_TRY(visit_begin(&ev));
-      for (int c0 = 0; c0 < n; c0 += chunk)
-        PP_TRY(layer_block(m, cs, l, mg, base, m->x + (size_t)c0 * D, std::min(chunk, n - c0), start_pos + c0));
-      PP_TRY(visit_end(l, l, ev));
-      if (streamed) PP_CUDA(cudaEventRecord(m->ring_free[l % c.ring_slots], cs));
+      rc = layer_weights(m, cs, l, l, n_visits, &base, &mg);
+      if (rc == PP_OK && ovl && streamed) rc = fan(true);
+      cudaEvent_t ev = nullptr;
+      if (rc == PP_OK) rc = visit_begin(&ev);
+      int k = 0;
+      for (int c0 = 0; c0 < n && rc == PP_OK; c0 += chunk, ++k) {
+        const int p = ovl ? k % NS : 0;
+        if (ovl) use_scratch(m, p);
+        rc = layer_block(m, S[p], l, mg, base, x0 + (size_t)c0 * D, std::min(chunk, n - c0), start_pos + c0,
+                         ovl ? m->qkv_ev[p][l] : nullptr, ovl && k > 0 ? m->qkv_ev[(k + NS - 1) % NS][l] : nullptr);
+      }
+      if (rc == PP_OK && ovl && streamed) rc = fan(false);
+      if (rc == PP_OK) rc = visit_end(l, l, ev);
+      if (rc == PP_OK && streamed) PP_CUDA(cudaEventRecord(m->ring_free[l % c.ring_slots], cs));
     }
+    if (ovl) {
+      use_scratch(m, 0);
+      m->gemm_wide = false;
+      if (rc == PP_OK) rc = fan(false);
+    }
+    PP_TRY(rc);
     if (m->trace)
       PP_CUDA(cudaMemcpyAsync(m->trace + ((size_t)c.n_layers * m->trace_pos + start_pos) * D, m->x,
                               sizeof(float) * n * D, cudaMemcpyDeviceToDevice, cs));
-    PP_TRY(head(m, cs, m->x + (size_t)(n - 1) * D, d_logits));
+    PP_TRY(head(m, cs, x0 + (size_t)(n - 1) * D, d_logits));
   }
   if (streamed && st != m->stream) {
     cudaEvent_t e;
@@ -1098,10 +1136,6 @@ int pp_set_chunk_overlap(pp_model* m, int32_t enable) {
   if (!m || (enable != 0 && enable != 1)) {
     set_err("bad pp_set_chunk_overlap arguments");
     return PP_ERR_ARG;
-  }
-  if (enable && m->cfg.mode == PP_MODE_STREAMED) {
-    set_err("chunk overlap needs resident weights");
-    return PP_ERR_UNSUPPORTED;
   }
   if (enable && !m->sets_ready) {
     PP_TRY(sync_model(m));

@@ -130,3 +130,51 @@ def test_layer_profile_streamed(m1b, slots, order):
     if slots == 1:
         assert all(p["wait_ms"] > 0 for p in prof[1:])
     assert s["prefetch_hits"] + s["prefetch_misses"] == visits * c.n_layers
+
+
+def test_layer_outer_chunk_overlap_resident(m350):
+    # the chunks of each layer on four streams: same bits as the serial chunk-outer order
+    c = m350.cfg
+    toks = synth.prompt(c)  # 747 tokens: 23 chunks of 32 and one of 11
+    ref_g = load(m350, max_seq=1024, max_chunk=32)
+    ref = ref_g.prefill(toks, 0, 32)
+    ref_kv = [ref_g.kv(l, w, 0, len(toks)) for l in (0, c.n_layers - 1) for w in (0, 1)]
+    ref_g.close()
+    g = load(m350, max_seq=1024, max_chunk=32, loop_order=pp.PP_LOOP_LAYER_OUTER)
+    try:
+        g.set_chunk_overlap(True)
+        got = g.prefill(toks, 0, 32)
+        got_kv = [g.kv(l, w, 0, len(toks)) for l in (0, c.n_layers - 1) for w in (0, 1)]
+        g.kv_reset()
+        g.prefill(toks[:300], 0, 17)
+        cont = g.prefill(toks[300:], 300, 32)
+    finally:
+        g.close()
+    assert np.array_equal(bits(got), bits(ref))
+    assert np.array_equal(bits(cont), bits(ref))
+    for a, b in zip(got_kv, ref_kv):
+        assert np.array_equal(bits(a), bits(b))
+
+
+@pytest.mark.parametrize("slots", [2, 1])
+def test_layer_outer_streamed_chunk_overlap(m1b, slots):
+    # streamed weights, each layer's chunks on four streams: every stream waits for the layer's copy and
+    # the slot is released after all of them; same bits and the same copies as without overlap
+    c = m1b.cfg
+    P, chunk = 700, 128
+    toks = synth.prompt(c, P)
+    res = load(m1b, max_seq=1024, max_chunk=chunk)
+    ref = res.prefill(toks, 0, chunk)
+    res.close()
+    g = load(m1b, max_seq=1024, max_chunk=chunk, mode=pp.PP_MODE_STREAMED, ring_slots=slots,
+             loop_order=pp.PP_LOOP_LAYER_OUTER)
+    try:
+        g.set_chunk_overlap(True)
+        g.reset_stats()
+        got = g.prefill(toks, 0, chunk)
+        s = g.stats()
+    finally:
+        g.close()
+    assert np.array_equal(bits(got), bits(ref))
+    assert s["h2d_bytes"] == c.n_layers * _layer_block_bytes(c) + 4 * P
+    assert s["prefetch_hits"] + s["prefetch_misses"] == c.n_layers
