@@ -249,6 +249,8 @@ int ev_get(pp_model* m, cudaEvent_t* e) {
 int sync_model(pp_model* m) {
   PP_CUDA(cudaStreamSynchronize(m->stream));
   if (m->copy_stream) PP_CUDA(cudaStreamSynchronize(m->copy_stream));
+  for (auto s : m->ostream)
+    if (s) PP_CUDA(cudaStreamSynchronize(s));
   if (m->done) PP_CUDA(cudaEventSynchronize(m->done));
   return PP_OK;
 }
@@ -575,6 +577,8 @@ int load_impl(pp_model* m, const pp_weights* w) {
 void free_impl(pp_model* m) {
   if (m->stream) cudaStreamSynchronize(m->stream);
   if (m->copy_stream) cudaStreamSynchronize(m->copy_stream);
+  for (auto s : m->ostream)
+    if (s) cudaStreamSynchronize(s);
   if (m->done) {
     cudaEventSynchronize(m->done);
     cudaEventDestroy(m->done);
