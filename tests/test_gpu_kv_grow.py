@@ -64,3 +64,20 @@ def test_grow_continuation_reset_and_errors(m350):
     assert b_100 % (2 * c.n_layers) == 0
     assert pp.pp_prefill_rc(g.h, np.ones(8, np.int32), 4090, 8, c.vocab) == pp.PP_ERR_CAPACITY
     g.close()
+
+
+def test_grow_with_chunk_overlap(m350):
+    # memory mapped at the start of each call, chunks on four streams: same bits as the reserved cache
+    c = m350.cfg
+    toks = synth.prompt(c)
+    ref_g = load(m350, max_seq=2048, max_chunk=64)
+    ref = ref_g.prefill(toks, 0, 64)
+    ref_g.close()
+    g = load(m350, max_seq=2048, max_chunk=64, kv_grow=1)
+    try:
+        g.set_chunk_overlap(True)
+        g.prefill(toks[:200], 0, 64)
+        got = g.prefill(toks[200:], 200, 64)  # grows the mapping, then continues the cache
+    finally:
+        g.close()
+    assert np.array_equal(bits(got), bits(ref))

@@ -243,6 +243,25 @@ def test_1b_layer_by_layer_and_logits(one_b):
     _assert_e2e(got, ref, "1b final")
 
 
+def test_chunk_overlap_both_engines():
+    # tiny model, 32 tokens in chunks of 8: four chunks on four streams give the serial bits with either
+    # GEMM engine (the mma.sync path also keeps its RoPE kernel)
+    torch_cuda()
+    m = synth.make_model(synth.CONFIGS["tiny"])
+    toks = synth.prompt(m.cfg)
+    out = []
+    for eng in (pp.PP_GEMM_MMA, pp.PP_GEMM_TC):
+        for overlap in (False, True):
+            g = load(m, max_seq=64, max_chunk=32, gemm_engine=eng)
+            try:
+                g.set_chunk_overlap(overlap)
+                out.append(g.prefill(toks, 0, 8))
+            finally:
+                g.close()
+    for o in out[1:]:
+        assert np.array_equal(bits(o), bits(out[0]))
+
+
 def test_engines_give_identical_logits():
     # the two GEMM engines compute the same integers, so whole prefills agree bit for bit
     torch_cuda()
