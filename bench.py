@@ -42,8 +42,8 @@ FP32_LANES = 128
 KERNEL_TRAFFIC = {
     # k_attention, mean over the 8 launches of one layer (chunk starts 0, 512, ..., 3584); the range merge
     # kernel's own bytes are listed in its profile summary
-    "attention": {"bytes_per_launch": 33144640.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
-                  "sha256": "285b18a54d6527342a8f11c64e00a366a2391d47a8505c52fe1409c8fe33f0d1"},
+    "attention": {"bytes_per_launch": 33144704.0, "source": "prompt_prefill_gb300/csrc/k_attention.cu",
+                  "sha256": "3126986e9cac0e39cadbd1c23e1552acda354fd2ad8b3df0a9b5b4c944e9d375"},
 }
 
 
