@@ -214,6 +214,7 @@ struct pp_model {
   bool overlap = false;
   bool gemm_wide = false;  // the current call overlaps chunks: widest GEMM tiles, no stream-K
   bool sets_ready = false;
+  int sets_alloc = 1;  // scratch sets fully allocated (set 0 at load)
   int active_set = 0;
   Scratch sets[kOverlap]{};
   cudaStream_t ostream[kOverlap - 1] = {};
@@ -402,13 +403,16 @@ int validate_cfg(const pp_config* c) {
 
 // One scratch set (residual rows, activations, codes, attention and stream-K
 // workspaces, the activation tensor maps) into the model's scratch fields.
-int alloc_scratch(pp_model* m) {
+// own_residual: the set holds the residual rows of every position of a call
+// (layer-outer order); the extra sets of chunk overlap use set 0's for that.
+int alloc_scratch(pp_model* m, bool own_residual = true) {
   const pp_config& c = m->cfg;
   const size_t D = c.dim, QD = (size_t)c.n_heads * c.head_dim,
                QKV = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn, MC = c.max_chunk;
   const size_t KMAX = std::max(std::max(D, QD), F);
   // residual stream: max_chunk rows chunk-outer, every position of a call layer-outer
-  PP_TRY(dalloc(m, &m->x, (c.loop_order == PP_LOOP_LAYER_OUTER ? std::max(MC, (size_t)c.max_seq) : MC) * D));
+  const bool all_rows = own_residual && c.loop_order == PP_LOOP_LAYER_OUTER;
+  PP_TRY(dalloc(m, &m->x, (all_rows ? std::max(MC, (size_t)c.max_seq) : MC) * D));
   // QKV rows staged for the RoPE kernel (the tcgen05 path rotates in its QKV epilogue instead)
   if (m->engine != PP_GEMM_TC) PP_TRY(dalloc(m, &m->qkv, MC * QKV));
   PP_TRY(dalloc(m, &m->qr, MC * QD));
@@ -879,13 +883,15 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     }
     use_scratch(m, 0);  // set 0 is the model's between calls
     m->gemm_wide = false;
-    PP_TRY(rc);
-    for (int i = 1; i < NS; ++i) {  // the call ends on the caller's stream
+    // the call ends on the caller's stream, also after an error: whatever the
+    // other streams have queued is ordered before the caller's next work
+    for (int i = 1; i < NS; ++i) {
       PP_TRY(ev_get(m, &e));
       PP_CUDA(cudaEventRecord(e, S[i]));
       PP_CUDA(cudaStreamWaitEvent(cs, e, 0));
       m->ev_pool.push_back(e);
     }
+    PP_TRY(rc);
   } else if (!layer_outer) {
     // "Batched Prefill": for each chunk, every layer over the chunk's rows
     int visit = 0;
@@ -958,7 +964,8 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     if (ovl) {
       use_scratch(m, 0);
       m->gemm_wide = false;
-      if (rc == PP_OK) rc = fan(false);
+      const int rf = fan(false);  // also after an error (see chunk-outer order)
+      if (rc == PP_OK) rc = rf;
     }
     PP_TRY(rc);
     if (m->trace)
@@ -1142,16 +1149,20 @@ int pp_set_chunk_overlap(pp_model* m, int32_t enable) {
     return PP_ERR_ARG;
   }
   if (enable && !m->sets_ready) {
+    // A call that failed part of the way leaves what it made in place (released
+    // with the model); a later call resumes from there.
     PP_TRY(sync_model(m));
-    for (int j = 1; j < pp_model::kOverlap; ++j) {
-      use_scratch(m, j);  // empty fields: the set is allocated into them
-      const int rc = alloc_scratch(m);
+    for (int j = m->sets_alloc; j < pp_model::kOverlap; ++j) {
+      use_scratch(m, j);  // the set is (re)allocated into its fields
+      const int rc = alloc_scratch(m, false);
       use_scratch(m, 0);
-      if (rc != PP_OK) return rc;  // what was allocated is released with the model
-      PP_CUDA(cudaStreamCreateWithFlags(&m->ostream[j - 1], cudaStreamNonBlocking));
+      if (rc != PP_OK) return rc;
+      m->sets_alloc = j + 1;
     }
+    for (int j = 1; j < pp_model::kOverlap; ++j)
+      if (!m->ostream[j - 1]) PP_CUDA(cudaStreamCreateWithFlags(&m->ostream[j - 1], cudaStreamNonBlocking));
     for (int p = 0; p < pp_model::kOverlap; ++p)
-      for (int l = 0; l < m->cfg.n_layers; ++l) {
+      while ((int)m->qkv_ev[p].size() < m->cfg.n_layers) {
         cudaEvent_t e;
         PP_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
         m->qkv_ev[p].push_back(e);
