@@ -471,15 +471,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         return reinterpret_cast<int4*>(p.part) +
                ((((size_t)tile * p.max_slots + slot) * 2 + rank) * N_DRAIN_WARPS + dw) * (COLS / 4) * 32 + lane;
       };
-      int4* mine = slot_ptr(cluster - c_first);
+      // When every other contributor has already arrived (the usual case for the
+      // tile's first k-blocks, which a cluster runs last), this CTA is the last
+      // one and its own sums never leave its registers.
+      if (et == 0) {
+        int arrived;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(arrived) : "l"(p.cnt + 2 * tile + rank) : "memory");
+        *last_flag = arrived == n_contrib - 1;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
+      if (!*last_flag) {  // (the flag is rewritten only after the next barrier, which every thread reaches after reading it)
+        int4* mine = slot_ptr(cluster - c_first);
 #pragma unroll
-      for (int j = 0; j < COLS / 4; ++j)
-        mine[32 * j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
-      __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
-      if (et == 0) *last_flag = atomicAdd(p.cnt + 2 * tile + rank, 1) == n_contrib - 1;
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
-      if (!*last_flag) return false;
+        for (int j = 0; j < COLS / 4; ++j)
+          mine[32 * j] = make_int4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
+        if (et == 0) *last_flag = atomicAdd(p.cnt + 2 * tile + rank, 1) == n_contrib - 1;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * N_DRAIN_WARPS) : "memory");
+        if (!*last_flag) return false;
+      }
       __threadfence();
       for (int sl = 0; sl < n_contrib; ++sl) {
         if (sl == cluster - c_first) continue;
