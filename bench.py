@@ -610,7 +610,7 @@ def main(argv=None):
     ap.add_argument("--ref-sample-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--overlap", type=int, default=1,
-                    help="1 (default): consecutive chunks on four streams (pp_set_chunk_overlap); 0: serial")
+                    help="1 (default): consecutive chunks on eight streams (pp_set_chunk_overlap); 0: serial")
     ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention | quant | norm_quant")
     ap.add_argument("--m", type=int, default=512)
     ap.add_argument("--n", type=int, default=28672)

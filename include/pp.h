@@ -203,7 +203,7 @@ int pp_reset_stats(pp_model* m);
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
 /* Chunk overlap (1 on, 0 off; off after pp_model_load). The chunks of a call
- * rotate over four streams, each with its own scratch set; a chunk waits, layer
+ * rotate over eight streams, each with its own scratch set; a chunk waits, layer
  * by layer, only for the earlier chunks' K/V rows of that layer before its
  * attention reads them ("Single-pass prefill": K/V history written position
  * by position), so one chunk's kernels can use the SMs the others leave idle.
@@ -212,7 +212,7 @@ int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
  * the chunks of each layer run concurrently (streamed: every stream waits for
  * the layer's copy, and the ring slot is released after all of them). Results
  * are bit-identical to the serial order. The first call that turns it on
- * allocates three more scratch sets and streams (PP_ERR_OOM if that fails)
+ * allocates seven more scratch sets and streams (PP_ERR_OOM if that fails)
  * after waiting for the model's work. Ignored while a trace or the per-layer
  * profile is on, for calls of a single chunk, and for streamed weights in
  * chunk-outer order. */

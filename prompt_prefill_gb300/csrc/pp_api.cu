@@ -210,7 +210,7 @@ struct pp_model {
     size_t attn_part_bytes;
     CUtensorMap amap_d, amap_qd, amap_f;
   };
-  static constexpr int kOverlap = 4;
+  static constexpr int kOverlap = 8;
   bool overlap = false;
   bool gemm_wide = false;  // the current call overlaps chunks: widest GEMM tiles, no stream-K
   bool sets_ready = false;

@@ -67,7 +67,7 @@ def test_grow_continuation_reset_and_errors(m350):
 
 
 def test_grow_with_chunk_overlap(m350):
-    # memory mapped at the start of each call, chunks on four streams: same bits as the reserved cache
+    # memory mapped at the start of each call, chunks on the overlap streams: same bits as the reserved cache
     c = m350.cfg
     toks = synth.prompt(c)
     ref_g = load(m350, max_seq=2048, max_chunk=64)

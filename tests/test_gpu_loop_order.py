@@ -133,7 +133,7 @@ def test_layer_profile_streamed(m1b, slots, order):
 
 
 def test_layer_outer_chunk_overlap_resident(m350):
-    # the chunks of each layer on four streams: same bits as the serial chunk-outer order
+    # the chunks of each layer rotating over the overlap streams: same bits as the serial chunk-outer order
     c = m350.cfg
     toks = synth.prompt(c)  # 747 tokens: 23 chunks of 32 and one of 11
     ref_g = load(m350, max_seq=1024, max_chunk=32)
@@ -158,10 +158,11 @@ def test_layer_outer_chunk_overlap_resident(m350):
 
 @pytest.mark.parametrize("slots", [2, 1])
 def test_layer_outer_streamed_chunk_overlap(m1b, slots):
-    # streamed weights, each layer's chunks on four streams: every stream waits for the layer's copy and
-    # the slot is released after all of them; same bits and the same copies as without overlap
+    # streamed weights, each layer's chunks rotating over the overlap streams (11 chunks: more than
+    # streams): every stream waits for the layer's copy and the slot is released after all of them; same
+    # bits and the same copies as without overlap
     c = m1b.cfg
-    P, chunk = 700, 128
+    P, chunk = 700, 64
     toks = synth.prompt(c, P)
     res = load(m1b, max_seq=1024, max_chunk=chunk)
     ref = res.prefill(toks, 0, chunk)

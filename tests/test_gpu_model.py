@@ -244,8 +244,9 @@ def test_1b_layer_by_layer_and_logits(one_b):
 
 
 def test_chunk_overlap_both_engines():
-    # tiny model, 32 tokens in chunks of 8: four chunks on four streams give the serial bits with either
-    # GEMM engine (the mma.sync path also keeps its RoPE kernel)
+    # tiny model, 32 tokens in chunks of 8 (fewer chunks than streams) and of 3 (11 chunks, more than
+    # streams, so scratch sets are reused; a ragged last chunk): the serial bits with either GEMM engine
+    # (the mma.sync path also keeps its RoPE kernel)
     torch_cuda()
     m = synth.make_model(synth.CONFIGS["tiny"])
     toks = synth.prompt(m.cfg)
@@ -255,7 +256,9 @@ def test_chunk_overlap_both_engines():
             g = load(m, max_seq=64, max_chunk=32, gemm_engine=eng)
             try:
                 g.set_chunk_overlap(overlap)
-                out.append(g.prefill(toks, 0, 8))
+                for chunk in (8, 3):
+                    g.kv_reset()
+                    out.append(g.prefill(toks, 0, chunk))
             finally:
                 g.close()
     for o in out[1:]:
@@ -308,8 +311,9 @@ def test_head_dim_128_fused_rope_engines_and_oracle():
 
 
 def test_1b_chunk_overlap_bit_identical(one_b):
-    # Chunks alternating between two streams (each waits only for the previous chunk's K/V rows of a
-    # layer) give the serial path's bits: logits, K/V rows, ragged chunks and a continuation call.
+    # Chunks rotating over the overlap streams (each waits only for the previous chunk's K/V rows of a
+    # layer) give the serial path's bits: logits, K/V rows, ragged chunks (21 chunks of 100: more than
+    # streams) and a continuation call.
     m, g = one_b
     toks = synth.prompt(m.cfg)  # 2048 tokens
     g.kv_reset()
