@@ -32,8 +32,14 @@ if ROOT not in sys.path:
 
 METRIC = "prefill tok/s (int8 8B-shape, 4096-tok prompt); % of int8-TC/HBM roofline"
 NORTH_HBM_GBS = 8000.0  # the 8 TB/s of the roofline definition
-SMS = 152
-FP32_LANES = 128
+FP32_LANES = 128  # FP32 FMA lanes per SM
+
+
+def sm_count() -> int:
+    """SMs of the current CUDA device (152 on a GB300)."""
+    import torch
+
+    return int(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
 
 # DRAM bytes (read + write) per launch of a kernel class at the 8B / chunk 512
 # workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
@@ -129,13 +135,14 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
-def peak_for(bound: str, peaks: dict) -> tuple[float, str]:
+def peak_for(bound: str, peaks: dict, sms: int | None = None) -> tuple[float, str]:
     if bound == "tensor":
         # the exact-integer GEMMs run at f16 operand rate; bf16 and f16 dense rates are equal
         return float(peaks["bf16_tflops_sustained"]), f"bf16/f16 dense sustained ({peaks['source']})"
     if bound == "alu":
         clk = float(peaks.get("sm_max_mhz", 2070.0))
-        return SMS * FP32_LANES * 2 * clk * 1e6 / 1e12, f"FP32 FMA: {SMS} SMs x {FP32_LANES} lanes x 2 x {clk:.0f} MHz"
+        sms = sms or sm_count()
+        return sms * FP32_LANES * 2 * clk * 1e6 / 1e12, f"FP32 FMA: {sms} SMs x {FP32_LANES} lanes x 2 x {clk:.0f} MHz"
     return float(peaks["hbm_gbs"]), f"HBM copy ({peaks['source']})"
 
 
@@ -287,6 +294,188 @@ def workload_config(cfg, args) -> dict:
 
 
 # ----------------------------------------------------------------------------- our arm
+def time_calls(stream, fn, steps: int, warmup: int) -> float:
+    """Milliseconds per call of fn() (enqueued on `stream`), CUDA events on that stream."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def profile_classes(g, step, steps_dominant: int = 1):
+    """Per kernel class: summed launch time of one step with every launch of the class bracketed by CUDA
+    events on its stream (chunks in serial order, so no other kernel runs inside a bracket). The
+    dominant class is then profiled over `steps_dominant` further steps. Returns ({class: ms per step},
+    {class: launches per step}, dominant)."""
+    import prompt_prefill_gb300 as pp
+
+    class_ms, class_launches = {}, {}
+    for cls, name in pp.KERNEL_NAMES.items():
+        g.set_profile_kernel(cls)
+        g.reset_stats()
+        step()
+        s = g.stats()
+        class_ms[name] = s["prof_ms"]
+        class_launches[name] = s["prof_launches"]
+    dominant = max(class_ms, key=class_ms.get)
+    if steps_dominant > 1:
+        g.set_profile_kernel({v: k for k, v in pp.KERNEL_NAMES.items()}[dominant])
+        g.reset_stats()
+        for _ in range(steps_dominant):
+            step()
+        s = g.stats()
+        class_ms[dominant] = s["prof_ms"] / steps_dominant
+        class_launches[dominant] = s["prof_launches"] // steps_dominant
+    g.set_profile_kernel(pp.PP_KERNEL_NONE)
+    g.reset_stats()
+    return class_ms, class_launches, dominant
+
+
+def prefill_roofline_ms(cfg, P, chunk, peaks, start_pos: int = 0) -> dict:
+    """max(int8 GEMM ops / tensor peak, bytes / 8 TB/s) for one call of P tokens."""
+    gemm_ops = 2 * P * cfg.layer_bytes() * cfg.n_layers
+    n_chunks = -(-P // chunk)
+    kv_row = 2 * cfg.n_kv_heads * cfg.head_dim * 4
+    kv_reads = sum(start_pos + min(P, (i + 1) * chunk) for i in range(n_chunks))
+    bytes_ = weight_bytes_read(cfg, P, chunk) + cfg.n_layers * kv_reads * kv_row
+    t_tc = gemm_ops / (peak_for("tensor", peaks)[0] * 1e12)
+    t_hbm = bytes_ / (NORTH_HBM_GBS * 1e9)
+    return {"t_roof_ms": 1000 * max(t_tc, t_hbm), "bound": "tensor" if t_tc >= t_hbm else "hbm",
+            "gemm_tops": gemm_ops / 1e12, "bytes_gb": bytes_ / 1e9}
+
+
+def run_small_configs(args, peaks) -> dict:
+    """The 350M-class (747 tokens, chunk 32) and 1B-class (2048 tokens, chunks 32..2048, then a call at
+    start_pos 2048 continuing the K/V cache) workloads: tok/s, prefill roofline fraction, and for
+    350M how much of a call the host spends enqueueing launches against the kernels' summed time."""
+    import time as _time
+
+    import torch
+
+    import prompt_prefill_gb300 as pp
+    import synth
+
+    stream = torch.cuda.current_stream()
+    steps, warm = max(3, min(args.steps, 10)), 3
+    out = {}
+    # ---- 350M: 747 tokens in chunks of 32
+    cfg = synth.CONFIGS["350m"]
+    model = synth.make_model(cfg)
+    P, chunk = cfg.prompt_len, cfg.chunk
+    g = pp.PrefillModel(cfg, model, max_seq=cfg.max_seq, max_chunk=chunk, gemm_engine=args.engine)
+    d_tok = torch.from_numpy(synth.prompt(cfg)).cuda()
+    d_logits = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+    step = lambda: g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)  # noqa: E731
+    res = {}
+    for overlap in (0, 1):
+        g.set_chunk_overlap(bool(overlap))
+        ms = time_calls(stream, step, steps, warm)
+        res["overlap" if overlap else "serial"] = {"ms": ms, "tok_per_s": P / (ms / 1000)}
+    g.set_chunk_overlap(False)
+    # host enqueue time of one call (the library's launches, no device wait) against the GPU time
+    torch.cuda.synchronize()
+    t0 = _time.perf_counter()
+    step()
+    host_ms = 1000 * (_time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    g.reset_stats()
+    step()
+    launches = g.stats()["kernel_launches"]
+    class_ms, _, _ = profile_classes(g, step)
+    kernel_ms = sum(class_ms.values())
+    roof = prefill_roofline_ms(cfg, P, chunk, peaks)
+    best = min(res["serial"]["ms"], res["overlap"]["ms"])
+    out["350m"] = {
+        "workload": f"350M-class int8 decoder (D{cfg.dim}, L{cfg.n_layers}, {cfg.n_heads}/{cfg.n_kv_heads} heads, "
+                    f"F{cfg.ffn}, V{cfg.vocab}): {P}-token prompt, chunk {chunk}",
+        "serial": res["serial"], "chunk_overlap": res["overlap"], "roofline": roof,
+        "frac_of_roofline": roof["t_roof_ms"] / best,
+        "launches_per_call": launches, "host_enqueue_ms_per_call": host_ms,
+        "kernel_ms_per_call_serial_profiled": kernel_ms, "kernel_ms_by_class": class_ms,
+        "host_enqueue_over_gpu_time": host_ms / res["serial"]["ms"]}
+    g.close()
+    del model
+    # ---- 1B: chunk sweep, then a continuation call at start_pos 2048
+    cfg = synth.CONFIGS["1b"]
+    model = synth.make_model(cfg)
+    P = cfg.prompt_len
+    toks = synth.prompt(cfg, 2 * P)
+    g = pp.PrefillModel(cfg, model, max_seq=2 * P, max_chunk=2048, gemm_engine=args.engine)
+    g.set_chunk_overlap(True)
+    d_tok = torch.from_numpy(toks).cuda()
+    d_logits = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+    sweep = {}
+    for chunk in cfg.extra["chunks"]:
+        ms = time_calls(stream, lambda: g.prefill_device(d_tok, P, 0, chunk, d_logits, stream), steps, warm)
+        roof = prefill_roofline_ms(cfg, P, chunk, peaks)
+        sweep[str(chunk)] = {"ms": ms, "tok_per_s": P / (ms / 1000), "frac_of_roofline": roof["t_roof_ms"] / ms,
+                             "roofline": roof, "weight_bytes_read": weight_bytes_read(cfg, P, chunk)}
+    # continuation: positions 2048..4095 after the first call wrote 0..2047
+    chunk = 512
+    g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)
+    ms = time_calls(stream, lambda: g.prefill_device(d_tok[P:], P, P, chunk, d_logits, stream), steps, warm)
+    roof = prefill_roofline_ms(cfg, P, chunk, peaks, start_pos=P)
+    g.close()
+    out["1b"] = {"workload": f"1B-class int8 decoder (D{cfg.dim}, L{cfg.n_layers}, {cfg.n_heads}/{cfg.n_kv_heads} "
+                             f"heads, F{cfg.ffn}, V{cfg.vocab}): {P}-token prompt, chunk sweep, chunk overlap on",
+                 "chunk_sweep": sweep,
+                 "continuation_start_pos_2048_chunk_512": {"ms": ms, "tok_per_s": P / (ms / 1000),
+                                                           "frac_of_roofline": roof["t_roof_ms"] / ms,
+                                                           "roofline": roof}}
+    return out
+
+
+def run_streamed_config(args, model, cfg8) -> dict:
+    """Weights in pinned host memory streamed into a 2-slot device ring ("Predictive prefetch"), prompts
+    122 / 512 / 2048 at chunk 512, chunk-outer and layer-outer: tok/s against the host-link bound,
+    host-to-device bytes against the per-token naive bytes, prefetch hits and misses."""
+    import torch
+
+    import prompt_prefill_gb300 as pp
+    import synth
+
+    stream = torch.cuda.current_stream()
+    cfg = synth.CONFIGS["8b-streamed"]
+    chunk = 512
+    bw = h2d_bandwidth_gbs()
+    steps, warm = max(1, min(args.steps, 3)), 3
+    out = {"h2d_gbs_measured": bw, "ring_slots": 2, "chunk": chunk,
+           "weights": "the resident workload's 8B-shaped weights, held in pinned host memory by the library"}
+    for order, tag in ((pp.PP_LOOP_CHUNK_OUTER, "chunk_outer"), (pp.PP_LOOP_LAYER_OUTER, "layer_outer")):
+        g = pp.PrefillModel(cfg8, model, max_seq=max(cfg.extra["prompt_lens"]), max_chunk=chunk,
+                            mode=pp.PP_MODE_STREAMED, ring_slots=2, gemm_engine=args.engine, loop_order=order)
+        if order == pp.PP_LOOP_LAYER_OUTER:
+            g.set_chunk_overlap(True)  # chunk-outer streaming is bound by the host link and stays serial
+        res = {}
+        for P in cfg.extra["prompt_lens"]:
+            d_tok = torch.from_numpy(synth.prompt(cfg, P)).cuda()
+            d_logits = torch.empty(cfg8.vocab, dtype=torch.float32, device="cuda")
+            for _ in range(warm):
+                g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)
+            torch.cuda.synchronize()
+            g.reset_stats()
+            ms = time_calls(stream, lambda: g.prefill_device(d_tok, P, 0, chunk, d_logits, stream), steps, 0)
+            st = g.stats()
+            h2d = st["h2d_bytes"] / steps
+            visits = (1 if order == pp.PP_LOOP_LAYER_OUTER else -(-P // chunk)) * cfg8.n_layers
+            layer_block = h2d / visits  # device-resident ids: the layer copies are the only host-to-device bytes
+            res[str(P)] = {"tok_per_s": P / (ms / 1000), "ms": ms, "h2d_bytes_per_prompt": h2d,
+                           "h2d_bytes_naive_per_prompt": layer_block * cfg8.n_layers * P,
+                           "prefetch_hits": st["prefetch_hits"] // steps, "prefetch_misses": st["prefetch_misses"] // steps,
+                           "h2d_bound_tok_per_s": P / (h2d / (bw * 1e9)), "frac_of_h2d_bound": (h2d / (bw * 1e9)) / (ms / 1000)}
+        out[tag] = res
+        g.close()
+    return out
+
+
 def run_ours(args, cfg, world, rank, local, pg):
     import torch
 
@@ -295,6 +484,7 @@ def run_ours(args, cfg, world, rank, local, pg):
 
     torch.cuda.set_device(local)
     peaks = load_peaks()
+    sms = sm_count()
     P, chunk = cfg.prompt_len, args.chunk
     model = synth.make_model(cfg)
     toks = synth.prompt(cfg, P, seed=cfg.seed + rank)
@@ -306,32 +496,23 @@ def run_ours(args, cfg, world, rank, local, pg):
     def step():
         g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)
 
-    # warm-up, then one profiled step per kernel class to find the dominant one. These steps run the
-    # chunks in serial order: with chunk overlap a launch's CUDA-event span would include the other
-    # stream's kernels, so the per-class breakdown and the isolated roofline come from serial steps.
+    # Warm-up, then profiled steps with the chunks in serial order: every launch of one kernel class
+    # bracketed by CUDA events on its stream, so each bracket holds that kernel alone (with chunk overlap a
+    # bracket would also hold the other streams' kernels). They give the per-class breakdown and the
+    # dominant kernel's own duration for `roofline`. Profiling is off again before the timed region.
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert g.device_status() == pp.PP_OK
-    class_ms, class_launches = {}, {}
-    for cls, name in pp.KERNEL_NAMES.items():
-        g.set_profile_kernel(cls)
-        g.reset_stats()
-        step()
-        s = g.stats()
-        class_ms[name] = s["prof_ms"]
-        class_launches[name] = s["prof_launches"]
-    dominant = max(class_ms, key=class_ms.get)
-    dom_cls = {v: k for k, v in pp.KERNEL_NAMES.items()}[dominant]
-    g.set_profile_kernel(dom_cls)
+    class_ms, class_launches, dominant = profile_classes(g, step, steps_dominant=max(1, min(args.steps, 5)))
     if args.overlap:
         g.set_chunk_overlap(True)
-        for _ in range(args.warmup):
-            step()
-        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
     g.reset_stats()
 
-    # timed region: K steps, device-resident inputs
+    # timed region: K steps, device-resident inputs, nothing but the prefill calls on the streams
     clocks = ClockSampler(local).start()
     barrier(pg)
     torch.cuda.synchronize()
@@ -350,9 +531,9 @@ def run_ours(args, cfg, world, rank, local, pg):
     launches = stats["kernel_launches"]
     logits = d_logits.cpu().numpy()
     assert np.all(np.isfinite(logits)), "non-finite logits"
+    assert g.device_status() == pp.PP_OK
 
     # e2e: the host C-ABI call (token ids host->device, logits device->host inside)
-    g.set_profile_kernel(pp.PP_KERNEL_NONE)
     barrier(pg)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -364,24 +545,23 @@ def run_ours(args, cfg, world, rank, local, pg):
 
     value = replica_tok_per_s(world, P, args.steps, ms_max / 1000.0)
     e2e_value = replica_tok_per_s(world, P, args.steps, t_e2e)
-    work = algorithmic_work(cfg, P, chunk)[dominant]
-    achieved_ms = stats["prof_ms"] / max(1, stats["prof_launches"])
-    per_launch = work["work"] / max(1, stats["prof_launches"] // args.steps)
+    awork = algorithmic_work(cfg, P, chunk)
+    work = awork[dominant]
     scale = 1e12 if work["unit"] == "TFLOP/s" else 1e9
-    achieved = per_launch / (achieved_ms / 1000.0) / scale
-    peak, peak_src = peak_for(work["bound"], peaks)
-    # the same kernel class in its serial profiled step (its launches alone on the GPU)
-    iso_ms = class_ms[dominant] / max(1, class_launches[dominant])
-    iso_achieved = (work["work"] / max(1, class_launches[dominant])) / (iso_ms / 1000.0) / scale
+    peak, peak_src = peak_for(work["bound"], peaks, sms)
+    # the dominant kernel's average launch duration in the profiled serial steps
+    per_launch_work = work["work"] / max(1, class_launches[dominant])
+    launch_ms = class_ms[dominant] / max(1, class_launches[dominant])
+    achieved = per_launch_work / (launch_ms / 1000.0) / scale
 
     # prefill roofline of the metric: max(GEMM ops / tensor peak, bytes / 8 TB/s)
-    gemm_ops = work_total = algorithmic_work(cfg, P, chunk)["gemm"]["work"]
+    gemm_ops = awork["gemm"]["work"]
     bytes_step = step_bytes(cfg, P, chunk)
     t_tc = gemm_ops / (peak_for("tensor", peaks)[0] * 1e12)
     t_roof = max(t_tc, bytes_step / (NORTH_HBM_GBS * 1e9))
     t_roof_meas = max(t_tc, bytes_step / (float(peaks["hbm_gbs"]) * 1e9))
     step_s = ms_max / 1000.0 / args.steps
-    del work_total
+    tensor_peak = peak_for("tensor", peaks)[0]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -390,23 +570,22 @@ def run_ours(args, cfg, world, rank, local, pg):
         "config": workload_config(cfg, args),
         "gemm_engine": {pp.PP_GEMM_MMA: "mma.sync s8", pp.PP_GEMM_TC: "tcgen05 exact-integer f16"}.get(g.gemm_engine),
         "chunk_overlap": bool(args.overlap),
-        "prefill_roofline": {"t_roof_ms": 1000 * t_roof, "frac": t_roof / step_s, "tensor_peak_tflops": peak_for(
-            "tensor", peaks)[0], "hbm_gbs": NORTH_HBM_GBS, "frac_vs_measured_hbm": t_roof_meas / step_s,
-            "gemm_tops": gemm_ops / 1e12, "bytes_gb": bytes_step / 1e9},
+        "prefill_roofline": {"t_roof_ms": 1000 * t_roof, "frac": t_roof / step_s, "tensor_peak_tflops": tensor_peak,
+                             "hbm_gbs": NORTH_HBM_GBS, "frac_vs_measured_hbm": t_roof_meas / step_s,
+                             "gemm_tops": gemm_ops / 1e12, "bytes_gb": bytes_step / 1e9},
         "roofline": {"kernel": dominant, "bound": work["bound"], "achieved": achieved, "peak": peak,
                      "unit": work["unit"], "frac": achieved / peak,
                      "traffic": kernel_traffic(dominant, "8b" if (args.workload, args.prompt, args.chunk) == ("8b", None, 512) else ""),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)", "peak_source": peak_src,
-                     "timed_with": "chunk overlap: each launch's span includes the other stream's kernels"
-                     if args.overlap else "serial chunks"},
-        "roofline_isolated": {"kernel": dominant, "achieved": iso_achieved, "peak": peak, "unit": work["unit"],
-                              "frac": iso_achieved / peak, "measured_in": "one profiled step, chunks in serial order"},
+                     "launch_ms": launch_ms, "launches_per_step": class_launches[dominant],
+                     "measured_in": "profiled steps with the chunks in serial order: CUDA events on the launching "
+                                    "stream around each launch of the kernel, averaged over its launches"},
         # the projection GEMMs as one class: the step's int8 GEMM work over their summed launch times (each
-        # launch bracketed by CUDA events in a profiled step), against the measured dense f16/bf16 rate (the
-        # tensor path they run on; sm_103a has no integer MMA kind)
+        # launch bracketed by CUDA events in a profiled serial step), against the measured dense f16/bf16 rate
+        # (the tensor path they run on; sm_103a has no integer MMA kind)
         "gemm_roofline": {"bound": "tensor", "achieved": gemm_ops / (class_ms["gemm"] / 1000.0) / 1e12,
-                          "peak": peak_for("tensor", peaks)[0], "unit": "TFLOP/s",
-                          "frac": gemm_ops / (class_ms["gemm"] / 1000.0) / 1e12 / peak_for("tensor", peaks)[0]},
+                          "peak": tensor_peak, "unit": "TFLOP/s",
+                          "frac": gemm_ops / (class_ms["gemm"] / 1000.0) / 1e12 / tensor_peak},
         "kernel_ms_per_step": {k: v for k, v in class_ms.items()},  # serial profiled steps
         "weight_bytes_read_per_step": weight_bytes_read(cfg, P, chunk),
         "weight_bytes_naive_per_step": layer_weight_bytes(cfg) * cfg.n_layers * P + cfg.vocab * cfg.dim + 4 * cfg.vocab,
@@ -420,6 +599,12 @@ def run_ours(args, cfg, world, rank, local, pg):
                                 "sample": f"oracle prefill of the first {args.cpu_sample_tokens} tokens of the prompt "
                                           f"in one chunk ({dt:.1f} s)"}
     g.close()
+    if rank == 0 and world == 1 and args.workload == "8b" and not args.no_configs:
+        # the other measured configurations, each on its own (not part of `value`)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["configs"] = run_small_configs(args, peaks)
+        line["streamed"] = run_streamed_config(args, model, cfg)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -609,6 +794,8 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--ref-sample-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the 350M, 1B and streamed measurements that follow the 8B line")
     ap.add_argument("--overlap", type=int, default=1,
                     help="1 (default): consecutive chunks on eight streams (pp_set_chunk_overlap); 0: serial")
     ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention | quant | norm_quant")

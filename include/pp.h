@@ -138,6 +138,9 @@ typedef struct pp_stats {
   int64_t prof_launches;      /* launches of the profiled kernel class */
   double prof_ms;             /* summed event-timed duration of those launches */
   int64_t kv_bytes;           /* device memory backing the K/V cache now (a level, not a counter) */
+  int64_t gemm_launches[5][3]; /* tcgen05 projection GEMM launches by [epilogue][tile width]: epilogue 0 store,
+                                  1 residual add, 2 SwiGLU, 3 raw int32, 4 QKV with RoPE and the K/V write;
+                                  tile width (weight rows per CTA pair) 256, 192, 128 */
 } pp_stats;
 
 typedef struct pp_model pp_model;
@@ -213,9 +216,9 @@ int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
  * the layer's copy, and the ring slot is released after all of them). Results
  * are bit-identical to the serial order. The first call that turns it on
  * allocates seven more scratch sets and streams (PP_ERR_OOM if that fails)
- * after waiting for the model's work. Ignored while a trace or the per-layer
- * profile is on, for calls of a single chunk, and for streamed weights in
- * chunk-outer order. */
+ * after waiting for the model's work. Ignored while the per-layer profile is
+ * on, for calls of a single chunk, and for streamed weights in chunk-outer
+ * order. */
 int pp_set_chunk_overlap(pp_model* m, int32_t enable);
 
 /* Per-layer stage profile ("Single-pass prefill", the per-layer profiler of
@@ -326,6 +329,27 @@ int pp_debug_loader_fault(pp_model* m, int32_t fault);
  * that would pass it fails with PP_ERR_OOM and leaks nothing. */
 int pp_debug_alloc_cap(int64_t bytes);
 
+/* Status of the single-step GEMM calls on the tcgen05 engine (pp_op_gemm,
+ * pp_op_gemm_acc, pp_op_gemm_noalloc) on the current device. Every mbarrier
+ * wait inside those kernels is bounded; when one runs out the kernel records
+ * it in a device status word that all these calls share, lets its copies land
+ * and exits early, leaving its output incomplete. This call waits for `stream`
+ * (cudaStream_t; NULL = legacy default stream), then returns PP_OK, or
+ * PP_ERR_DEVICE_TIMEOUT (and clears the word) if any such call timed out since
+ * the last query. The word lives in the library's own device memory. */
+int pp_op_status(void* stream);
+
+/* Test hook: from now on every single-step tcgen05 GEMM call holds back its MMA
+ * issuer and bounds each mbarrier wait by wait_us microseconds, so every call
+ * times out on purpose (pp_op_status then reports PP_ERR_DEVICE_TIMEOUT) without
+ * faulting or hanging the GPU; wait_us = 0 restores normal calls. Process-wide.
+ * Errors: PP_ERR_ARG (wait_us < 0). */
+int pp_debug_op_stall(int32_t wait_us);
+
+/* Capacity of the fixed scratch of pp_op_gemm_noalloc, per device. */
+#define PP_NOALLOC_PART_BYTES (32 * 1024 * 1024) /* partial int32 tiles */
+#define PP_NOALLOC_COUNTERS 4096                 /* per-tile arrival counters */
+
 /* The tcgen05 GEMM of pp_op_gemm (engine PP_GEMM_TC) without any device
  * allocation, for callers that may not allocate device memory while they run
  * (an application whose device memory is all held by its own pool allocator,
@@ -333,20 +357,38 @@ int pp_debug_alloc_cap(int64_t bytes);
  * synchronise the device). The pages have no counterpart: it only changes
  * where the GEMM's stream-K scratch lives.
  * The scratch (partial int32 tiles of GEMMs with few output tiles and long K,
- * and their arrival counters) is a fixed array inside the library: 32 MiB plus
- * 4096 counters, placed on every device that loads the library's device code
- * and kept until the process exits. Shapes whose plan needs more fail with
- * PP_ERR_ARG and a message naming both sizes (e.g. m = 1024, n = 4096,
- * k = 14336); shapes that need no scratch always run.
+ * and their arrival counters) is a fixed array inside the library:
+ * PP_NOALLOC_PART_BYTES plus PP_NOALLOC_COUNTERS counters, placed on every
+ * device that loads the library's device code and kept until the process
+ * exits, whether or not this function is ever called. It is not counted by
+ * pp_debug_alloc_cap nor in any model's memory figures. Shapes whose plan needs
+ * more (pp_op_gemm_noalloc_need; e.g. m = 1024, n = 4096, k = 14336 on a GB300)
+ * fail with PP_ERR_ARG and a message naming both sizes; shapes that need no
+ * scratch always run.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for the life of the process, so make that
+ * first call before any stream capture, and do not reset the device
+ * (cudaDeviceReset) after it.
  * All calls on a device share its one array, which keeps the last call's
  * contents (the counters are cleared on `stream` at the start of every call):
  * calls on the same device whose executions overlap, for example on two
- * streams, race and give wrong results. Arguments and errors as pp_op_gemm,
- * with a16, w and w_scale 16-byte aligned. */
+ * streams, race and give wrong results. A bounded wait that runs out is
+ * reported by pp_op_status. Arguments and errors as pp_op_gemm, with a16, w and
+ * w_scale 16-byte aligned. */
 int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, const float* w_scale,
                        const float* a_scale, int32_t m, int32_t n, int32_t k, float* out, int32_t ldo, void* stream);
+
+/* Scratch that pp_op_gemm_noalloc (and pp_op_gemm on the tcgen05 engine) plans
+ * for an m x n x k GEMM on the current device: partial-tile bytes and counters
+ * (both 0 when it runs whole tiles; the plan depends on the device's SM count).
+ * Errors: PP_ERR_ARG (k % 64, n % 128), PP_ERR_UNSUPPORTED (no sm_103 device). */
+int pp_op_gemm_noalloc_need(int32_t m, int32_t n, int32_t k, int64_t* part_bytes, int64_t* counters);
+
+/* Test hook: set every arrival counter of the fixed scratch on the current
+ * device to `value` (synchronous), as a call that gave up part of the way would
+ * leave them. pp_op_gemm_noalloc clears what it uses, so its results do not
+ * change. */
+int pp_debug_noalloc_poison(int32_t value);
 
 /* RoPE + K/V write for `rows` positions start_pos..: qkv [rows][(H+2Hkv)*hd]
  * f32 (q heads, then k heads, then v heads) -> q_out [rows][H][hd] rotated,

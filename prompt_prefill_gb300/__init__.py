@@ -30,6 +30,10 @@ PP_GEMM_AUTO, PP_GEMM_MMA, PP_GEMM_TC = 0, 1, 2
 PP_KERNEL_COUNT = 6
 KERNEL_NAMES = {0: "gemm", 1: "attention", 2: "norm_quant", 3: "rope_kv", 4: "lm_head", 5: "embed"}
 PP_EPI_STORE, PP_EPI_RESID, PP_EPI_SWIGLU = 0, 1, 2
+# epilogue indices of pp_stats.gemm_launches (3: raw int32, 4: QKV with RoPE + K/V write) and its tile widths
+GEMM_EPI_NAMES = {0: "store", 1: "residual", 2: "swiglu", 3: "int32", 4: "rope"}
+GEMM_TILE_WIDTHS = (256, 192, 128)
+PP_NOALLOC_PART_BYTES, PP_NOALLOC_COUNTERS = 32 * 1024 * 1024, 4096
 
 
 class PPError(RuntimeError):
@@ -56,10 +60,14 @@ class pp_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("calls", "chunks", "tokens", "weight_bytes_read", "h2d_bytes",
                                                "prefetch_hits", "prefetch_misses", "kernel_launches",
                                                "prof_launches")] + [("prof_ms", ctypes.c_double),
-                                                                    ("kv_bytes", ctypes.c_int64)]
+                                                                    ("kv_bytes", ctypes.c_int64),
+                                                                    ("gemm_launches", (ctypes.c_int64 * 3) * 5)]
 
     def as_dict(self) -> dict:
-        return {n: getattr(self, n) for n, _ in self._fields_}
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["gemm_launches"] = {(e, GEMM_TILE_WIDTHS[b]): int(self.gemm_launches[e][b])
+                              for e in range(5) for b in range(3) if self.gemm_launches[e][b]}
+        return d
 
 
 class pp_layer_profile(ctypes.Structure):
@@ -101,6 +109,11 @@ SIGNATURES = {
     "pp_debug_gemm_stall": ([_i32, _vp, _vp, _i32, _i32, _i32, _vp], ctypes.c_int),
     "pp_debug_loader_fault": ([_vp, _i32], ctypes.c_int),
     "pp_debug_alloc_cap": ([ctypes.c_int64], ctypes.c_int),
+    "pp_op_status": ([_vp], ctypes.c_int),
+    "pp_debug_op_stall": ([_i32], ctypes.c_int),
+    "pp_op_gemm_noalloc_need": ([_i32, _i32, _i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)],
+                                ctypes.c_int),
+    "pp_debug_noalloc_poison": ([_i32], ctypes.c_int),
 }
 
 _lock = threading.Lock()
@@ -311,6 +324,26 @@ def pp_op_gemm_noalloc(epilogue, a16, w, w_scale, a_scale, m, n, k, out, ldo, st
     inside the library; see include/pp.h for the size limit and sharing rules)."""
     _check(lib().pp_op_gemm_noalloc(epilogue, _ptr(a16), _ptr(w), _ptr(w_scale), _ptr(a_scale), m, n, k, _ptr(out),
                                     ldo, _stream(stream)), "pp_op_gemm_noalloc")
+
+
+def pp_op_status(stream=None) -> int:
+    """Status of the single-step tcgen05 GEMM calls since the last query (waits for the stream)."""
+    return int(lib().pp_op_status(_stream(stream)))
+
+
+def pp_debug_op_stall(wait_us: int):
+    _check(lib().pp_debug_op_stall(wait_us), "pp_debug_op_stall")
+
+
+def pp_op_gemm_noalloc_need(m: int, n: int, k: int) -> tuple[int, int]:
+    """(partial-tile bytes, counters) the tcgen05 GEMM plans for this shape on the current device."""
+    pb, cc = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().pp_op_gemm_noalloc_need(m, n, k, ctypes.byref(pb), ctypes.byref(cc)), "pp_op_gemm_noalloc_need")
+    return pb.value, cc.value
+
+
+def pp_debug_noalloc_poison(value: int):
+    _check(lib().pp_debug_noalloc_poison(value), "pp_debug_noalloc_poison")
 
 
 def pp_set_exact_segment(seg_k: int):

@@ -91,6 +91,7 @@ struct TcParams {
   TcRope rope;            // EPI_ROPE destinations
   long long wait_cycles;  // bound of every mbarrier wait (clock64 cycles)
   int hold_mma;           // test hook: the MMA issuer issues nothing, so every other role's wait runs out
+  int early_w;            // the first stages' weight loads may precede griddepcontrol.wait
 };
 
 // The units (tile, k-block range) a cluster works on, in order.
@@ -277,10 +278,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
   // The prologue above overlaps the previous kernel's tail; its results are read
-  // from here on. The producer first issues the weight loads of the stages it
-  // can fill without waiting (no kernel of the stream writes the weights; a
-  // streamed layer's copy is waited for before the layer's first kernel) and
-  // only then waits.
+  // from here on. With early_w the producer first issues the weight loads of the
+  // stages it can fill without waiting (the model's weights, which no kernel of
+  // the stream writes; a streamed layer's ring slot is waited for by a plain
+  // stream-ordered launch before the layer's first kernel) and only then waits.
   ppdev::pdl_trigger();
   if (warp != 0) ppdev::pdl_wait();
 
@@ -299,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const Sched sc(p, cluster, n_clusters);
       // weights of the first STAGES k-blocks (every stage starts empty), then the wait
       int pre = 0;
-      for (int u = 0; u < sc.units() && pre < STAGES; ++u) {
+      for (int u = 0; p.early_w && u < sc.units() && pre < STAGES; ++u) {
         int t, kb0, kb1;
         sc.unit(u, t, kb0, kb1);
         const int n_row = (t / p.num_m_tiles) * BN + (int)rank * (BN / 2);
@@ -729,7 +730,8 @@ int max_clusters() {
 }
 
 template <int EPI, int BN>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters, cudaStream_t s,
+                     bool pdl) {
   using C = Cfg<BN>;
   static bool attr = false;
   if (!attr) {
@@ -737,15 +739,15 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParam
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(k_gemm_tc<EPI, BN>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, ma, mw, p);
+  return launch_pdl_if(pdl, k_gemm_tc<EPI, BN>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, ma, mw, p);
 }
 
 template <int EPI>
 cudaError_t launch_bn(int bn, const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters,
-                      cudaStream_t s) {
-  if (bn == 256) return launch_t<EPI, 256>(ma, mw, p, clusters, s);
-  if (bn == 192) return launch_t<EPI, 192>(ma, mw, p, clusters, s);
-  if (bn == 128) return launch_t<EPI, 128>(ma, mw, p, clusters, s);
+                      cudaStream_t s, bool pdl) {
+  if (bn == 256) return launch_t<EPI, 256>(ma, mw, p, clusters, s, pdl);
+  if (bn == 192) return launch_t<EPI, 192>(ma, mw, p, clusters, s, pdl);
+  if (bn == 128) return launch_t<EPI, 128>(ma, mw, p, clusters, s, pdl);
   return cudaErrorInvalidValue;
 }
 
@@ -868,8 +870,9 @@ void tc_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
                            int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits,
-                           const TcRope& rope, bool wide) {
+                           const TcRope& rope, bool wide, bool pdl, bool early_w) {
   TcParams p{};
+  p.early_w = early_w ? 1 : 0;
   p.wait_cycles = waits.cycles;
   p.hold_mma = waits.hold_mma;
   p.M = m;
@@ -897,15 +900,15 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
     pl.clusters = std::min(pl.num_tiles, max_clusters());  // no workspace: whole tiles
   }
   switch (epi) {
-    case EPI_STORE: return launch_bn<EPI_STORE>(bn, ma, mw, p, pl.clusters, s);
-    case EPI_RESID: return launch_bn<EPI_RESID>(bn, ma, mw, p, pl.clusters, s);
-    case EPI_SWIGLU: return launch_bn<EPI_SWIGLU>(bn, ma, mw, p, pl.clusters, s);
-    case EPI_ACC: return launch_bn<EPI_ACC>(bn, ma, mw, p, pl.clusters, s);
+    case EPI_STORE: return launch_bn<EPI_STORE>(bn, ma, mw, p, pl.clusters, s, pdl);
+    case EPI_RESID: return launch_bn<EPI_RESID>(bn, ma, mw, p, pl.clusters, s, pdl);
+    case EPI_SWIGLU: return launch_bn<EPI_SWIGLU>(bn, ma, mw, p, pl.clusters, s, pdl);
+    case EPI_ACC: return launch_bn<EPI_ACC>(bn, ma, mw, p, pl.clusters, s, pdl);
     case EPI_ROPE:
       if (!rope.table || !rope.q_out || !rope.k_cache || !rope.v_cache || rope.hd % 16 ||
           n != (rope.H + 2 * rope.Hkv) * rope.hd)
         return cudaErrorInvalidValue;
-      return launch_bn<EPI_ROPE>(bn, ma, mw, p, pl.clusters, s);
+      return launch_bn<EPI_ROPE>(bn, ma, mw, p, pl.clusters, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

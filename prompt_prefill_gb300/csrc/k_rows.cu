@@ -237,15 +237,17 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab, int dim, float* x, int* status,
-                         cudaStream_t s) {
-  return launch_pdl(k_embed, dim3(n), dim3(kRowThreads), 0, s, tok, emb, vocab, dim, x, status);
+                         cudaStream_t s, bool pdl) {
+  return launch_pdl_if(pdl, k_embed, dim3(n), dim3(kRowThreads), 0, s, tok, emb, vocab, dim, x, status);
 }
 
 cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
-                              int8_t* q8, __half* q16, float* a_scale, cudaStream_t s) {
+                              int8_t* q8, __half* q16, float* a_scale, cudaStream_t s, bool pdl) {
   const int nv = (k / 4 + kRowThreads - 1) / kRowThreads;  // float4 per thread
   cudaError_t e = cudaSuccess;
-  auto go = [&](auto kern) { e = launch_pdl(kern, dim3(rows), dim3(kRowThreads), 0, s, x, ldx, g, k, eps, y, q8, q16, a_scale); };
+  auto go = [&](auto kern) {
+    e = launch_pdl_if(pdl, kern, dim3(rows), dim3(kRowThreads), 0, s, x, ldx, g, k, eps, y, q8, q16, a_scale);
+  };
   if (g) {
     if (nv <= 4) go(k_norm_quant<true, 4>);
     else if (nv <= 16) go(k_norm_quant<true, 16>);
@@ -264,15 +266,15 @@ cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cu
 }
 
 cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
-                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s, bool paired) {
-  return launch_pdl(paired ? k_rope_kv<true> : k_rope_kv<false>, dim3(rows), dim3(kRowThreads), 0, s, qkv, start_pos,
+                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s, bool paired, bool pdl) {
+  return launch_pdl_if(pdl, paired ? k_rope_kv<true> : k_rope_kv<false>, dim3(rows), dim3(kRowThreads), 0, s, qkv, start_pos,
                     H, Hkv, hd, reinterpret_cast<const float2*>(table), q_out, k_cache, v_cache);
 }
 
 cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,
-                           int dim, float* logits, cudaStream_t s) {
+                           int dim, float* logits, cudaStream_t s, bool pdl) {
   const int blocks = sm_count() * 4;
-  return launch_pdl(k_lm_head, dim3(blocks), dim3(kRowThreads), (size_t)dim, s, q8, a_scale, w, ws, vocab, dim, logits);
+  return launch_pdl_if(pdl, k_lm_head, dim3(blocks), dim3(kRowThreads), (size_t)dim, s, q8, a_scale, w, ws, vocab, dim, logits);
 }
 
 }  // namespace pp

@@ -231,6 +231,8 @@ struct pp_model {
   std::vector<LayerVisitEv> lprof_pending;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> copy_ev;  // copy start/end of each visit of the current call
   std::vector<void*> allocations;
+  // streams whose next kernel follows a wait on another stream's event (wait_event)
+  std::vector<cudaStream_t> plain_next;
 };
 
 namespace {
@@ -301,16 +303,34 @@ int collect(pp_model* m) {
   return PP_OK;
 }
 
+// Make `st` wait for event `e` recorded on another stream. The next kernel
+// launched on `st` is then launched plainly stream-ordered, without
+// programmatic early start: every cross-stream dependency (a streamed layer's
+// copy into its ring slot, earlier chunks' K/V rows, the previous call on
+// another stream) holds by plain stream order, whatever a kernel reads before
+// its griddepcontrol.wait (the GEMM producer's first weight loads).
+int wait_event(pp_model* m, cudaStream_t st, cudaEvent_t e) {
+  PP_CUDA(cudaStreamWaitEvent(st, e, 0));
+  if (std::find(m->plain_next.begin(), m->plain_next.end(), st) == m->plain_next.end()) m->plain_next.push_back(st);
+  return PP_OK;
+}
+
+// Launch one kernel through fn(pdl) on stream st, counting it and, when its
+// class is profiled, bracketing it with CUDA events. pdl is false for the
+// first kernel after a wait_event on st.
 template <class F>
 int launch(pp_model* m, int cls, cudaStream_t st, F&& fn) {
   const bool prof = m->cfg.profile_kernel == cls;
+  auto it = std::find(m->plain_next.begin(), m->plain_next.end(), st);
+  const bool pdl = it == m->plain_next.end();
+  if (!pdl) m->plain_next.erase(it);
   EventPair p{};
   if (prof) {
     PP_TRY(ev_get(m, &p.a));
     PP_TRY(ev_get(m, &p.b));
     PP_CUDA(cudaEventRecord(p.a, st));
   }
-  cudaError_t e = fn();
+  cudaError_t e = fn(pdl);
   if (e != cudaSuccess) {
     set_err("kernel launch (class %d) failed: %s", cls, cudaGetErrorString(e));
     return PP_ERR_CUDA;
@@ -333,14 +353,15 @@ int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* 
          int K, float* out, int ldo, const TcRope& rope = TcRope{}) {
   if (m->engine == PP_GEMM_TC) {
     const int bi = tc_bn_index(M, N, K, m->gemm_wide);
+    m->stats.gemm_launches[epi][bi] += 1;
     const CUtensorMap& wm = m->wmap[((size_t)mg * 4 + which) * 3 + bi];
     const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
-    return launch(m, PP_KERNEL_GEMM, st, [&] {
+    return launch(m, PP_KERNEL_GEMM, st, [&](bool pdl) {
       return launch_gemm_tc(epi, am, wm, kTcBn[bi], ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
-                            st, TcWaits{}, rope, m->gemm_wide);
+                            st, TcWaits{}, rope, m->gemm_wide, pdl, /*early_w=*/true);
     });
   }
-  return launch(m, PP_KERNEL_GEMM, st, [&] {
+  return launch(m, PP_KERNEL_GEMM, st, [&](bool) {  // plain launches
     return launch_gemm_mma(epi, m->a8, w, ws, m->as, M, N, K, out, ldo, nullptr, st);
   });
 }
@@ -665,7 +686,7 @@ int stream_layer(pp_model* m, cudaStream_t st, int v, int n_visits, const uint8_
   PP_CUDA(cudaEventRecord(hp.a, m->copy_stream));  // copy of visit v done
   PP_CUDA(cudaEventRecord(hp.b, st));              // the compute stream reached layer v
   const int slot = v % S;
-  PP_CUDA(cudaStreamWaitEvent(st, m->ring_ready[slot], 0));
+  PP_TRY(wait_event(m, st, m->ring_ready[slot]));
   if (prefetch && v + 1 < n_visits) PP_TRY(issue_copy(v + 1));
   m->prefetch_pending.push_back(hp);
   m->prefetch_layer.push_back(v % c.n_layers);
@@ -708,8 +729,8 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
   float* kcl = m->kc + kvl * l;
   float* vcl = m->vc + kvl * l;
   // attention block
-  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(x, D, L.attn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs);
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&](bool pdl) {
+    return launch_norm_quant(x, D, L.attn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs, pdl);
   }));
   PP_TRY(trace_codes(m, cs, l, 0, pos0, C, D));
   if (m->engine == PP_GEMM_TC) {
@@ -726,31 +747,29 @@ int layer_block(pp_model* m, cudaStream_t cs, int l, int mg, const uint8_t* base
     PP_TRY(gemm(m, cs, EPI_ROPE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, nullptr, QKV, rp));
   } else {
     PP_TRY(gemm(m, cs, EPI_STORE, mg, 0, L.sqkv, L.wqkv, C, QKV, D, m->qkv, QKV));
-    PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&] {
-      return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs, true);
+    PP_TRY(launch(m, PP_KERNEL_ROPE_KV, cs, [&](bool pdl) {
+      return launch_rope_kv(m->qkv, C, pos0, H, Hkv, hd, m->rope, m->qr, kcl, vcl, cs, true, pdl);
     }));
   }
-  if (kv_wait) PP_CUDA(cudaStreamWaitEvent(cs, kv_wait, 0));
+  if (kv_wait) PP_TRY(wait_event(m, cs, kv_wait));
   if (kv_done) PP_CUDA(cudaEventRecord(kv_done, cs));
-  PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&] {
-    // after another stream's event the launch is plainly stream-ordered
-    return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs,
-                            kv_wait == nullptr);
+  PP_TRY(launch(m, PP_KERNEL_ATTENTION, cs, [&](bool pdl) {
+    return launch_attention(m->qr, kcl, vcl, C, pos0, H, Hkv, hd, m->o, m->attn_part, m->attn_part_bytes, cs, pdl);
   }));
   if (attention_workspace_bytes(C, pos0, H, Hkv, hd)) m->stats.kernel_launches += 1;  // the range merge
-  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, q8, q16, m->as, cs);
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&](bool pdl) {
+    return launch_norm_quant(m->o, QD, nullptr, C, QD, 0.f, nullptr, q8, q16, m->as, cs, pdl);
   }));
   PP_TRY(trace_codes(m, cs, l, 1, pos0, C, QD));
   PP_TRY(gemm(m, cs, EPI_RESID, mg, 1, L.so, L.wo, C, D, QD, x, D));
   // FFN block
-  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs);
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&](bool pdl) {
+    return launch_norm_quant(x, D, L.ffn_norm, C, D, c.rms_eps, nullptr, q8, q16, m->as, cs, pdl);
   }));
   PP_TRY(trace_codes(m, cs, l, 2, pos0, C, D));
   PP_TRY(gemm(m, cs, EPI_SWIGLU, mg, 2, L.sgu, L.wgu, C, 2 * F, D, m->h, F));
-  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, q8, q16, m->as, cs);
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&](bool pdl) {
+    return launch_norm_quant(m->h, F, nullptr, C, F, 0.f, nullptr, q8, q16, m->as, cs, pdl);
   }));
   PP_TRY(trace_codes(m, cs, l, 3, pos0, C, F));
   PP_TRY(gemm(m, cs, EPI_RESID, mg, 3, L.sd, L.wd, C, D, F, x, D));
@@ -774,11 +793,11 @@ int head(pp_model* m, cudaStream_t cs, const float* xlast, float* d_logits) {
   const pp_config& c = m->cfg;
   const int D = c.dim;
   __half* q16 = m->engine == PP_GEMM_TC ? m->a16 : nullptr;
-  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&] {
-    return launch_norm_quant(xlast, D, m->final_norm, 1, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs);
+  PP_TRY(launch(m, PP_KERNEL_NORM_QUANT, cs, [&](bool pdl) {
+    return launch_norm_quant(xlast, D, m->final_norm, 1, D, c.rms_eps, nullptr, m->a8, q16, m->as, cs, pdl);
   }));
-  PP_TRY(launch(m, PP_KERNEL_LM_HEAD, cs, [&] {
-    return launch_lm_head(m->a8, m->as, m->w_out, m->s_out, c.vocab, D, d_logits, cs);
+  PP_TRY(launch(m, PP_KERNEL_LM_HEAD, cs, [&](bool pdl) {
+    return launch_lm_head(m->a8, m->as, m->w_out, m->s_out, c.vocab, D, d_logits, cs, pdl);
   }));
   return PP_OK;
 }
@@ -810,13 +829,13 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   }
   // The model's scratch, K/V cache and ring are shared by every call: order
   // this call after the previous one, whichever stream that one ran on.
-  PP_CUDA(cudaStreamWaitEvent(st, m->done, 0));
+  PP_TRY(wait_event(m, st, m->done));
   if (streamed && st != m->stream) {
     // keep the ring's events on one compute stream
     cudaEvent_t e;
     PP_TRY(ev_get(m, &e));
     PP_CUDA(cudaEventRecord(e, st));
-    PP_CUDA(cudaStreamWaitEvent(m->stream, e, 0));
+    PP_TRY(wait_event(m, m->stream, e));
     m->ev_pool.push_back(e);
   }
   cudaStream_t cs = streamed ? m->stream : st;
@@ -843,7 +862,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     m->lprof_pending.push_back(e);
     return PP_OK;
   };
-  const bool overlap = m->overlap && !streamed && !layer_outer && !m->trace && !m->layer_prof && n > chunk;
+  const bool overlap = m->overlap && !streamed && !layer_outer && !m->layer_prof && n > chunk;
   if (overlap) {
     // "Batched Prefill" with consecutive chunks on NS streams: chunk k runs on
     // stream k % NS with scratch set k % NS and waits, layer by layer, for the
@@ -860,7 +879,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     PP_CUDA(cudaEventRecord(e, cs));
     for (int i = 1; i < NS; ++i) {
       S[i] = m->ostream[i - 1];
-      PP_CUDA(cudaStreamWaitEvent(S[i], e, 0));
+      PP_TRY(wait_event(m, S[i], e));
     }
     m->ev_pool.push_back(e);
     int rc = PP_OK, k = 0;
@@ -873,12 +892,20 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
       cudaStream_t sk = S[p];
       const int C = std::min(chunk, n - c0);
       const int pos0 = start_pos + c0;
-      rc = launch(m, PP_KERNEL_EMBED, sk, [&] {
-        return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, sk);
+      rc = launch(m, PP_KERNEL_EMBED, sk, [&](bool pdl) {
+        return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, sk, pdl);
       });
       for (int l = 0; l < c.n_layers && rc == PP_OK; ++l)
         rc = layer_block(m, sk, l, l, m->d_layers + m->lay.bytes * l, m->x, C, pos0, m->qkv_ev[p][l],
                          k > 0 ? m->qkv_ev[prev][l] : nullptr);
+      if (rc == PP_OK && m->trace) {  // the chunk's rows leaving the last layer (disjoint per chunk)
+        const cudaError_t e = cudaMemcpyAsync(m->trace + ((size_t)c.n_layers * m->trace_pos + pos0) * D, m->x,
+                                              sizeof(float) * C * D, cudaMemcpyDeviceToDevice, sk);
+        if (e != cudaSuccess) {
+          set_err("trace copy failed: %s", cudaGetErrorString(e));
+          rc = PP_ERR_CUDA;
+        }
+      }
       if (rc == PP_OK && c0 + C == n) rc = head(m, sk, m->x + (size_t)(C - 1) * D, d_logits);
     }
     use_scratch(m, 0);  // set 0 is the model's between calls
@@ -888,7 +915,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     for (int i = 1; i < NS; ++i) {
       PP_TRY(ev_get(m, &e));
       PP_CUDA(cudaEventRecord(e, S[i]));
-      PP_CUDA(cudaStreamWaitEvent(cs, e, 0));
+      PP_TRY(wait_event(m, cs, e));
       m->ev_pool.push_back(e);
     }
     PP_TRY(rc);
@@ -898,7 +925,9 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     for (int c0 = 0; c0 < n; c0 += chunk) {
       const int C = std::min(chunk, n - c0);
       const int pos0 = start_pos + c0;
-      PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, cs); }));
+      PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&](bool pdl) {
+        return launch_embed(d_tok + c0, C, m->emb, c.vocab, D, m->x, m->status, cs, pdl);
+      }));
       for (int l = 0; l < c.n_layers; ++l, ++visit) {
         const uint8_t* base;
         int mg;
@@ -921,7 +950,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     // order (their residual rows are disjoint slices of set 0's m->x); with
     // streamed weights every stream waits for the layer's copy and the ring
     // slot is freed only after every stream's work on the layer.
-    const bool ovl = m->overlap && !m->trace && !m->layer_prof && n > chunk;
+    const bool ovl = m->overlap && !m->layer_prof && n > chunk;
     constexpr int NS = pp_model::kOverlap;
     cudaStream_t S[NS];
     S[0] = cs;
@@ -931,12 +960,14 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
         cudaEvent_t e;
         PP_TRY(ev_get(m, &e));
         PP_CUDA(cudaEventRecord(e, out ? cs : S[i]));
-        PP_CUDA(cudaStreamWaitEvent(out ? S[i] : cs, e, 0));
+        PP_TRY(wait_event(m, out ? S[i] : cs, e));
         m->ev_pool.push_back(e);
       }
       return PP_OK;
     };
-    PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&] { return launch_embed(d_tok, n, m->emb, c.vocab, D, m->x, m->status, cs); }));
+    PP_TRY(launch(m, PP_KERNEL_EMBED, cs, [&](bool pdl) {
+      return launch_embed(d_tok, n, m->emb, c.vocab, D, m->x, m->status, cs, pdl);
+    }));
     float* const x0 = m->x;
     if (ovl) {
       PP_TRY(fan(true));
@@ -977,7 +1008,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     cudaEvent_t e;
     PP_TRY(ev_get(m, &e));
     PP_CUDA(cudaEventRecord(e, m->stream));
-    PP_CUDA(cudaStreamWaitEvent(st, e, 0));
+    PP_TRY(wait_event(m, st, e));
     m->ev_pool.push_back(e);
   }
   PP_CUDA(cudaEventRecord(m->done, st));
@@ -1273,8 +1304,80 @@ static int check_gemm(int32_t engine, const int8_t* a8, const uint16_t* a16, con
 }
 
 
-// Process-wide stream-K workspace of the single-step GEMM entry points, grown
-// on demand (growing synchronises the device) and kept until exit.
+// ---------------------------------------------------------------------------
+// Device-side state of the single-step GEMM entry points that lives in this
+// library's own device memory: the status word their bounded waits report to,
+// and the fixed stream-K scratch of pp_op_gemm_noalloc (for callers that may
+// not allocate device memory while they run: for example a host application
+// that has already handed all device memory to its own pool allocator, or a
+// latency-critical loop where cudaMalloc/cudaFree would block or synchronise
+// the device). The CUDA runtime places these arrays on each device when the
+// library's device code is loaded there; they stay until the process exits.
+namespace {
+constexpr size_t kStaticPartBytes = PP_NOALLOC_PART_BYTES;  // partial int32 tiles
+constexpr int kStaticCounters = PP_NOALLOC_COUNTERS;        // per-tile arrival counters
+static_assert(kStaticPartBytes % 256 == 0, "whole 256-byte lines");
+static __device__ __align__(256) int32_t g_static_part[kStaticPartBytes / sizeof(int32_t)];
+static __device__ __align__(256) int g_static_cnt[kStaticCounters];
+static __device__ int g_op_status;  // DEV_OK or DEV_TIMEOUT, shared by every single-step GEMM call
+
+struct StaticScratch {
+  bool ready = false;
+  int32_t* part = nullptr;
+  int* cnt = nullptr;
+  int* status = nullptr;
+};
+std::mutex g_static_mu;
+StaticScratch g_static_dev[128];  // by device ordinal
+
+// Device addresses of the arrays above on the current device. In host code the
+// arrays' names stand for host-side shadows, not device addresses, so every
+// pointer handed to a kernel comes from cudaGetSymbolAddress, looked up once per
+// device (with that device current) on its first single-step GEMM call.
+int static_scratch(StaticScratch* out) {
+  int dev = 0;
+  PP_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 128) {
+    set_err("device ordinal %d out of range", dev);
+    return PP_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticScratch& sc = g_static_dev[dev];
+  if (!sc.ready) {
+    void* part = nullptr;
+    void* cnt = nullptr;
+    void* st = nullptr;
+    PP_CUDA(cudaGetSymbolAddress(&part, g_static_part));
+    PP_CUDA(cudaGetSymbolAddress(&cnt, g_static_cnt));
+    PP_CUDA(cudaGetSymbolAddress(&st, g_op_status));
+    sc.part = static_cast<int32_t*>(part);
+    sc.cnt = static_cast<int*>(cnt);
+    sc.status = static_cast<int*>(st);
+    sc.ready = true;
+  }
+  *out = sc;
+  return PP_OK;
+}
+
+// Bounded waits of the single-step tcgen05 GEMMs (pp_debug_op_stall).
+std::atomic<long long> g_op_wait_us{0};
+
+TcWaits op_waits() {
+  TcWaits w;
+  const long long us = g_op_wait_us.load();
+  if (us > 0) {
+    int dev = 0, khz = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+    w.cycles = us * (khz > 0 ? khz : 2000000) / 1000;  // kHz -> cycles per microsecond
+    w.hold_mma = 1;
+  }
+  return w;
+}
+}  // namespace
+
+// Process-wide stream-K workspace of pp_op_gemm / pp_op_gemm_acc, grown on
+// demand (growing synchronises the device) and kept until exit.
 static std::mutex g_op_ws_mu;
 static TcWorkspace g_op_ws;
 
@@ -1300,29 +1403,31 @@ static cudaError_t op_workspace(int m, int n, int k, TcWorkspace* out) {
   return cudaSuccess;
 }
 
-static cudaError_t op_gemm_launch(int32_t engine, int epi, const int8_t* a8, const uint16_t* a16, const int8_t* w,
-                                  const float* ws, const float* as, int m, int n, int k, float* out, int ldo,
-                                  int32_t* acc, cudaStream_t st) {
-  if (engine == PP_GEMM_MMA) return launch_gemm_mma(epi, a8, w, ws, as, m, n, k, out, ldo, acc, st);
+static int op_gemm_launch(int32_t engine, int epi, const int8_t* a8, const uint16_t* a16, const int8_t* w,
+                          const float* ws, const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc,
+                          cudaStream_t st) {
+  if (engine == PP_GEMM_MMA) return ok_launch(launch_gemm_mma(epi, a8, w, ws, as, m, n, k, out, ldo, acc, st), "gemm");
+  StaticScratch sc;
+  PP_TRY(static_scratch(&sc));
   CUtensorMap ma, mw;
-  cudaError_t e = make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k);
-  if (e != cudaSuccess) return e;
+  PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
   const int bn = tc_bn(m, n, k);
-  e = make_tmap_w(&mw, w, n, k, bn);
-  if (e != cudaSuccess) return e;
+  PP_CUDA(make_tmap_w(&mw, w, n, k, bn));
   TcWorkspace wsp;
-  e = op_workspace(m, n, k, &wsp);
-  if (e != cudaSuccess) return e;
-  return launch_gemm_tc(epi, ma, mw, bn, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), nullptr, wsp, st);
+  PP_CUDA(op_workspace(m, n, k, &wsp));
+  // programmatic early start, but no weight load before griddepcontrol.wait:
+  // a caller's kernel may have written w just before this call
+  return ok_launch(launch_gemm_tc(epi, ma, mw, bn, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), sc.status, wsp,
+                                  st, op_waits(), TcRope{}, false, true, /*early_w=*/false),
+                   "gemm");
 }
 
 int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
                    int32_t k, int32_t* acc, void* stream) {
   PP_TRY(check_gemm(engine, a8, a16, w, m, n, k));
   if (!acc) { set_err("null acc"); return PP_ERR_ARG; }
-  return ok_launch(op_gemm_launch(engine, EPI_ACC, a8, a16, w, nullptr, nullptr, m, n, k, nullptr, 0, acc,
-                                  static_cast<cudaStream_t>(stream)),
-                   "gemm_acc");
+  return op_gemm_launch(engine, EPI_ACC, a8, a16, w, nullptr, nullptr, m, n, k, nullptr, 0, acc,
+                        static_cast<cudaStream_t>(stream));
 }
 
 int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_t* a16, const int8_t* w,
@@ -1339,56 +1444,53 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
     set_err("bad pp_op_gemm arguments (ldo %% 4, 16-byte aligned out)");
     return PP_ERR_ARG;
   }
-  return ok_launch(op_gemm_launch(engine, epilogue, a8, a16, w, w_scale, a_scale, m, n, k, out, ldo, nullptr,
-                                  static_cast<cudaStream_t>(stream)),
-                   "gemm");
+  return op_gemm_launch(engine, epilogue, a8, a16, w, w_scale, a_scale, m, n, k, out, ldo, nullptr,
+                        static_cast<cudaStream_t>(stream));
 }
 
-// ---------------------------------------------------------------------------
-// The GEMM with its stream-K scratch in this library's own device memory, for
-// callers that may not allocate device memory while they run: for example a
-// host application that has already handed all device memory to its own pool
-// allocator, or a latency-critical loop where cudaMalloc/cudaFree would block
-// or synchronise the device. The scratch is a fixed array that the CUDA runtime
-// places on each device when the library's device code is loaded there; it
-// stays allocated until the process exits.
-namespace {
-constexpr size_t kStaticPartBytes = size_t(32) << 20;  // partial int32 tiles
-constexpr int kStaticCounters = 4096;                   // per-tile arrival counters
-static __device__ __align__(256) int32_t g_static_part[kStaticPartBytes / sizeof(int32_t)];
-static __device__ __align__(256) int g_static_cnt[kStaticCounters];
-
-struct StaticScratch {
-  bool ready = false;
-  int32_t* part = nullptr;
-  int* cnt = nullptr;
-};
-std::mutex g_static_mu;
-StaticScratch g_static_dev[128];  // by device ordinal
-
-// Device addresses of the static arrays on the current device, looked up once.
-int static_scratch(StaticScratch* out) {
-  int dev = 0;
-  PP_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= 128) {
-    set_err("device ordinal %d out of range", dev);
-    return PP_ERR_UNSUPPORTED;
+int pp_op_status(void* stream) {
+  StaticScratch sc;
+  PP_TRY(static_scratch(&sc));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  PP_CUDA(cudaMemcpyAsync(&v, sc.status, sizeof(int), cudaMemcpyDeviceToHost, st));
+  PP_CUDA(cudaStreamSynchronize(st));
+  if (v == DEV_OK) return PP_OK;
+  PP_CUDA(cudaMemsetAsync(sc.status, 0, sizeof(int), st));
+  {
+    // a call that gave up can leave stream-K arrival counters behind
+    std::lock_guard<std::mutex> lk(g_op_ws_mu);
+    if (g_op_ws.cnt) PP_CUDA(cudaMemsetAsync(g_op_ws.cnt, 0, g_op_ws.counters * sizeof(int), st));
   }
-  std::lock_guard<std::mutex> lk(g_static_mu);
-  StaticScratch& sc = g_static_dev[dev];
-  if (!sc.ready) {
-    void* part = nullptr;
-    void* cnt = nullptr;
-    PP_CUDA(cudaGetSymbolAddress(&part, g_static_part));
-    PP_CUDA(cudaGetSymbolAddress(&cnt, g_static_cnt));
-    sc.part = static_cast<int32_t*>(part);
-    sc.cnt = static_cast<int*>(cnt);
-    sc.ready = true;
+  PP_CUDA(cudaStreamSynchronize(st));
+  set_err("a bounded device wait of a single-step GEMM gave up");
+  return PP_ERR_DEVICE_TIMEOUT;
+}
+
+int pp_debug_op_stall(int32_t wait_us) {
+  if (wait_us < 0) {
+    set_err("bad pp_debug_op_stall arguments");
+    return PP_ERR_ARG;
   }
-  *out = sc;
+  g_op_wait_us.store(wait_us);
   return PP_OK;
 }
-}  // namespace
+
+int pp_op_gemm_noalloc_need(int32_t m, int32_t n, int32_t k, int64_t* part_bytes, int64_t* counters) {
+  if (!part_bytes || !counters || m <= 0 || n <= 0 || k <= 0 || k % 64 || n % 128) {
+    set_err("bad pp_op_gemm_noalloc_need arguments (k %% 64, n %% 128)");
+    return PP_ERR_ARG;
+  }
+  if (!tc_available()) {
+    set_err("the tcgen05 engine needs an sm_103 device");
+    return PP_ERR_UNSUPPORTED;
+  }
+  size_t pb = 0, cc = 0;
+  tc_workspace_need(m, n, k, &pb, &cc);
+  *part_bytes = (int64_t)pb;
+  *counters = (int64_t)cc;
+  return PP_OK;
+}
 
 int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, const float* w_scale,
                        const float* a_scale, int32_t m, int32_t n, int32_t k, float* out, int32_t ldo, void* stream) {
@@ -1421,8 +1523,16 @@ int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, c
   wsp.cnt = sc.cnt;
   wsp.counters = kStaticCounters;
   return ok_launch(launch_gemm_tc(epilogue, ma, mw, bn, w_scale, a_scale, m, n, k, out, ldo, nullptr, g_tc_seg.load(),
-                                  nullptr, wsp, st),
+                                  sc.status, wsp, st, op_waits(), TcRope{}, false, true, /*early_w=*/false),
                    "gemm_noalloc");
+}
+
+int pp_debug_noalloc_poison(int32_t value) {
+  StaticScratch sc;
+  PP_TRY(static_scratch(&sc));
+  std::vector<int> v(kStaticCounters, value);
+  PP_CUDA(cudaMemcpy(sc.cnt, v.data(), v.size() * sizeof(int), cudaMemcpyHostToDevice));
+  return PP_OK;
 }
 
 int pp_set_exact_segment(int32_t seg_k) {

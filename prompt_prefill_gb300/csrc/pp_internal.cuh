@@ -23,17 +23,21 @@ enum Epi : int { EPI_STORE = PP_EPI_STORE, EPI_RESID = PP_EPI_RESID, EPI_SWIGLU 
 enum : int { DEV_OK = 0, DEV_BAD_TOKEN = 1, DEV_TIMEOUT = 2 };
 
 // ---- elementwise / row kernels (k_rows.cu)
+// pdl (every launcher below that takes it): allow the launch to start early behind the
+// stream's previous kernel (programmatic dependent launch); false gives a plain
+// stream-ordered launch, for the first kernel after a wait on another stream's event.
 cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab, int dim, float* x, int* status,
-                         cudaStream_t s);
+                         cudaStream_t s, bool pdl = true);
 cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
-                              int8_t* q8, __half* q16, float* a_scale, cudaStream_t s);
+                              int8_t* q8, __half* q16, float* a_scale, cudaStream_t s, bool pdl = true);
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s);
 // paired: the q and k head columns of qkv are in pair order (dims j and j + hd/2 at
 // columns 2j and 2j + 1 of the head), as the model's packed QKV weights produce them.
 cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,
-                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s, bool paired = false);
+                           float* q_out, float* k_cache, float* v_cache, cudaStream_t s, bool paired = false,
+                           bool pdl = true);
 cudaError_t launch_lm_head(const int8_t* q8, const float* a_scale, const int8_t* w, const float* ws, int vocab,
-                           int dim, float* logits, cudaStream_t s);
+                           int dim, float* logits, cudaStream_t s, bool pdl = true);
 
 // ---- GEMMs
 // mma.sync engine (k_gemm_mma.cu): a8 [m][k] int8, w [n][k] int8.
@@ -78,10 +82,16 @@ struct TcRope {
   float* k_cache = nullptr;  // [pos][Hkv][hd]
   float* v_cache = nullptr;  // [pos][Hkv][hd]
 };
+// early_w: the producer may load the first pipeline stages' weights before its
+// griddepcontrol.wait, i.e. while the stream's previous kernel still runs. Only
+// for weights that no kernel of the stream writes (the model's own weight blocks;
+// a streamed layer's ring slot is waited for with a plain launch first); the
+// single-step entry points leave it off, so a caller's kernel that writes w just
+// before the call is always seen.
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw, int bn, const float* ws,
                            const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
                            int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits = TcWaits{},
-                           const TcRope& rope = TcRope{}, bool wide = false);
+                           const TcRope& rope = TcRope{}, bool wide = false, bool pdl = true, bool early_w = false);
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
 // ---- attention (k_attention.cu)
@@ -197,8 +207,13 @@ __device__ __forceinline__ float2 rope_rot(float a, float b, float2 cs) {
   return make_float2(__fmaf_rn(a, cs.x, -__fmul_rn(b, cs.y)), __fmaf_rn(a, cs.y, __fmul_rn(b, cs.x)));
 }
 
-// SwiGLU gate: silu(g) * u = g / (1 + exp(-g)) * u with the fast exponential and
-// division (a few ulp; g < -87 gives exp(-g) = inf and a zero result).
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// SwiGLU gate: silu(g) * u = (g / (1 + exp(-g))) * u in f32, each step rounded to
+// nearest: CUDA's full-accuracy expf (at most 2 ulp), an IEEE add, an IEEE division
+// and an IEEE multiply, so the result is within a few ulp of the exact value. For
+// g < -88.7 exp(-g) overflows to inf and the gate gives -0 where the exact value is a
+// subnormal of magnitude below 2^-126 * |g|.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
 
 }  // namespace ppdev

@@ -33,6 +33,13 @@ def bits(a: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(a).view(np.uint32)
 
 
+def swiglu_close(got: np.ndarray, ref: np.ndarray, rel: float = 1e-6, floor: float = 1e-36) -> bool:
+    """Each SwiGLU output within `rel` of the oracle's value (a few ulp of f32), with an
+    absolute floor for results in the subnormal range (exp(-g) overflows for g < -88.7)."""
+    d = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    return bool(np.all(d <= rel * np.abs(ref.astype(np.float64)) + floor))
+
+
 def max_rel(a, b, scale) -> float:
     return float(np.abs(a.astype(np.float64) - b.astype(np.float64)).max() / scale)
 
@@ -54,8 +61,12 @@ def logits_close(gpu: np.ndarray, ref: np.ndarray, tol: float = 1e-2):
     return err <= tol * std, err / std, int(np.argmax(gpu)) == top_ref, gap / std
 
 
-def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3):
+def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3, calls=None):
     """Verify a GPU prefill layer by layer against the oracle.
+
+    calls: the prefill calls that cover toks, as (start_pos, n, chunk) in
+    position order (default: one call of every token from position 0); later
+    calls continue the K/V cache of earlier ones, on both sides.
 
     The GPU runs with its trace on (residual stream at every layer boundary,
     int8 codes and scales at every quantisation point). For each layer the
@@ -83,10 +94,14 @@ def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3):
     tx = torch.empty(((c.n_layers + 1) * P * c.dim,), dtype=torch.float32, device="cuda")
     tc = torch.zeros((c.n_layers * 4 * P * kmax,), dtype=torch.int8, device="cuda")
     ts = torch.empty((c.n_layers * 4 * P,), dtype=torch.float32, device="cuda")
+    calls = calls or [(0, P, chunk)]
+    assert calls[0][0] == 0 and all(a[0] + a[1] == b[0] for a, b in zip(calls, calls[1:]))
+    assert calls[-1][0] + calls[-1][1] == P
     g.kv_reset()
     g.set_trace(tx, tc, ts, P)
     try:
-        logits = g.prefill(toks, 0, chunk)
+        for start, n, ch in calls:
+            logits = g.prefill(toks[start:start + n], start, ch)
     finally:
         g.set_trace(None, None, None, 0)
     X = host(tx).reshape(c.n_layers + 1, P, c.dim)
@@ -96,21 +111,25 @@ def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3):
     om = oracle.OracleModel(model, max_seq=P)
     widths = (c.dim, c.n_heads * c.head_dim, c.dim, c.ffn)
     report = []
+    for start, n, _ in calls:
+        rows = slice(start, start + n)
+        for L in range(c.n_layers):
+            y, st = om.layer_forced(L, X[L][rows], codes[L][:, rows], scales[L][:, rows], start)
+            assert np.array_equal(bits(y), bits(X[L + 1][rows])), \
+                f"layer {L}, positions {start}..: residual rows differ with equal codes"
+            for pt in range(4):
+                if st["mismatches"][pt]:
+                    assert st["max_code_diff"][pt] == 1, (L, pt, st)
+                    assert st["max_margin"][pt] <= margin_tol, (L, pt, st)
+                    assert st["mismatches"][pt] <= 1e-3 * n * widths[pt], (L, pt, st)
+                if st["scale_mismatches"][pt]:
+                    assert st["max_scale_rel"][pt] <= 1e-5, (L, pt, st)
+            report.append(st)
     for L in range(c.n_layers):
-        y, st = om.layer_forced(L, X[L], codes[L], scales[L], 0)
-        assert np.array_equal(bits(y), bits(X[L + 1])), f"layer {L}: residual rows differ with equal codes"
-        for pt in range(4):
-            if st["mismatches"][pt]:
-                assert st["max_code_diff"][pt] == 1, (L, pt, st)
-                assert st["max_margin"][pt] <= margin_tol, (L, pt, st)
-                assert st["mismatches"][pt] <= 1e-3 * P * widths[pt], (L, pt, st)
-            if st["scale_mismatches"][pt]:
-                assert st["max_scale_rel"][pt] <= 1e-5, (L, pt, st)
         for which in (0, 1):
             ref = om.kv(L, which)[:P]
             got = g.kv(L, which, 0, P)
             assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max(), (L, which)
-        report.append(st)
     ref_logits = om.final_logits(X[c.n_layers][P - 1])
     om.close()
     return logits, ref_logits, report

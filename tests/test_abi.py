@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -55,8 +56,10 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(pp.pp_config) == 4 * len(fields)
     sbody = re.search(r"typedef struct pp_stats \{(.*?)\} pp_stats;", text, re.S).group(1)
     sbody = re.sub(r"/\*.*?\*/", "", sbody, flags=re.S)
-    sfields = re.findall(r"\b(int64_t|double)\s+(\w+);", sbody)
-    assert [n for _, n in sfields] == [n for n, _ in pp.pp_stats._fields_]
+    sfields = re.findall(r"\b(int64_t|double)\s+(\w+)((?:\[\d+\])*);", sbody)
+    assert [n for _, n, _ in sfields] == [n for n, _ in pp.pp_stats._fields_]
+    n_words = sum(int(np.prod([int(d) for d in re.findall(r"\d+", dims)] or [1])) for _, _, dims in sfields)
+    assert ctypes.sizeof(pp.pp_stats) == 8 * n_words
     lbody = re.search(r"typedef struct pp_layer_profile \{(.*?)\} pp_layer_profile;", text, re.S).group(1)
     lbody = re.sub(r"/\*.*?\*/", "", lbody, flags=re.S)
     lfields = re.findall(r"\b(int64_t|double)\s+(\w+);", lbody)

@@ -35,6 +35,47 @@ def test_bounded_wait_runs_out_and_the_device_stays_usable():
     assert np.array_equal(host(acc), oracle.gemm_i8(a, w))
 
 
+@pytest.mark.parametrize("call", ["gemm", "gemm_acc", "noalloc"])
+def test_single_step_gemm_reports_a_bounded_wait_that_runs_out(call):
+    # The single-step GEMM calls share a device status word: with their MMA issuer held back and every
+    # wait bounded to 20 ms (pp_debug_op_stall) each call's kernel gives up and records the timeout,
+    # which pp_op_status reports once; normal calls afterwards are exact and report PP_OK.
+    torch = torch_cuda()
+    m, n, k = 512, 4096, 14336  # the down projection at 512 rows: stream-K partial tiles on a GB300
+    a = synth.uniform_i8(92, 1, (m, k))
+    w = synth.uniform_i8(92, 2, (n, k))
+    ws = synth.uniform_f32(92, 3, (n,), 1e-4, 2e-3)
+    as_ = synth.uniform_f32(92, 4, (m,), 1e-3, 5e-2)
+    da, a16, dw, dws, das = dev(a), dev(a.astype(np.float16)), dev(w), dev(ws), dev(as_)
+    out = empty((m, n), torch.float32)
+    acc = empty((m, n), torch.int32)
+
+    def run():
+        if call == "gemm":
+            pp.pp_op_gemm(pp.PP_GEMM_TC, pp.PP_EPI_STORE, da, a16, dw, dws, das, m, n, k, out, n)
+        elif call == "gemm_acc":
+            pp.pp_op_gemm_acc(pp.PP_GEMM_TC, da, a16, dw, m, n, k, acc)
+        else:
+            pp.pp_op_gemm_noalloc(pp.PP_EPI_STORE, a16, dw, dws, das, m, n, k, out, n)
+
+    assert pp.pp_op_status() == pp.PP_OK
+    pp.pp_debug_op_stall(20000)
+    try:
+        run()
+    finally:
+        pp.pp_debug_op_stall(0)
+    assert pp.pp_op_status() == pp.PP_ERR_DEVICE_TIMEOUT
+    assert "bounded device wait" in pp.last_error()
+    assert pp.pp_op_status() == pp.PP_OK  # reported once, then cleared
+    run()
+    assert pp.pp_op_status() == pp.PP_OK
+    ref = oracle.gemm_i8(a, w)
+    if call == "gemm_acc":
+        assert np.array_equal(host(acc), ref)
+    else:
+        assert np.array_equal(bits(host(out)), bits(oracle.dequant_block(ref, ws, as_)))
+
+
 def test_loader_without_prefetch_changes_nothing():
     torch_cuda()
     mod = synth.make_model(synth.CONFIGS["1b"])

@@ -12,7 +12,7 @@ import pytest
 import oracle
 import prompt_prefill_gb300 as pp
 import synth
-from tests.gpu_util import bits, dev, empty, host, torch_cuda
+from tests.gpu_util import bits, dev, empty, host, swiglu_close, torch_cuda
 
 pytestmark = pytest.mark.gpu
 TC = pp.PP_GEMM_TC
@@ -132,8 +132,46 @@ def test_tc_swiglu(torch, m, F, k):
     g = oracle.dequant_block(oracle.gemm_i8(a, wg), sg, as_)
     u = oracle.dequant_block(oracle.gemm_i8(a, wu), su, as_)
     ref = np.vectorize(lambda x, y: float(oracle.silu_mul(x, y)), otypes=[np.float32])(g, u)
-    assert np.abs(got.astype(np.float64) - ref).max() <= 4e-6 * max(1.0, np.abs(ref).max())  # fast exp/div
+    # full-accuracy expf (<= 2 ulp) and IEEE add, division and multiply: within a few ulp of each value
+    assert swiglu_close(got, ref)
     assert np.array_equal(bits(got), bits(host(out_mma)))  # same epilogue code, same integers
+
+
+# gate values at and around the edges of the f32 exponential: exp(-g) overflows for g < -88.72, the
+# quotient g / (1 + exp(-g)) is subnormal or near the smallest normal for g in about [-103, -87],
+# and 1 + exp(-g) rounds to 1 for g > 16.6
+EDGE_G = (-100.0, -88.0, -87.5, 0.0, 30.0, 88.0, -30.0, -5.0, 1.0, 16.0, 17.0, -16.5)
+
+
+@pytest.mark.parametrize("eng", [TC, pp.PP_GEMM_MMA])
+def test_swiglu_gate_edges(torch, eng):
+    # Every token row is the one-hot code 1 at k = t, every gate row holds the code 127 at each k and a
+    # row scale that puts g = (float(127) * s_g) * 1 at one of EDGE_G; up rows are random. Both engines
+    # compute the same exact integers, so the epilogue sees the same g and u as the oracle.
+    m, k, F = 64, 64, 192
+    a = np.zeros((m, k), np.int8)
+    a[np.arange(m), np.arange(m)] = 1
+    wg = np.full((F, k), 127, np.int8)
+    wu = synth.uniform_i8(85, 3, (F, k))
+    sg = np.array([EDGE_G[r % len(EDGE_G)] / 127.0 for r in range(F)], np.float32)
+    su = synth.uniform_f32(85, 5, (F,), 1e-3, 5e-2)
+    as_ = np.ones((m,), np.float32)
+    B = 16
+    wgu = np.concatenate([np.concatenate([wg[b * B:(b + 1) * B], wu[b * B:(b + 1) * B]]) for b in range(F // B)])
+    sgu = np.concatenate([np.concatenate([sg[b * B:(b + 1) * B], su[b * B:(b + 1) * B]]) for b in range(F // B)])
+    out = empty((m, F), torch.float32)
+    pp.pp_op_gemm(eng, pp.PP_EPI_SWIGLU, dev(a), dev(a.astype(np.float16)), dev(wgu), dev(sgu), dev(as_), m, 2 * F,
+                  k, out, F)
+    got = host(out)
+    g = oracle.dequant_block(oracle.gemm_i8(a, wg), sg, as_)
+    u = oracle.dequant_block(oracle.gemm_i8(a, wu), su, as_)
+    assert np.allclose(g[0, :len(EDGE_G)], EDGE_G, rtol=1e-6, atol=0)  # the gate values reach the edges
+    ref = np.vectorize(lambda x, y: float(oracle.silu_mul(x, y)), otypes=[np.float32])(g, u)
+    assert np.all(np.isfinite(got))
+    assert swiglu_close(got, ref)
+    # the far negative gates give (signed) zero or a value within the subnormal floor
+    far = np.array([EDGE_G[r % len(EDGE_G)] <= -87.5 for r in range(F)])
+    assert np.abs(got[:, far]).max() <= 1e-35
 
 
 def test_tc_shape_errors(torch):

@@ -21,8 +21,9 @@ from tests.gpu_util import bits, dev, empty, host, torch_cuda
 pytestmark = pytest.mark.gpu
 
 # (m, n, k): the long-K down projection at 512 and 256 rows (planned with
-# stream-K partial tiles, i.e. they use the scratch), and a QKV-shaped GEMM
-# that runs whole tiles.
+# stream-K partial tiles on a GB300, i.e. they use the scratch), and a
+# QKV-shaped GEMM that runs whole tiles. Whether a shape uses the scratch
+# depends on the device's SM count; the tests read the plan from the library.
 SHAPES = [(512, 4096, 14336), (256, 8192, 14336), (512, 6144, 4096)]
 
 
@@ -62,8 +63,55 @@ def test_noalloc_equals_allocating_gemm_twice(torch, m, n, k, epi):
         assert np.array_equal(bits(host(out)), bits(ref))
 
 
+def test_noalloc_clears_counters_left_behind(torch):
+    # Arrival counters that a call which gave up part of the way would leave in the fixed scratch
+    # (set here from the host): the next call clears what it uses and still equals pp_op_gemm.
+    m, n, k = SHAPES[0]
+    part, cnt = pp.pp_op_gemm_noalloc_need(m, n, k)
+    if cnt == 0:
+        pytest.skip("this device plans the shape without stream-K scratch")
+    a, w, ws, as_, _ = _inputs(m, n, k, 97)
+    da, da16, dw, dws, das = dev(a), dev(a.astype(np.float16)), dev(w), dev(ws), dev(as_)
+    ref = empty((m, n), torch.float32)
+    pp.pp_op_gemm(pp.PP_GEMM_TC, pp.PP_EPI_STORE, da, da16, dw, dws, das, m, n, k, ref, n)
+    ref = host(ref)
+    for value in (1, 7):
+        pp.pp_debug_noalloc_poison(value)
+        out = empty((m, n), torch.float32)
+        pp.pp_op_gemm_noalloc(pp.PP_EPI_STORE, da16, dw, dws, das, m, n, k, out, n)
+        assert np.array_equal(bits(host(out)), bits(ref))
+    assert pp.pp_op_status() == pp.PP_OK
+
+
+def test_noalloc_accepts_exactly_the_shapes_its_scratch_holds(torch):
+    # the library's own plan decides: a shape whose partial tiles or counters exceed the fixed
+    # capacity is rejected with PP_ERR_ARG, every other shape runs
+    for m, n, k in [(1024, 4096, 14336), (768, 4096, 14336)] + SHAPES:
+        part, cnt = pp.pp_op_gemm_noalloc_need(m, n, k)
+        fits = part <= pp.PP_NOALLOC_PART_BYTES and cnt <= pp.PP_NOALLOC_COUNTERS
+        a16 = empty((m, k), torch.float16)
+        w = empty((n, k), torch.int8)
+        ws = empty((n,), torch.float32)
+        as_ = empty((m,), torch.float32)
+        out = empty((m, n), torch.float32)
+        if fits:
+            a16.zero_()
+            w.zero_()
+            pp.pp_op_gemm_noalloc(pp.PP_EPI_STORE, a16, w, ws, as_, m, n, k, out, n)
+            continue
+        with pytest.raises(pp.PPError) as e:
+            pp.pp_op_gemm_noalloc(pp.PP_EPI_STORE, a16, w, ws, as_, m, n, k, out, n)
+        assert e.value.status == pp.PP_ERR_ARG
+        assert "scratch" in str(e.value)
+    torch.cuda.synchronize()
+    assert pp.pp_op_status() == pp.PP_OK
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(torch):
-    m, n, k = 1024, 4096, 14336  # stream-K plan needs more than the fixed 32 MiB
+    m, n, k = 1024, 4096, 14336  # on a GB300 the stream-K plan needs more than the fixed 32 MiB
+    part, cnt = pp.pp_op_gemm_noalloc_need(m, n, k)
+    if part <= pp.PP_NOALLOC_PART_BYTES and cnt <= pp.PP_NOALLOC_COUNTERS:
+        pytest.skip("on this device the shape fits the fixed scratch")
     a16 = empty((m, k), torch.float16)
     w = empty((n, k), torch.int8)
     ws = empty((n,), torch.float32)
