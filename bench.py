@@ -375,10 +375,14 @@ def run_small_configs(args, peaks) -> dict:
     d_logits = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
     step = lambda: g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)  # noqa: E731
     res = {}
-    for overlap in (0, 1):
-        g.set_chunk_overlap(bool(overlap))
-        ms = time_calls(stream, step, steps, warm)
-        res["overlap" if overlap else "serial"] = {"ms": ms, "tok_per_s": P / (ms / 1000)}
+    for graphs in (0, 1):
+        g.set_graphs(bool(graphs))
+        for overlap in (0, 1):
+            g.set_chunk_overlap(bool(overlap))
+            ms = time_calls(stream, step, steps, warm)
+            res[("overlap" if overlap else "serial") + ("_graph" if graphs else "")] = {
+                "ms": ms, "tok_per_s": P / (ms / 1000)}
+    g.set_graphs(False)
     g.set_chunk_overlap(False)
     # host enqueue time of one call (the library's launches, no device wait) against the GPU time
     torch.cuda.synchronize()
@@ -392,15 +396,16 @@ def run_small_configs(args, peaks) -> dict:
     class_ms, _, _ = profile_classes(g, step)
     kernel_ms = sum(class_ms.values())
     roof = prefill_roofline_ms(cfg, P, chunk, peaks)
-    best = min(res["serial"]["ms"], res["overlap"]["ms"])
+    best = min(v["ms"] for v in res.values())
     out["350m"] = {
         "workload": f"350M-class int8 decoder (D{cfg.dim}, L{cfg.n_layers}, {cfg.n_heads}/{cfg.n_kv_heads} heads, "
                     f"F{cfg.ffn}, V{cfg.vocab}): {P}-token prompt, chunk {chunk}",
-        "serial": res["serial"], "chunk_overlap": res["overlap"], "roofline": roof,
-        "frac_of_roofline": roof["t_roof_ms"] / best,
+        "calls": res, "roofline": roof, "frac_of_roofline": roof["t_roof_ms"] / best,
         "launches_per_call": launches, "host_enqueue_ms_per_call": host_ms,
         "kernel_ms_per_call_serial_profiled": kernel_ms, "kernel_ms_by_class": class_ms,
-        "host_enqueue_over_gpu_time": host_ms / res["serial"]["ms"]}
+        # launch by launch vs the same call replayed from a CUDA graph: the host's share of a call
+        "graph_speedup_serial": res["serial"]["ms"] / res["serial_graph"]["ms"],
+        "graph_speedup_overlap": res["overlap"]["ms"] / res["overlap_graph"]["ms"]}
     g.close()
     del model
     # ---- 1B: chunk sweep, then a continuation call at start_pos 2048
@@ -410,6 +415,7 @@ def run_small_configs(args, peaks) -> dict:
     toks = synth.prompt(cfg, 2 * P)
     g = pp.PrefillModel(cfg, model, max_seq=2 * P, max_chunk=2048, gemm_engine=args.engine)
     g.set_chunk_overlap(True)
+    g.set_graphs(bool(args.graphs))
     d_tok = torch.from_numpy(toks).cuda()
     d_logits = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
     sweep = {}
@@ -507,6 +513,7 @@ def run_ours(args, cfg, world, rank, local, pg):
     class_ms, class_launches, dominant = profile_classes(g, step, steps_dominant=max(1, min(args.steps, 5)))
     if args.overlap:
         g.set_chunk_overlap(True)
+    g.set_graphs(bool(args.graphs))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -569,7 +576,7 @@ def run_ours(args, cfg, world, rank, local, pg):
         "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded N(0,0.02) int8 per-row weights, uniform ids)",
         "config": workload_config(cfg, args),
         "gemm_engine": {pp.PP_GEMM_MMA: "mma.sync s8", pp.PP_GEMM_TC: "tcgen05 exact-integer f16"}.get(g.gemm_engine),
-        "chunk_overlap": bool(args.overlap),
+        "chunk_overlap": bool(args.overlap), "cuda_graphs": bool(args.graphs),
         "prefill_roofline": {"t_roof_ms": 1000 * t_roof, "frac": t_roof / step_s, "tensor_peak_tflops": tensor_peak,
                              "hbm_gbs": NORTH_HBM_GBS, "frac_vs_measured_hbm": t_roof_meas / step_s,
                              "gemm_tops": gemm_ops / 1e12, "bytes_gb": bytes_step / 1e9},
@@ -798,6 +805,8 @@ def main(argv=None):
                     help="skip the 350M, 1B and streamed measurements that follow the 8B line")
     ap.add_argument("--overlap", type=int, default=1,
                     help="1 (default): consecutive chunks on eight streams (pp_set_chunk_overlap); 0: serial")
+    ap.add_argument("--graphs", type=int, default=1,
+                    help="1 (default): each prefill call replayed from a CUDA graph after its first (pp_set_graphs)")
     ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention | quant | norm_quant")
     ap.add_argument("--m", type=int, default=512)
     ap.add_argument("--n", type=int, default=28672)

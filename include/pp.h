@@ -138,9 +138,11 @@ typedef struct pp_stats {
   int64_t prof_launches;      /* launches of the profiled kernel class */
   double prof_ms;             /* summed event-timed duration of those launches */
   int64_t kv_bytes;           /* device memory backing the K/V cache now (a level, not a counter) */
-  int64_t gemm_launches[5][3]; /* tcgen05 projection GEMM launches by [epilogue][tile width]: epilogue 0 store,
+  int64_t gemm_launches[5][6]; /* tcgen05 projection GEMM launches by [epilogue][tile]: epilogue 0 store,
                                   1 residual add, 2 SwiGLU, 3 raw int32, 4 QKV with RoPE and the K/V write;
-                                  tile width (weight rows per CTA pair) 256, 192, 128 */
+                                  tile 0-2: chunks of more than 128 rows, 256 tokens x 256 / 192 / 128
+                                  weight rows per CTA pair; tile 3-5: chunks of at most 128 rows, 256
+                                  weight rows x 128 / 64 / 32 tokens */
 } pp_stats;
 
 typedef struct pp_model pp_model;
@@ -220,6 +222,18 @@ int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
  * on, for calls of a single chunk, and for streamed weights in chunk-outer
  * order. */
 int pp_set_chunk_overlap(pp_model* m, int32_t enable);
+
+/* CUDA graphs (1 on, 0 off; off after pp_model_load). With graphs on, the
+ * first pp_prefill / pp_prefill_device call with a given (token and logits
+ * buffers, n, start_pos, chunk, chunk overlap) is captured from the model's own
+ * stream into an executable graph, which that call and every later identical
+ * one launch as a whole on the caller's stream instead of launching each of
+ * its kernels (thousands per call at small chunks) from the host. The graph
+ * replays the same launches, so results and pp_stats are as without it.
+ * Up to 8 graphs are kept per model (least recently used dropped first); off
+ * frees them. Calls in streamed mode, with kv_grow, with a profiled kernel
+ * class, with the per-layer profile or with a trace run launch by launch. */
+int pp_set_graphs(pp_model* m, int32_t enable);
 
 /* Per-layer stage profile ("Single-pass prefill", the per-layer profiler of
  * I/O and compute; "Predictive prefetch", the sync vs async loader A/B),

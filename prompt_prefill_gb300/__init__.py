@@ -30,9 +30,10 @@ PP_GEMM_AUTO, PP_GEMM_MMA, PP_GEMM_TC = 0, 1, 2
 PP_KERNEL_COUNT = 6
 KERNEL_NAMES = {0: "gemm", 1: "attention", 2: "norm_quant", 3: "rope_kv", 4: "lm_head", 5: "embed"}
 PP_EPI_STORE, PP_EPI_RESID, PP_EPI_SWIGLU = 0, 1, 2
-# epilogue indices of pp_stats.gemm_launches (3: raw int32, 4: QKV with RoPE + K/V write) and its tile widths
+# epilogue indices of pp_stats.gemm_launches (3: raw int32, 4: QKV with RoPE + K/V write)
 GEMM_EPI_NAMES = {0: "store", 1: "residual", 2: "swiglu", 3: "int32", 4: "rope"}
-GEMM_TILE_WIDTHS = (256, 192, 128)
+# tiles of pp_stats.gemm_launches: (tokens, weight rows) per CTA pair
+GEMM_TILES = ((256, 256), (256, 192), (256, 128), (128, 256), (64, 256), (32, 256))
 PP_NOALLOC_PART_BYTES, PP_NOALLOC_COUNTERS = 32 * 1024 * 1024, 4096
 
 
@@ -61,12 +62,12 @@ class pp_stats(ctypes.Structure):
                                                "prefetch_hits", "prefetch_misses", "kernel_launches",
                                                "prof_launches")] + [("prof_ms", ctypes.c_double),
                                                                     ("kv_bytes", ctypes.c_int64),
-                                                                    ("gemm_launches", (ctypes.c_int64 * 3) * 5)]
+                                                                    ("gemm_launches", (ctypes.c_int64 * 6) * 5)]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
-        d["gemm_launches"] = {(e, GEMM_TILE_WIDTHS[b]): int(self.gemm_launches[e][b])
-                              for e in range(5) for b in range(3) if self.gemm_launches[e][b]}
+        d["gemm_launches"] = {(e, GEMM_TILES[b]): int(self.gemm_launches[e][b])
+                              for e in range(5) for b in range(6) if self.gemm_launches[e][b]}
         return d
 
 
@@ -92,6 +93,7 @@ SIGNATURES = {
     "pp_set_profile_kernel": ([_vp, _i32], ctypes.c_int),
     "pp_set_layer_profile": ([_vp, _i32], ctypes.c_int),
     "pp_set_chunk_overlap": ([_vp, _i32], ctypes.c_int),
+    "pp_set_graphs": ([_vp, _i32], ctypes.c_int),
     "pp_get_layer_profile": ([_vp, ctypes.POINTER(pp_layer_profile), _i32], ctypes.c_int),
     "pp_set_trace": ([_vp, _vp, _vp, _vp, _i32], ctypes.c_int),
     "pp_status_str": ([ctypes.c_int], ctypes.c_char_p),
@@ -271,6 +273,10 @@ def pp_set_chunk_overlap(h: int, enable: bool):
     _check(lib().pp_set_chunk_overlap(h, 1 if enable else 0), "pp_set_chunk_overlap")
 
 
+def pp_set_graphs(h: int, enable: bool):
+    _check(lib().pp_set_graphs(h, 1 if enable else 0), "pp_set_graphs")
+
+
 def pp_get_layer_profile(h: int, n_layers: int) -> list:
     arr = (pp_layer_profile * n_layers)()
     _check(lib().pp_get_layer_profile(h, arr, n_layers), "pp_get_layer_profile")
@@ -440,6 +446,9 @@ class PrefillModel:
 
     def set_chunk_overlap(self, enable=True):
         pp_set_chunk_overlap(self.h, enable)
+
+    def set_graphs(self, enable=True):
+        pp_set_graphs(self.h, enable)
 
     def layer_profile(self):
         return pp_get_layer_profile(self.h, self.cfg.n_layers)

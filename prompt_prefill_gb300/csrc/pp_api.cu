@@ -191,8 +191,13 @@ struct pp_model {
   // tcgen05 engine: tensor maps of every weight matrix (per layer, or per ring
   // slot in streamed mode: qkv, o, gate/up, down) and of the fp16 activation
   // buffer viewed with each GEMM's k (dim, n_heads*head_dim, ffn)
+  // weight maps: per weight matrix, one per tile width of k_gemm_tc (kTcBn) and
+  // one for k_gemm_tw (chunks of at most 128 rows)
   std::vector<CUtensorMap> wmap;
-  CUtensorMap amap_d{}, amap_qd{}, amap_f{};
+  // activation maps of the fp16 code buffer viewed with each GEMM's k (0 dim, 1
+  // n_heads*head_dim, 2 ffn): k_gemm_tc's, and k_gemm_tw's per token tile (kTwNt)
+  CUtensorMap amap[3]{};
+  CUtensorMap amap_tw[3][3]{};
   TcWorkspace tcws;  // stream-K partial tiles and counters of the projection GEMMs
   float* attn_part = nullptr;  // per-key-range partial attention state of one chunk
   size_t attn_part_bytes = 0;
@@ -208,7 +213,8 @@ struct pp_model {
     TcWorkspace tcws;
     float* attn_part;
     size_t attn_part_bytes;
-    CUtensorMap amap_d, amap_qd, amap_f;
+    CUtensorMap amap[3];
+    CUtensorMap amap_tw[3][3];
   };
   static constexpr int kOverlap = 8;
   bool overlap = false;
@@ -233,6 +239,21 @@ struct pp_model {
   std::vector<void*> allocations;
   // streams whose next kernel follows a wait on another stream's event (wait_event)
   std::vector<cudaStream_t> plain_next;
+  // CUDA graphs of repeated calls (pp_set_graphs): one executable graph per call
+  // shape and buffer set, with the statistics one execution adds
+  struct GraphEntry {
+    const int32_t* d_tok;
+    float* d_logits;
+    int n, start_pos, chunk, overlap, seg;
+    cudaGraphExec_t exec;
+    pp_stats delta;
+    uint64_t last_use;
+  };
+  static constexpr int kGraphCache = 8;
+  bool graphs = false;
+  bool capturing = false;
+  std::vector<GraphEntry> gcache;
+  uint64_t gclock = 0;
 };
 
 namespace {
@@ -343,6 +364,14 @@ int launch(pp_model* m, int cls, cudaStream_t st, F&& fn) {
   return PP_OK;
 }
 
+// Stream-K workspace the tcgen05 engine plans for an m x n x k GEMM (either kernel).
+void gemm_workspace_need(int m, int n, int k, size_t* part, size_t* cnt) {
+  if (m <= kTwMaxRows)
+    tw_workspace_need(m, n, k, part, cnt);
+  else
+    tc_workspace_need(m, n, k, part, cnt);
+}
+
 // K-extent of one exact f32 segment of the tcgen05 engine (pp_set_exact_segment).
 std::atomic<int> g_tc_seg{kTcSegK};
 int tc_segment() { return g_tc_seg.load(); }
@@ -352,13 +381,22 @@ int tc_segment() { return g_tc_seg.load(); }
 int gemm(pp_model* m, cudaStream_t st, int epi, int mg, int which, const float* ws, const int8_t* w, int M, int N,
          int K, float* out, int ldo, const TcRope& rope = TcRope{}) {
   if (m->engine == PP_GEMM_TC) {
+    const int kind = K == m->cfg.dim ? 0 : (K == m->cfg.ffn ? 2 : 1);
+    const CUtensorMap* wm = &m->wmap[((size_t)mg * 4 + which) * 4];
+    if (M <= kTwMaxRows) {  // short chunk: weights on the MMA's M side (k_gemm_tw)
+      const int ti = tw_nt_index(M);
+      m->stats.gemm_launches[epi][3 + ti] += 1;
+      return launch(m, PP_KERNEL_GEMM, st, [&](bool pdl) {
+        return launch_gemm_tw(epi, m->amap_tw[kind][ti], wm[3], kTwNt[ti], ws, m->as, M, N, K, out, ldo, nullptr,
+                              tc_segment(), m->status, m->tcws, st, TcWaits{}, rope, m->gemm_wide, pdl,
+                              /*early_w=*/true);
+      });
+    }
     const int bi = tc_bn_index(M, N, K, m->gemm_wide);
     m->stats.gemm_launches[epi][bi] += 1;
-    const CUtensorMap& wm = m->wmap[((size_t)mg * 4 + which) * 3 + bi];
-    const CUtensorMap& am = K == m->cfg.dim ? m->amap_d : (K == m->cfg.ffn ? m->amap_f : m->amap_qd);
     return launch(m, PP_KERNEL_GEMM, st, [&](bool pdl) {
-      return launch_gemm_tc(epi, am, wm, kTcBn[bi], ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(), m->status, m->tcws,
-                            st, TcWaits{}, rope, m->gemm_wide, pdl, /*early_w=*/true);
+      return launch_gemm_tc(epi, m->amap[kind], wm[bi], kTcBn[bi], ws, m->as, M, N, K, out, ldo, nullptr, tc_segment(),
+                            m->status, m->tcws, st, TcWaits{}, rope, m->gemm_wide, pdl, /*early_w=*/true);
     });
   }
   return launch(m, PP_KERNEL_GEMM, st, [&](bool) {  // plain launches
@@ -370,15 +408,20 @@ int make_weight_maps(pp_model* m, const uint8_t* block) {
   const pp_config& c = m->cfg;
   const LayerPtrs L = layer_ptrs(m->lay, block);
   const int D = c.dim, QD = c.n_heads * c.head_dim, QKV = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn;
-  // one map per tile width: the width a launch uses depends on its chunk's row count
   const int8_t* w[4] = {L.wqkv, L.wo, L.wgu, L.wd};
   const int n[4] = {QKV, D, 2 * F, D}, k[4] = {D, QD, D, F};
-  for (int i = 0; i < 4; ++i)
+  // per matrix: one map per k_gemm_tc tile width (the width a launch uses depends on its
+  // chunk's row count), then k_gemm_tw's
+  for (int i = 0; i < 4; ++i) {
     for (int b = 0; b < 3; ++b) {
       CUtensorMap t;
       PP_CUDA(make_tmap_w(&t, w[i], n[i], k[i], kTcBn[b]));
       m->wmap.push_back(t);
     }
+    CUtensorMap t;
+    PP_CUDA(make_tmap_tw_weights(&t, w[i], n[i], k[i]));
+    m->wmap.push_back(t);
+  }
   return PP_OK;
 }
 
@@ -453,10 +496,12 @@ int alloc_scratch(pp_model* m, bool own_residual = true) {
     // stream-K workspace: the largest need over every chunk-row count and projection
     size_t part = 0, cnt = 0;
     const int shapes[4][2] = {{(int)QKV, (int)D}, {(int)D, (int)QD}, {(int)(2 * F), (int)D}, {(int)D, (int)F}};
-    for (size_t rows = 256; rows < MC + 256; rows += 256)
+    std::vector<size_t> row_counts = {32, 64, 128};  // the short-chunk kernel's token tiles
+    for (size_t rows = 256; rows < MC + 256; rows += 256) row_counts.push_back(rows);
+    for (size_t rows : row_counts)
       for (auto& sh : shapes) {
         size_t pb = 0, cc = 0;
-        tc_workspace_need((int)std::min(rows, MC), sh[0], sh[1], &pb, &cc);
+        gemm_workspace_need((int)std::min(rows, MC), sh[0], sh[1], &pb, &cc);
         part = std::max(part, pb);
         cnt = std::max(cnt, cc);
       }
@@ -467,9 +512,11 @@ int alloc_scratch(pp_model* m, bool own_residual = true) {
       m->tcws.part_bytes = part;
       m->tcws.counters = cnt;
     }
-    PP_CUDA(make_tmap_a(&m->amap_d, m->a16, (int)MC, (int)D));
-    PP_CUDA(make_tmap_a(&m->amap_qd, m->a16, (int)MC, (int)QD));
-    PP_CUDA(make_tmap_a(&m->amap_f, m->a16, (int)MC, (int)F));
+    const int ks[3] = {(int)D, (int)QD, (int)F};
+    for (int i = 0; i < 3; ++i) {
+      PP_CUDA(make_tmap_a(&m->amap[i], m->a16, (int)MC, ks[i]));
+      for (int j = 0; j < 3; ++j) PP_CUDA(make_tmap_tw_tokens(&m->amap_tw[i][j], m->a16, (int)MC, ks[i], kTwNt[j]));
+    }
   }
   return PP_OK;
 }
@@ -477,8 +524,20 @@ int alloc_scratch(pp_model* m, bool own_residual = true) {
 // Make scratch set j the model's fields (the active set's pointers are kept in sets[]).
 void use_scratch(pp_model* m, int j) {
   if (j == m->active_set) return;
-  m->sets[m->active_set] = pp_model::Scratch{m->x, m->qkv, m->qr, m->o, m->h, m->as, m->a8, m->a16, m->tcws,
-                                             m->attn_part, m->attn_part_bytes, m->amap_d, m->amap_qd, m->amap_f};
+  pp_model::Scratch& cur = m->sets[m->active_set];
+  cur.x = m->x;
+  cur.qkv = m->qkv;
+  cur.qr = m->qr;
+  cur.o = m->o;
+  cur.h = m->h;
+  cur.as = m->as;
+  cur.a8 = m->a8;
+  cur.a16 = m->a16;
+  cur.tcws = m->tcws;
+  cur.attn_part = m->attn_part;
+  cur.attn_part_bytes = m->attn_part_bytes;
+  memcpy(cur.amap, m->amap, sizeof m->amap);
+  memcpy(cur.amap_tw, m->amap_tw, sizeof m->amap_tw);
   const pp_model::Scratch& o = m->sets[j];
   m->x = o.x;
   m->qkv = o.qkv;
@@ -491,9 +550,8 @@ void use_scratch(pp_model* m, int j) {
   m->tcws = o.tcws;
   m->attn_part = o.attn_part;
   m->attn_part_bytes = o.attn_part_bytes;
-  m->amap_d = o.amap_d;
-  m->amap_qd = o.amap_qd;
-  m->amap_f = o.amap_f;
+  memcpy(m->amap, o.amap, sizeof m->amap);
+  memcpy(m->amap_tw, o.amap_tw, sizeof m->amap_tw);
   m->active_set = j;
 }
 
@@ -599,6 +657,8 @@ int load_impl(pp_model* m, const pp_weights* w) {
   return PP_OK;
 }
 
+void graphs_clear(pp_model* m);
+
 void free_impl(pp_model* m) {
   if (m->stream) cudaStreamSynchronize(m->stream);
   if (m->copy_stream) cudaStreamSynchronize(m->copy_stream);
@@ -618,6 +678,7 @@ void free_impl(pp_model* m) {
   for (auto& e : m->copy_ev)
     if (e.first) { cudaEventDestroy(e.first); cudaEventDestroy(e.second); }
   for (auto e : m->ev_pool) cudaEventDestroy(e);
+  graphs_clear(m);
   for (int s = 0; s < 2; ++s) {
     if (m->ring_ready[s]) cudaEventDestroy(m->ring_ready[s]);
     if (m->ring_free[s]) cudaEventDestroy(m->ring_free[s]);
@@ -829,7 +890,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   }
   // The model's scratch, K/V cache and ring are shared by every call: order
   // this call after the previous one, whichever stream that one ran on.
-  PP_TRY(wait_event(m, st, m->done));
+  if (!m->capturing) PP_TRY(wait_event(m, st, m->done));  // a graph launch waits outside the graph
   if (streamed && st != m->stream) {
     // keep the ring's events on one compute stream
     cudaEvent_t e;
@@ -1011,7 +1072,7 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     PP_TRY(wait_event(m, st, e));
     m->ev_pool.push_back(e);
   }
-  PP_CUDA(cudaEventRecord(m->done, st));
+  if (!m->capturing) PP_CUDA(cudaEventRecord(m->done, st));
   m->stats.calls += 1;
   m->stats.chunks += n_chunks;
   m->stats.tokens += n;
@@ -1020,6 +1081,113 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
   return PP_OK;
 }
 
+
+// Statistics one graph execution adds (the counters its capture incremented).
+pp_stats stats_delta(const pp_stats& a, const pp_stats& b) {
+  pp_stats d = b;
+  d.calls -= a.calls;
+  d.chunks -= a.chunks;
+  d.tokens -= a.tokens;
+  d.weight_bytes_read -= a.weight_bytes_read;
+  d.h2d_bytes -= a.h2d_bytes;
+  d.prefetch_hits -= a.prefetch_hits;
+  d.prefetch_misses -= a.prefetch_misses;
+  d.kernel_launches -= a.kernel_launches;
+  d.prof_launches -= a.prof_launches;
+  d.prof_ms -= a.prof_ms;
+  for (int e = 0; e < 5; ++e)
+    for (int b2 = 0; b2 < 6; ++b2) d.gemm_launches[e][b2] -= a.gemm_launches[e][b2];
+  return d;
+}
+
+void stats_add(pp_stats* s, const pp_stats& d) {
+  s->calls += d.calls;
+  s->chunks += d.chunks;
+  s->tokens += d.tokens;
+  s->weight_bytes_read += d.weight_bytes_read;
+  s->h2d_bytes += d.h2d_bytes;
+  s->kernel_launches += d.kernel_launches;
+  for (int e = 0; e < 5; ++e)
+    for (int b = 0; b < 6; ++b) s->gemm_launches[e][b] += d.gemm_launches[e][b];
+}
+
+void graphs_clear(pp_model* m) {
+  for (auto& g : m->gcache) cudaGraphExecDestroy(g.exec);
+  m->gcache.clear();
+}
+
+// One prefill call: through a cached CUDA graph of the whole call when graphs
+// are on and the call qualifies (resident weights, no profiling, tracing or
+// K/V growth), else launch by launch. A graph is captured from the model's own
+// stream the first time a (buffers, n, start_pos, chunk) combination is seen
+// and replayed on `st` afterwards; replay runs exactly the launches of the
+// capture, so the results are the same bits.
+int prefill_call(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
+                 cudaStream_t st) {
+  const pp_config& c = m->cfg;
+  const bool use_graph = m->graphs && c.mode == PP_MODE_RESIDENT && !c.kv_grow && c.profile_kernel == PP_KERNEL_NONE &&
+                         !m->trace && !m->layer_prof;
+  if (!use_graph) return prefill_impl(m, d_tok, n, start_pos, chunk, d_logits, st);
+  const int ovl = m->overlap ? 1 : 0, seg = tc_segment();
+  pp_model::GraphEntry* hit = nullptr;
+  for (auto& g : m->gcache)
+    if (g.d_tok == d_tok && g.d_logits == d_logits && g.n == n && g.start_pos == start_pos && g.chunk == chunk &&
+        g.overlap == ovl && g.seg == seg)
+      hit = &g;
+  if (!hit) {
+    if ((int)m->gcache.size() >= pp_model::kGraphCache) {  // drop the least recently used graph
+      auto lru = std::min_element(m->gcache.begin(), m->gcache.end(),
+                                  [](const pp_model::GraphEntry& a, const pp_model::GraphEntry& b) {
+                                    return a.last_use < b.last_use;
+                                  });
+      PP_TRY(sync_model(m));  // its last replay may still run
+      cudaGraphExecDestroy(lru->exec);
+      m->gcache.erase(lru);
+    }
+    const pp_stats before = m->stats;
+    const std::vector<cudaStream_t> plain = m->plain_next;
+    m->plain_next.clear();
+    PP_CUDA(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeRelaxed));
+    m->capturing = true;
+    const int rc = prefill_impl(m, d_tok, n, start_pos, chunk, d_logits, m->stream);
+    m->capturing = false;
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(m->stream, &graph);
+    const pp_stats after = m->stats;
+    m->stats = before;  // nothing ran yet
+    m->plain_next = plain;
+    if (rc != PP_OK || ec != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      if (rc != PP_OK) return rc;
+      set_err("capturing the prefill graph failed: %s", cudaGetErrorString(ec));
+      return PP_ERR_CUDA;
+    }
+    pp_model::GraphEntry g{};
+    g.d_tok = d_tok;
+    g.d_logits = d_logits;
+    g.n = n;
+    g.start_pos = start_pos;
+    g.chunk = chunk;
+    g.overlap = ovl;
+    g.seg = seg;
+    g.delta = stats_delta(before, after);
+    const cudaError_t ei = cudaGraphInstantiate(&g.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+      set_err("instantiating the prefill graph failed: %s", cudaGetErrorString(ei));
+      return PP_ERR_CUDA;
+    }
+    m->gcache.push_back(g);
+    hit = &m->gcache.back();
+  }
+  hit->last_use = ++m->gclock;
+  // the model's scratch and K/V cache are shared with the previous call, whatever its stream
+  PP_CUDA(cudaStreamWaitEvent(st, m->done, 0));
+  PP_CUDA(cudaGraphLaunch(hit->exec, st));
+  PP_CUDA(cudaEventRecord(m->done, st));
+  stats_add(&m->stats, hit->delta);
+  return PP_OK;
+}
 }  // namespace
 
 // =====================================================================  C ABI
@@ -1081,7 +1249,7 @@ int pp_prefill_device(pp_model* m, const int32_t* d_tokens, int32_t n, int32_t s
   PP_TRY(check_prefill_args(m, n, start_pos, chunk));
   if (!d_tokens || !d_logits) { set_err("null device pointer"); return PP_ERR_ARG; }
   // NULL is the legacy default stream, as for every other entry point
-  return prefill_impl(m, d_tokens, n, start_pos, chunk, d_logits, static_cast<cudaStream_t>(stream));
+  return prefill_call(m, d_tokens, n, start_pos, chunk, d_logits, static_cast<cudaStream_t>(stream));
 }
 
 int pp_prefill(pp_model* m, const int32_t* tokens, int32_t n, int32_t start_pos, int32_t chunk, float* logits_out) {
@@ -1094,7 +1262,7 @@ int pp_prefill(pp_model* m, const int32_t* tokens, int32_t n, int32_t start_pos,
     }
   PP_CUDA(cudaMemcpyAsync(m->tok, tokens, sizeof(int32_t) * n, cudaMemcpyHostToDevice, m->stream));
   m->stats.h2d_bytes += (int64_t)sizeof(int32_t) * n;
-  PP_TRY(prefill_impl(m, m->tok, n, start_pos, chunk, m->logits, m->stream));
+  PP_TRY(prefill_call(m, m->tok, n, start_pos, chunk, m->logits, m->stream));
   PP_CUDA(cudaMemcpyAsync(logits_out, m->logits, sizeof(float) * m->cfg.vocab, cudaMemcpyDeviceToHost, m->stream));
   PP_CUDA(cudaStreamSynchronize(m->stream));
   PP_TRY(collect(m));
@@ -1202,6 +1370,19 @@ int pp_set_chunk_overlap(pp_model* m, int32_t enable) {
     m->sets_ready = true;
   }
   m->overlap = enable != 0;
+  return PP_OK;
+}
+
+int pp_set_graphs(pp_model* m, int32_t enable) {
+  if (!m || (enable != 0 && enable != 1)) {
+    set_err("bad pp_set_graphs arguments");
+    return PP_ERR_ARG;
+  }
+  if (!enable) {
+    PP_TRY(sync_model(m));
+    graphs_clear(m);
+  }
+  m->graphs = enable != 0;
   return PP_OK;
 }
 
@@ -1376,6 +1557,30 @@ TcWaits op_waits() {
 }
 }  // namespace
 
+// One tcgen05 GEMM of a single-step entry point, with its tensor maps made for the
+// call: k_gemm_tw for chunks of at most 128 rows, k_gemm_tc beyond (as in the model).
+// Programmatic early start, but no weight load before griddepcontrol.wait: a caller's
+// kernel may have written w just before the call.
+static cudaError_t op_tc_launch(int epi, const uint16_t* a16, const int8_t* w, const float* ws, const float* as, int m,
+                                int n, int k, float* out, int ldo, int32_t* acc, int* status, const TcWorkspace& wsp,
+                                cudaStream_t st, const TcWaits& waits) {
+  CUtensorMap ma, mw;
+  const __half* a = reinterpret_cast<const __half*>(a16);
+  cudaError_t e;
+  if (m <= kTwMaxRows) {
+    const int nt = tw_nt(m);
+    if ((e = make_tmap_tw_tokens(&ma, a, m, k, nt)) != cudaSuccess) return e;
+    if ((e = make_tmap_tw_weights(&mw, w, n, k)) != cudaSuccess) return e;
+    return launch_gemm_tw(epi, ma, mw, nt, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), status, wsp, st, waits,
+                          TcRope{}, false, true, /*early_w=*/false);
+  }
+  const int bn = tc_bn(m, n, k);
+  if ((e = make_tmap_a(&ma, a, m, k)) != cudaSuccess) return e;
+  if ((e = make_tmap_w(&mw, w, n, k, bn)) != cudaSuccess) return e;
+  return launch_gemm_tc(epi, ma, mw, bn, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), status, wsp, st, waits,
+                        TcRope{}, false, true, /*early_w=*/false);
+}
+
 // Process-wide stream-K workspace of pp_op_gemm / pp_op_gemm_acc, grown on
 // demand (growing synchronises the device) and kept until exit.
 static std::mutex g_op_ws_mu;
@@ -1383,7 +1588,7 @@ static TcWorkspace g_op_ws;
 
 static cudaError_t op_workspace(int m, int n, int k, TcWorkspace* out) {
   size_t part = 0, cnt = 0;
-  tc_workspace_need(m, n, k, &part, &cnt);
+  gemm_workspace_need(m, n, k, &part, &cnt);
   std::lock_guard<std::mutex> lk(g_op_ws_mu);
   if (part > g_op_ws.part_bytes || cnt > g_op_ws.counters) {
     if (g_op_ws.part) cudaFree(g_op_ws.part);
@@ -1409,17 +1614,9 @@ static int op_gemm_launch(int32_t engine, int epi, const int8_t* a8, const uint1
   if (engine == PP_GEMM_MMA) return ok_launch(launch_gemm_mma(epi, a8, w, ws, as, m, n, k, out, ldo, acc, st), "gemm");
   StaticScratch sc;
   PP_TRY(static_scratch(&sc));
-  CUtensorMap ma, mw;
-  PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
-  const int bn = tc_bn(m, n, k);
-  PP_CUDA(make_tmap_w(&mw, w, n, k, bn));
   TcWorkspace wsp;
   PP_CUDA(op_workspace(m, n, k, &wsp));
-  // programmatic early start, but no weight load before griddepcontrol.wait:
-  // a caller's kernel may have written w just before this call
-  return ok_launch(launch_gemm_tc(epi, ma, mw, bn, ws, as, m, n, k, out, ldo, acc, g_tc_seg.load(), sc.status, wsp,
-                                  st, op_waits(), TcRope{}, false, true, /*early_w=*/false),
-                   "gemm");
+  return ok_launch(op_tc_launch(epi, a16, w, ws, as, m, n, k, out, ldo, acc, sc.status, wsp, st, op_waits()), "gemm");
 }
 
 int pp_op_gemm_acc(int32_t engine, const int8_t* a8, const uint16_t* a16, const int8_t* w, int32_t m, int32_t n,
@@ -1486,7 +1683,7 @@ int pp_op_gemm_noalloc_need(int32_t m, int32_t n, int32_t k, int64_t* part_bytes
     return PP_ERR_UNSUPPORTED;
   }
   size_t pb = 0, cc = 0;
-  tc_workspace_need(m, n, k, &pb, &cc);
+  gemm_workspace_need(m, n, k, &pb, &cc);
   *part_bytes = (int64_t)pb;
   *counters = (int64_t)cc;
   return PP_OK;
@@ -1502,7 +1699,7 @@ int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, c
     return PP_ERR_ARG;
   }
   size_t need_part = 0, need_cnt = 0;
-  tc_workspace_need(m, n, k, &need_part, &need_cnt);
+  gemm_workspace_need(m, n, k, &need_part, &need_cnt);
   if (need_part > kStaticPartBytes || need_cnt > (size_t)kStaticCounters) {
     set_err("GEMM m=%d n=%d k=%d needs %zu bytes of scratch and %zu counters; the fixed scratch holds %zu bytes and %d",
             m, n, k, need_part, need_cnt, kStaticPartBytes, kStaticCounters);
@@ -1513,17 +1710,13 @@ int pp_op_gemm_noalloc(int32_t epilogue, const uint16_t* a16, const int8_t* w, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: counters must start at zero
   if (need_cnt) PP_CUDA(cudaMemsetAsync(sc.cnt, 0, need_cnt * sizeof(int), st));
-  CUtensorMap ma, mw;
-  PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
-  const int bn = tc_bn(m, n, k);
-  PP_CUDA(make_tmap_w(&mw, w, n, k, bn));
   TcWorkspace wsp;
   wsp.part = sc.part;
   wsp.part_bytes = kStaticPartBytes;
   wsp.cnt = sc.cnt;
   wsp.counters = kStaticCounters;
-  return ok_launch(launch_gemm_tc(epilogue, ma, mw, bn, w_scale, a_scale, m, n, k, out, ldo, nullptr, g_tc_seg.load(),
-                                  sc.status, wsp, st, op_waits(), TcRope{}, false, true, /*early_w=*/false),
+  return ok_launch(op_tc_launch(epilogue, a16, w, w_scale, a_scale, m, n, k, out, ldo, nullptr, sc.status, wsp, st,
+                                op_waits()),
                    "gemm_noalloc");
 }
 
@@ -1554,10 +1747,6 @@ int pp_debug_gemm_stall(int32_t wait_us, const uint16_t* a16, const int8_t* w, i
   int dev = 0, khz = 0;
   PP_CUDA(cudaGetDevice(&dev));
   PP_CUDA(cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev));
-  CUtensorMap ma, mw;
-  PP_CUDA(make_tmap_a(&ma, reinterpret_cast<const __half*>(a16), m, k));
-  const int bn = tc_bn(m, n, k);
-  PP_CUDA(make_tmap_w(&mw, w, n, k, bn));
   int* status = nullptr;
   PP_CUDA(cudaMalloc(&status, sizeof(int)));
   cudaError_t e = cudaMemset(status, 0, sizeof(int));
@@ -1565,8 +1754,7 @@ int pp_debug_gemm_stall(int32_t wait_us, const uint16_t* a16, const int8_t* w, i
   waits.cycles = (long long)wait_us * (khz > 0 ? khz : 2000000) / 1000;  // kHz -> cycles per microsecond
   waits.hold_mma = 1;
   if (e == cudaSuccess)  // no stream-K workspace: whole tiles, no counters left behind
-    e = launch_gemm_tc(EPI_ACC, ma, mw, bn, nullptr, nullptr, m, n, k, nullptr, n, acc, g_tc_seg.load(), status,
-                       TcWorkspace{}, nullptr, waits);
+    e = op_tc_launch(EPI_ACC, a16, w, nullptr, nullptr, m, n, k, nullptr, n, acc, status, TcWorkspace{}, nullptr, waits);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   int st = 0;
   if (e == cudaSuccess) e = cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost);

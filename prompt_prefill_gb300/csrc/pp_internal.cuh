@@ -94,6 +94,25 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& ma, const CUtensorMap& mw
                            const TcRope& rope = TcRope{}, bool wide = false, bool pdl = true, bool early_w = false);
 constexpr int kTcSegK = 1024;  // 1024 * 127^2 < 2^24: every f32 partial sum of a segment is an exact integer
 
+// tcgen05 engine for chunks of at most 128 rows (k_gemm_tw.cu): the weights are the MMA's M side
+// (256 weight rows per CTA pair, converted into tensor memory) and the chunk's tokens its N side
+// (NT = tw_nt(m) = 32, 64 or 128). Same operands, segments, workspace, waits and epilogues as
+// launch_gemm_tc; the token map's box is made for one NT, the weight map for every launch.
+constexpr int kTwNt[3] = {128, 64, 32};
+constexpr int kTwMaxRows = 128;
+int tw_nt(int m);
+inline int tw_nt_index(int m) {
+  const int nt = tw_nt(m);
+  return nt == 128 ? 0 : (nt == 64 ? 1 : 2);
+}
+cudaError_t make_tmap_tw_tokens(CUtensorMap* map, const __half* a16, int rows, int k, int nt);
+cudaError_t make_tmap_tw_weights(CUtensorMap* map, const int8_t* w, int n, int k);
+void tw_workspace_need(int m, int n, int k, size_t* part_bytes, size_t* counters);
+cudaError_t launch_gemm_tw(int epi, const CUtensorMap& mt, const CUtensorMap& mw, int nt, const float* ws,
+                           const float* as, int m, int n, int k, float* out, int ldo, int32_t* acc, int seg_k,
+                           int* status, const TcWorkspace& wsp, cudaStream_t s, const TcWaits& waits = TcWaits{},
+                           const TcRope& rope = TcRope{}, bool wide = false, bool pdl = true, bool early_w = false);
+
 // ---- attention (k_attention.cu)
 // Keys per range of the attention work split, at fixed absolute positions.
 constexpr int kAttnRange = 512;

@@ -66,7 +66,7 @@ def test_peaks_and_alu_peak():
              "source": "measured"}
     assert bench.peak_for("tensor", peaks)[0] == 1715.2
     assert bench.peak_for("hbm", peaks)[0] == 6790.7
-    assert abs(bench.peak_for("alu", peaks)[0] - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+    assert abs(bench.peak_for("alu", peaks, sms=152)[0] - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
 
 
 def test_clock_sampler_without_nvidia_smi(monkeypatch):

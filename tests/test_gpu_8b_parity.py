@@ -4,16 +4,16 @@ configuration the benchmark times.
 A 2-layer decoder with the Llama-3-8B shapes (dim 4096, FFN 14336, 32 query
 heads over 8 KV heads of 128, RoPE theta 5e5; a smaller vocabulary) runs
 1024 tokens in chunks of 512 with chunk overlap on and the tcgen05 engine (the
-benchmark's policy: the chunks on their own streams, every GEMM at its widest
-tile), then a continuation call of 512 tokens at position 1024, whose
-attention merges two key ranges and whose single chunk takes the serial tile
-rule (the stream-K down projection among them).
+benchmark's policy: the chunks on their own streams, no stream-K), then a
+continuation call of 512 tokens at position 1024, whose attention merges two
+key ranges and whose single chunk takes the serial rule (the stream-K down
+projection among them).
 
 Checked ("Batched Prefill", section "Correctness": the batched path computes
 what the per-token path computes):
   - which GEMM instantiations ran (pp_stats.gemm_launches), so the test
-    provably covers the QKV/RoPE, SwiGLU and residual kernels at width 256
-    that the benchmark launches;
+    provably covers the QKV/RoPE, SwiGLU and residual kernels with the
+    256 x 256 tiles that the benchmark launches;
   - layer by layer against the oracle with codes forced at tie decisions
     (bit-exact residual rows, K/V rows within f32 rounding), on both calls;
   - the final logits from the GPU's last row within 1e-2 x std of the oracle's,
@@ -50,7 +50,9 @@ def test_8b_dims_chunk_overlap_matches_oracle():
             launches.append(g.stats()["gemm_launches"])
         kv_ref = [g.kv(L, which, 0, CFG.prompt_len) for L in range(CFG.n_layers) for which in (0, 1)]
         L2 = CFG.n_layers * 2  # layers x chunks of the first call
-        assert launches[0] == {(4, 256): L2, (2, 256): L2, (1, 256): 2 * L2}, launches[0]
+        # 512-row chunks with chunk overlap: 256-token x 256-weight-row tiles for every projection
+        T = (256, 256)
+        assert launches[0] == {(4, T): L2, (2, T): L2, (1, T): 2 * L2}, launches[0]
         # the continuation's single chunk: serial tile rule, one launch per projection and layer
         by_epi = {}
         for (e, _), v in launches[1].items():

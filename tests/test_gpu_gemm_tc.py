@@ -37,10 +37,15 @@ def _acc(torch, engine, a, w):
 TC_SHAPES = [(1, 256, 64), (8, 768, 256), (37, 256, 768), (130, 512, 320), (200, 2048, 1024), (300, 512, 4096),
              (512, 1024, 14336), (600, 768, 2048), (33, 384, 704)]
 
-# One shape per tile width on 76 CTA pairs: a weight-row tile of 256 (76 tiles
-# of 256 cost as much as 152 of 128), of 192 (76 tiles of 192 beat 114 of 128)
-# and of 128 (few tiles).
-WIDTH_SHAPES = [(16, 19456, 128), (40, 14592, 192), (290, 512, 1024)]
+# Both tcgen05 kernels and every tile: chunks of at most 128 rows run 256
+# weight rows x 32 / 64 / 128 tokens (weights in tensor memory), longer chunks
+# 256 tokens x 256 / 192 / 128 weight rows; with whole tiles and with stream-K
+# partial tiles (few tiles and long k on 76 CTA pairs): the 350M down projection
+# at a 32-row chunk, a 64-row chunk over k = 8192, the 8B down projection at
+# 512 rows, and a ragged 300-row chunk with k not a multiple of the 1024-k
+# segment.
+WIDTH_SHAPES = [(16, 19456, 128), (40, 14592, 192), (290, 512, 1024), (32, 1024, 4096), (64, 2048, 8192),
+                (512, 4096, 14336), (512, 28672, 4096), (300, 4096, 2880), (100, 4096, 4096)]
 
 
 @pytest.mark.parametrize("m,n,k", TC_SHAPES)
@@ -90,7 +95,7 @@ def test_tc_and_mma_engines_agree_at_8b_shapes(torch):
 
 
 @pytest.mark.parametrize("m,n,k", WIDTH_SHAPES)
-def test_tc_acc_bit_exact_every_tile_width(torch, m, n, k):
+def test_tc_acc_bit_exact_every_token_tile(torch, m, n, k):
     a = synth.uniform_i8(88, m + k, (m, k))
     w = synth.uniform_i8(88, n + k, (n, k))
     assert np.array_equal(_acc(torch, TC, a, w), oracle.gemm_i8(a, w))
