@@ -715,6 +715,77 @@ def run_streamed(args, cfg, world, rank, local, pg):
 
 
 # ----------------------------------------------------------------------------- one kernel
+def graph_ms_per_launch(launch, n: int, reps: int = 5) -> float:
+    """Replay `n` launches captured in one CUDA graph and return the best average device time per launch
+    (CUDA events on the replay stream): the host's launch path is out of the figure, the gap between two
+    kernels is in it, as in a model step."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        launch(0)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(n):
+            launch(i)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) / n)
+    del graph
+    return best
+
+
+def run_row_op(args, peaks):
+    """The per-token quantiser (--op quant) or RMSNorm + quantiser (--op norm_quant) over --m rows of --k,
+    int8 and fp16 codes and the row scale written. Timed as graph replays of max(--steps, 96) launches:
+    with the inputs rotating through more than twice the L2 (every launch reads its rows from HBM; the
+    reported figure) and with one input that stays in L2 (the model's case: the previous kernel has just
+    written the rows). A torch f32 -> fp16 copy of the same rows is timed the same way for context."""
+    import torch
+
+    import prompt_prefill_gb300 as pp
+
+    m, k = args.m, args.k
+    n = max(args.steps, 96)
+    nbuf = max(2, -(-(2 * 129 * 2**20) // (4 * m * k)))
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    xs = [torch.randn((m, k), device="cuda", generator=gen) for _ in range(nbuf)]
+    g = 1.0 + 0.02 * torch.randn((k,), device="cuda", generator=gen)
+    q8 = torch.empty((m, k), dtype=torch.int8, device="cuda")
+    q16 = torch.empty((m, k), dtype=torch.float16, device="cuda")
+    asc = torch.empty((m,), device="cuda")
+    if args.op == "norm_quant":
+        def op(x):
+            pp.pp_op_rmsnorm_quantize(x, g, m, k, 1e-5, None, q8, q16, asc)
+    else:
+        def op(x):
+            pp.pp_op_quantize(x, m, k, q8, q16, asc)
+    ms_hbm = graph_ms_per_launch(lambda i: op(xs[i % nbuf]), n)
+    ms_l2 = graph_ms_per_launch(lambda i: op(xs[0]), n)
+    ms_copy = graph_ms_per_launch(lambda i: q16.copy_(xs[i % nbuf]), n)
+    # bytes the kernel must move: f32 rows in, int8 + fp16 codes and the row scale out (+ the gains)
+    work = m * (4 * k + k + 2 * k + 4) + (4 * k if args.op == "norm_quant" else 0)
+    achieved = work / (ms_hbm / 1000) / 1e9
+    peak, src = peak_for("hbm", peaks)
+    print(json.dumps({"op": args.op, "m": m, "k": k, "launches_per_graph": n, "input_buffers": nbuf,
+                      "ms": ms_hbm, "achieved": achieved, "unit": "GB/s", "peak": peak, "frac": achieved / peak,
+                      "peak_source": src, "bytes_per_launch": work, "ms_l2_resident": ms_l2,
+                      "achieved_l2_resident": work / (ms_l2 / 1000) / 1e9,
+                      "ms_torch_f32_to_f16_copy": ms_copy}), flush=True)
+    return 0
+
+
 def run_op(args):
     """Time one kernel alone at a given shape (for ncu captures and per-kernel
     rooflines): --op gemm --engine 1|2 --m --n --k, --op attention --m
@@ -753,21 +824,7 @@ def run_op(args):
         pairs = sum(start + i + 1 for i in range(m))
         work, unit, bound = 4.0 * hd * H * pairs, "TFLOP/s", "alu"
     elif args.op in ("quant", "norm_quant"):
-        # per-token quantiser (and RMSNorm before it) over m rows of k; writes int8 and fp16 codes
-        x = torch.randn((m, k), device="cuda")
-        g = 1.0 + 0.02 * torch.randn((k,), device="cuda")
-        q8 = torch.empty((m, k), dtype=torch.int8, device="cuda")
-        q16 = torch.empty((m, k), dtype=torch.float16, device="cuda")
-        asc = torch.empty((m,), device="cuda")
-        if args.op == "norm_quant":
-            def once():
-                pp.pp_op_rmsnorm_quantize(x, g, m, k, 1e-5, None, q8, q16, asc)
-        else:
-            def once():
-                pp.pp_op_quantize(x, m, k, q8, q16, asc)
-        # bytes the kernel must move: f32 rows in, int8 + fp16 codes and the row scale out (+ the gains)
-        work = m * (4 * k + k + 2 * k + 4) + (4 * k if args.op == "norm_quant" else 0)
-        unit, bound = "GB/s", "hbm"
+        return run_row_op(args, peaks)
     else:
         raise SystemExit(f"unknown --op {args.op}")
     for _ in range(args.warmup):

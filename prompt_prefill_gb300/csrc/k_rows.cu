@@ -3,6 +3,8 @@
 // output projection. All are HBM/L2-bound; each keeps every per-row reduction
 // in one fixed order so that a row's result never depends on which other rows
 // share its launch (the chunk size).
+#include <cfloat>
+
 #include "pp_internal.cuh"
 
 namespace pp {
@@ -49,17 +51,90 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
+// Maximum that returns NaN when either operand is NaN (fmaxf ignores a NaN).
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ float block_max_nan(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowThreads / 32; ++i) m = max_nan(m, red[i]);
+  return m;
+}
+
+// Codes by IEEE addition. For a finite row with amax > 0 and inv = 127/amax
+// finite, every v = y * inv has |v| <= 127 (1 + 2^-24)^2 < 127.5, so the
+// clamp of the quantiser never acts. kCodeMagic = 1.5 * 2^23 + 0x6600 is an
+// even integer in [2^23, 2^24), where the f32 grid is the integers: the
+// round-to-nearest-even sum kCodeMagic + v is exactly kCodeMagic + q with
+// q = rint_even(v), so its low 16 bits are 0x6600 + q, the fp16 bits of
+// 1536 + q (fp16 spacing is 1 on [1024, 2048)), and its low byte is q in two's
+// complement. Two sums give a half2 of 1536 + q by one byte permute; the fp16
+// subtraction of 1536 is exact (Sterbenz), leaving q. No conversion instruction
+// is needed.
+constexpr float kCodeMagic = 12609024.0f;  // 0x4B406600
+
+struct Codes4 {
+  uint32_t q8;  // four int8 codes
+  uint2 q16;    // four fp16 codes
+};
+
+__device__ __forceinline__ Codes4 codes_fast(const float y[4], float inv) {
+  uint32_t u[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) u[e] = __float_as_uint(__fadd_rn(__fmul_rn(y[e], inv), kCodeMagic));
+  const uint32_t h01 = __byte_perm(u[0], u[1], 0x5410), h23 = __byte_perm(u[2], u[3], 0x5410);
+  const __half2 off = __float2half2_rn(1536.0f);
+  __half2 a = *reinterpret_cast<const __half2*>(&h01), b = *reinterpret_cast<const __half2*>(&h23);
+  a = __hsub2(a, off);
+  b = __hsub2(b, off);
+  Codes4 c;
+  c.q8 = __byte_perm(h01, h23, 0x6420);
+  c.q16 = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  return c;
+}
+
+// The quantiser's definition written out, for rows the fast form does not
+// cover (a non-finite element, or amax so small that 127/amax overflows).
+__device__ __forceinline__ Codes4 codes_exact(const float y[4], float inv, bool zero) {
+  int qi[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int q = zero ? 0 : __float2int_rn(__fmul_rn(y[e], inv));
+    qi[e] = q > 127 ? 127 : (q < -127 ? -127 : q);
+  }
+  Codes4 c;
+  c.q8 = (uint32_t)(uint8_t)qi[0] | (uint32_t)(uint8_t)qi[1] << 8 | (uint32_t)(uint8_t)qi[2] << 16 |
+         (uint32_t)(uint8_t)qi[3] << 24;
+  const __half2 a = __halves2half2(__int2half_rn(qi[0]), __int2half_rn(qi[1]));
+  const __half2 b = __halves2half2(__int2half_rn(qi[2]), __int2half_rn(qi[3]));
+  c.q16 = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  return c;
+}
+
 // RMSNorm (optional) then the per-token absmax quantiser ("Batched Prefill",
 // "The Solution": quantise each token once per chunk; every output row reuses
 // the codes). One CTA per row:
 //   r = 1 / sqrt(sum(x^2)/k + eps), y = (x * r) * g            (NORM only)
 //   amax = max|y|, inv = 127/amax, q = clamp(rint_even(y*inv), +-127), a_scale = amax/127
 // All f32 with IEEE division and square root; amax == 0 gives q = 0, a_scale = 0.
+// amax is reduced with a NaN-propagating maximum: a finite row whose inv is
+// finite takes the conversion-free codes (codes_fast); any other row (NaN or
+// infinity in it, or a tiny amax) recomputes amax ignoring NaN and takes the
+// written-out definition, a branch uniform over the CTA. Both give the same
+// codes wherever both apply.
 // NV > 0: the thread's NV float4 of the row are loaded once and kept in
-// registers for all three passes (k <= 4 * NV * kRowThreads); NV == 0 streams
-// the row from memory in each pass (any k). Every pass visits the thread's
-// elements in the same order, so both forms give the same bits. q8 or q16 may
-// be null (that copy of the codes is not written).
+// registers for all passes (k <= 4 * NV * kRowThreads), and for NV <= 4 the
+// thread's norm weights are loaded with them; NV == 0 streams the row from
+// memory in each pass (any k). Every pass visits the thread's elements in the
+// same order, so all forms give the same bits. q8 or q16 may be null (that copy
+// of the codes is not written).
 template <bool NORM, int NV>
 __global__ void __launch_bounds__(kRowThreads)
     k_norm_quant(const float* __restrict__ x, int ldx, const float* __restrict__ g, int k, float eps,
@@ -67,13 +142,15 @@ __global__ void __launch_bounds__(kRowThreads)
                  float* __restrict__ a_scale) {
   ppdev::pdl_trigger();
   ppdev::pdl_wait();
-  __shared__ float red_sum[kRowThreads / 32], red_max[kRowThreads / 32];
+  __shared__ float red_sum[kRowThreads / 32], red_max[kRowThreads / 32], red_max2[kRowThreads / 32];
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
   const float4* g4 = reinterpret_cast<const float4*>(g);
   const int k4 = k >> 2;
   constexpr int NR = NV > 0 ? NV : 1;
-  float4 xv[NR];
+  constexpr bool GPRE = NORM && NV > 0 && NV <= 4;  // norm weights held in registers too
+  constexpr int NG = GPRE ? NR : 1;
+  float4 xv[NR], gv[NG];
   if (NV > 0) {
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
@@ -81,21 +158,30 @@ __global__ void __launch_bounds__(kRowThreads)
       if (c < k4) xv[j] = xr[c];
     }
   }
-  auto for_each = [&](auto&& f) {  // f(x[4c .. 4c+3], c) for this thread's c in increasing order
+  if (GPRE) {
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      const int c = threadIdx.x + j * kRowThreads;
+      if (c < k4) gv[j] = __ldg(g4 + c);
+    }
+  }
+  // f(x[4c .. 4c+3], g[4c .. 4c+3], c) for this thread's c in increasing order
+  auto for_each = [&](auto&& f) {
     if (NV > 0) {
 #pragma unroll
       for (int j = 0; j < NR; ++j) {
         const int c = threadIdx.x + j * kRowThreads;
-        if (c < k4) f(xv[j], c);
+        if (c < k4) f(xv[j], GPRE ? gv[GPRE ? j : 0] : (NORM ? __ldg(g4 + c) : make_float4(1.f, 1.f, 1.f, 1.f)), c);
       }
     } else {
-      for (int c = threadIdx.x; c < k4; c += kRowThreads) f(xr[c], c);
+      for (int c = threadIdx.x; c < k4; c += kRowThreads)
+        f(xr[c], NORM ? __ldg(g4 + c) : make_float4(1.f, 1.f, 1.f, 1.f), c);
     }
   };
   float r = 1.f;
   if (NORM) {
     float ss = 0.f;
-    for_each([&](const float4& v, int) {
+    for_each([&](const float4& v, const float4&, int) {
       ss = fmaf(v.x, v.x, ss);
       ss = fmaf(v.y, v.y, ss);
       ss = fmaf(v.z, v.z, ss);
@@ -104,36 +190,35 @@ __global__ void __launch_bounds__(kRowThreads)
     ss = block_sum(ss, red_sum);
     r = 1.0f / sqrtf(ss / (float)k + eps);
   }
-  auto yval = [&](float xv_, float gv) { return NORM ? __fmul_rn(__fmul_rn(xv_, r), gv) : xv_; };
+  auto yval = [&](float xv_, float gv_) { return NORM ? __fmul_rn(__fmul_rn(xv_, r), gv_) : xv_; };
   float amax = 0.f;
-  for_each([&](const float4& v, int c) {
-    const float4 gg = NORM ? g4[c] : make_float4(1.f, 1.f, 1.f, 1.f);
-    amax = fmaxf(amax, fabsf(yval(v.x, gg.x)));
-    amax = fmaxf(amax, fabsf(yval(v.y, gg.y)));
-    amax = fmaxf(amax, fabsf(yval(v.z, gg.z)));
-    amax = fmaxf(amax, fabsf(yval(v.w, gg.w)));
+  for_each([&](const float4& v, const float4& gg, int) {
+    amax = max_nan(amax, fabsf(yval(v.x, gg.x)));
+    amax = max_nan(amax, fabsf(yval(v.y, gg.y)));
+    amax = max_nan(amax, fabsf(yval(v.z, gg.z)));
+    amax = max_nan(amax, fabsf(yval(v.w, gg.w)));
   });
-  amax = block_max(amax, red_max);
+  amax = block_max_nan(amax, red_max);
+  float inv = amax == 0.f ? 0.f : 127.0f / amax;
+  const bool fast = amax <= FLT_MAX && inv <= FLT_MAX;  // false for NaN and infinity
+  if (!fast) {  // uniform over the CTA: amax as the definition takes it, NaN ignored
+    amax = 0.f;
+    for_each([&](const float4& v, const float4& gg, int) {
+      amax = fmaxf(amax, fabsf(yval(v.x, gg.x)));
+      amax = fmaxf(amax, fabsf(yval(v.y, gg.y)));
+      amax = fmaxf(amax, fabsf(yval(v.z, gg.z)));
+      amax = fmaxf(amax, fabsf(yval(v.w, gg.w)));
+    });
+    amax = block_max(amax, red_max2);
+    inv = amax == 0.f ? 0.f : 127.0f / amax;
+  }
   const bool zero = amax == 0.f;
-  const float inv = zero ? 0.f : 127.0f / amax;
-  for_each([&](const float4& v, int c) {
-    const float4 gg = NORM ? g4[c] : make_float4(1.f, 1.f, 1.f, 1.f);
-    float y[4] = {yval(v.x, gg.x), yval(v.y, gg.y), yval(v.z, gg.z), yval(v.w, gg.w)};
-    int qi[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      int q = zero ? 0 : __float2int_rn(__fmul_rn(y[e], inv));
-      qi[e] = q > 127 ? 127 : (q < -127 ? -127 : q);
-    }
+  for_each([&](const float4& v, const float4& gg, int c) {
+    const float y[4] = {yval(v.x, gg.x), yval(v.y, gg.y), yval(v.z, gg.z), yval(v.w, gg.w)};
+    const Codes4 q = fast ? codes_fast(y, inv) : codes_exact(y, inv, zero);
     const size_t base = (size_t)row * k + 4 * (size_t)c;
-    char4 p = make_char4((signed char)qi[0], (signed char)qi[1], (signed char)qi[2], (signed char)qi[3]);
-    if (q8) *reinterpret_cast<char4*>(q8 + base) = p;
-    if (q16) {
-      __half2 h01 = __halves2half2(__int2half_rn(qi[0]), __int2half_rn(qi[1]));
-      __half2 h23 = __halves2half2(__int2half_rn(qi[2]), __int2half_rn(qi[3]));
-      reinterpret_cast<__half2*>(q16 + base)[0] = h01;
-      reinterpret_cast<__half2*>(q16 + base)[1] = h23;
-    }
+    if (q8) *reinterpret_cast<uint32_t*>(q8 + base) = q.q8;
+    if (q16) *reinterpret_cast<uint2*>(q16 + base) = q.q16;
     if (y_out) reinterpret_cast<float4*>(y_out + base)[0] = make_float4(y[0], y[1], y[2], y[3]);
   });
   if (threadIdx.x == 0) a_scale[row] = zero ? 0.f : amax / 127.0f;

@@ -49,6 +49,46 @@ def test_quantize_ties_hand_case(torch):
     assert q8.tolist() == [[127, 2, 4, -2, 0, -126, 0, 2]] and s.tolist() == [1.0]
 
 
+@pytest.mark.parametrize("k", [4096, 14336, 20000])  # codes kept in registers (two widths) and streamed
+def test_quantize_every_tie_and_neighbour(torch, k):
+    # amax = 127 makes inv = 1, so y * inv = y: every half-integer in [-127, 127] is a tie, and its float
+    # neighbours on either side round away from it; the rest of the row is random
+    ties = np.arange(-127, 127, dtype=np.float64) + 0.5
+    vals = np.concatenate([ties, np.nextafter(ties.astype(np.float32), np.float32(np.inf)),
+                           np.nextafter(ties.astype(np.float32), np.float32(-np.inf)), [127.0, -127.0, 0.0, -0.0]])
+    x = synth.normal_f32(23, k, (3, k), 0.0, 40.0)
+    x = np.clip(x, -127.0, 127.0).astype(np.float32)
+    for r in range(3):
+        x[r, r:r + vals.size] = vals
+    q8, q16, s = _quantize_gpu(torch, x)
+    rq, rs = oracle.quantize_rows(x)
+    assert np.array_equal(q8, rq)
+    assert np.array_equal(bits(s), bits(rs)) and s.tolist() == [1.0, 1.0, 1.0]
+    assert np.array_equal(bits(q16), bits(rq.astype(np.float16)))  # +0 for every zero code
+
+
+@pytest.mark.parametrize("k", [4096, 14336, 20000])
+def test_quantize_tiny_and_non_finite_rows(torch, k):
+    # rows outside the conversion-free form: amax below 127 / FLT_MAX (127 / amax overflows to inf, every
+    # nonzero code saturates), an infinity (inv = 0) and a NaN (ignored by amax). The definition leaves the
+    # code of a NaN product undefined, so those positions are not compared.
+    rng = np.random.default_rng(24)
+    x = synth.normal_f32(24, k, (4, k), 0.0, 1.0)
+    x[0] = (rng.uniform(1e-38, 3e-37, k) * rng.choice([-1.0, 1.0], k)).astype(np.float32)
+    x[0, 5] = 0.0
+    x[1, 7] = np.inf
+    x[2, k - 3] = np.nan
+    x[3, 11] = -np.inf
+    q8, q16, s = _quantize_gpu(torch, x)
+    rq, rs = oracle.quantize_rows(x)
+    defined = np.isfinite(x)
+    assert np.array_equal(q8[defined], rq[defined])
+    assert np.array_equal(q16[defined].astype(np.float32), rq[defined].astype(np.float32))
+    assert np.array_equal(bits(s), bits(rs))
+    assert set(np.unique(q8[0])) == {-127, 0, 127} and q8[0, 5] == 0
+    assert np.isinf(s[1]) and np.isinf(s[3]) and np.isfinite(s[2])
+
+
 @pytest.mark.parametrize("rows,k", [(3, 256), (17, 1024), (9, 4096)])
 def test_rmsnorm_quantize(torch, rows, k):
     x = synth.normal_f32(22, k, (rows, k), 0.0, 3.0)
