@@ -312,6 +312,34 @@ int pp_op_gemm(int32_t engine, int32_t epilogue, const int8_t* a8, const uint16_
                const float* w_scale, const float* a_scale, int32_t m, int32_t n, int32_t k, float* out,
                int32_t ldo, void* stream);
 
+/* ------------------------------------------------------ host-buffer checks
+ * The bit-exact steps on host buffers, for a caller without a device memory
+ * library ("Batched Prefill", "Correctness": the batched GEMM is checked bit for
+ * bit against per-token dot products). Each call copies its inputs into device
+ * memory it allocates, runs the library's kernels on the legacy default stream,
+ * waits for them, copies the results into the caller's buffers and frees what it
+ * allocated. Every pointer is caller-owned host memory; nothing is kept after the
+ * call. The GEMMs run on the tcgen05 engine when n % 128 == 0 and on the mma.sync
+ * engine otherwise (both give the same bits). Errors: PP_ERR_ARG (a null
+ * pointer, a size <= 0, k % 4 for the quantiser, k % 64 or n % 32 for the GEMMs),
+ * PP_ERR_OOM, PP_ERR_CUDA, PP_ERR_DEVICE_TIMEOUT (a bounded wait of the tcgen05
+ * GEMM gave up). After an error the outputs are untouched. */
+
+/* pp_op_quantize on host rows: x [rows][k] f32 in; q [rows][k] int8 and
+ * a_scale [rows] f32 out. */
+int pp_debug_quantize(const float* x, int32_t rows, int32_t k, int8_t* q, float* a_scale);
+
+/* acc[t][r] = sum_i a[t][i] * w[r][i] as int32: a [m][k], w [n][k] int8 in,
+ * acc [m][n] int32 out. */
+int pp_debug_gemm_i8(const int8_t* a, const int8_t* w, int32_t m, int32_t n, int32_t k, int32_t* acc);
+
+/* The dequantising epilogue on the same GEMM: out[t][r] =
+ * (float(acc[t][r]) * w_scale[r]) * a_scale[t], then, if resid is not NULL,
+ * out[t][r] = resid[t][r] + out[t][r] (the residual epilogue), all in f32 with
+ * round-to-nearest. w_scale [n], a_scale [m], resid and out [m][n] f32. */
+int pp_debug_gemm_epilogue(const int8_t* a, const int8_t* w, const float* w_scale, const float* a_scale,
+                           const float* resid, int32_t m, int32_t n, int32_t k, float* out);
+
 /* K-extent of one exact f32 accumulation segment of the tcgen05 engine
  * (process-wide; default and maximum 1024, multiple of 64). Partial sums of
  * up to 1024 products of int8 values stay below 2^24 and are exact in f32;

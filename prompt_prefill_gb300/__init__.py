@@ -113,6 +113,9 @@ SIGNATURES = {
     "pp_debug_alloc_cap": ([ctypes.c_int64], ctypes.c_int),
     "pp_op_status": ([_vp], ctypes.c_int),
     "pp_debug_op_stall": ([_i32], ctypes.c_int),
+    "pp_debug_quantize": ([_vp, _i32, _i32, _vp, _vp], ctypes.c_int),
+    "pp_debug_gemm_i8": ([_vp, _vp, _i32, _i32, _i32, _vp], ctypes.c_int),
+    "pp_debug_gemm_epilogue": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp], ctypes.c_int),
     "pp_op_gemm_noalloc_need": ([_i32, _i32, _i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)],
                                 ctypes.c_int),
     "pp_debug_noalloc_poison": ([_i32], ctypes.c_int),
@@ -339,6 +342,44 @@ def pp_op_status(stream=None) -> int:
 
 def pp_debug_op_stall(wait_us: int):
     _check(lib().pp_debug_op_stall(wait_us), "pp_debug_op_stall")
+
+
+def pp_debug_quantize(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """The quantiser on host rows (x [rows][k] f32): (int8 codes, f32 row scales)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, k = x.shape
+    q = np.empty((rows, k), np.int8)
+    s = np.empty((rows,), np.float32)
+    _check(lib().pp_debug_quantize(_ptr(x), rows, k, _ptr(q), _ptr(s)), "pp_debug_quantize")
+    return q, s
+
+
+def pp_debug_gemm_i8(a: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """acc[t][r] = sum_i a[t][i] w[r][i] (int32) from host int8 a [m][k], w [n][k]."""
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    (m, k), n = a.shape, w.shape[0]
+    assert w.shape[1] == k
+    acc = np.empty((m, n), np.int32)
+    _check(lib().pp_debug_gemm_i8(_ptr(a), _ptr(w), m, n, k, _ptr(acc)), "pp_debug_gemm_i8")
+    return acc
+
+
+def pp_debug_gemm_epilogue(a: np.ndarray, w: np.ndarray, w_scale: np.ndarray, a_scale: np.ndarray,
+                           resid: np.ndarray | None = None) -> np.ndarray:
+    """(float(acc) * w_scale[r]) * a_scale[t] (+ resid[t][r]) from host buffers, f32 [m][n]."""
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    ws = np.ascontiguousarray(w_scale, dtype=np.float32)
+    as_ = np.ascontiguousarray(a_scale, dtype=np.float32)
+    (m, k), n = a.shape, w.shape[0]
+    assert w.shape[1] == k and ws.shape == (n,) and as_.shape == (m,)
+    r = None if resid is None else np.ascontiguousarray(resid, dtype=np.float32)
+    assert r is None or r.shape == (m, n)
+    out = np.empty((m, n), np.float32)
+    _check(lib().pp_debug_gemm_epilogue(_ptr(a), _ptr(w), _ptr(ws), _ptr(as_), _ptr(r), m, n, k, _ptr(out)),
+           "pp_debug_gemm_epilogue")
+    return out
 
 
 def pp_op_gemm_noalloc_need(m: int, n: int, k: int) -> tuple[int, int]:

@@ -308,6 +308,13 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
+// int8 codes widened to fp16 (every integer in [-128, 127] is an fp16 value):
+// the tcgen05 engine's activation operand for codes that arrive as int8.
+__global__ void k_widen_i8(const int8_t* __restrict__ a, long long n, __half* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    out[i] = __int2half_rn(a[i]);
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -343,6 +350,11 @@ cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows,
     else go(k_norm_quant<false, 0>);
   }
   return e;
+}
+
+cudaError_t launch_widen_i8(const int8_t* a, long long n, __half* out, cudaStream_t s) {
+  k_widen_i8<<<sm_count() * 8, 256, 0, s>>>(a, n, out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s) {

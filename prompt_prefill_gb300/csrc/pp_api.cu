@@ -575,8 +575,7 @@ int load_impl(pp_model* m, const pp_weights* w) {
   PP_CUDA(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
   PP_CUDA(cudaEventCreateWithFlags(&m->done, cudaEventDisableTiming));
   m->lay = make_layout(c);
-  const size_t D = c.dim, V = c.vocab, QD = (size_t)c.n_heads * c.head_dim,
-               QKV = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, F = c.ffn, MC = c.max_chunk;
+  const size_t D = c.dim, V = c.vocab;
   const size_t KVE = (size_t)c.n_layers * c.max_seq * c.n_kv_heads * c.head_dim;
 
   // global tensors
@@ -1191,6 +1190,82 @@ int prefill_call(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
 }  // namespace
 
 // =====================================================================  C ABI
+// ---------------------------------------------------------------- host-buffer checks
+namespace {
+// Device copies of one call's buffers, freed when the call returns.
+class DeviceScratch {
+ public:
+  DeviceScratch() = default;
+  DeviceScratch(const DeviceScratch&) = delete;
+  DeviceScratch& operator=(const DeviceScratch&) = delete;
+  ~DeviceScratch() {
+    for (void* p : bufs_) cudaFree(p);
+  }
+  template <class T>
+  int alloc(T** out, size_t n) {
+    void* p = nullptr;
+    const cudaError_t e = cudaMalloc(&p, std::max<size_t>(n * sizeof(T), 256));
+    if (e != cudaSuccess) {
+      set_err("cudaMalloc(%zu) failed: %s", n * sizeof(T), cudaGetErrorString(e));
+      return e == cudaErrorMemoryAllocation ? PP_ERR_OOM : PP_ERR_CUDA;
+    }
+    bufs_.push_back(p);
+    *out = static_cast<T*>(p);
+    return PP_OK;
+  }
+  template <class T>
+  int upload(T** out, const T* host, size_t n) {
+    PP_TRY(alloc(out, n));
+    PP_CUDA(cudaMemcpy(*out, host, n * sizeof(T), cudaMemcpyHostToDevice));
+    return PP_OK;
+  }
+
+ private:
+  std::vector<void*> bufs_;
+};
+
+// The GEMM of pp_debug_gemm_i8 (acc != NULL) or pp_debug_gemm_epilogue (out != NULL).
+int debug_gemm(const int8_t* a, const int8_t* w, const float* w_scale, const float* a_scale, const float* resid,
+               int32_t m, int32_t n, int32_t k, int32_t* acc, float* out) {
+  if (!a || !w || m <= 0 || n <= 0 || k <= 0 || k % 64 || n % 32 || (out && (!w_scale || !a_scale))) {
+    set_err("bad pp_debug_gemm arguments (k %% 64, n %% 32)");
+    return PP_ERR_ARG;
+  }
+  const int32_t engine = n % 128 == 0 ? PP_GEMM_TC : PP_GEMM_MMA;
+  const size_t mk = (size_t)m * k, mn = (size_t)m * n;
+  DeviceScratch d;
+  int8_t *da = nullptr, *dw = nullptr;
+  __half* da16 = nullptr;
+  PP_TRY(d.upload(&da, a, mk));
+  PP_TRY(d.upload(&dw, w, (size_t)n * k));
+  if (engine == PP_GEMM_TC) {
+    PP_TRY(d.alloc(&da16, mk));
+    PP_CUDA(launch_widen_i8(da, (long long)mk, da16, nullptr));
+  }
+  const uint16_t* a16 = reinterpret_cast<const uint16_t*>(da16);
+  if (acc) {
+    int32_t* dacc = nullptr;
+    PP_TRY(d.alloc(&dacc, mn));
+    PP_TRY(pp_op_gemm_acc(engine, da, a16, dw, m, n, k, dacc, nullptr));
+    if (engine == PP_GEMM_TC) PP_TRY(pp_op_status(nullptr));
+    PP_CUDA(cudaMemcpy(acc, dacc, mn * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    return PP_OK;
+  }
+  float *dws = nullptr, *das = nullptr, *dout = nullptr;
+  PP_TRY(d.upload(&dws, w_scale, (size_t)n));
+  PP_TRY(d.upload(&das, a_scale, (size_t)m));
+  if (resid) {
+    PP_TRY(d.upload(&dout, resid, mn));
+  } else {
+    PP_TRY(d.alloc(&dout, mn));
+  }
+  PP_TRY(pp_op_gemm(engine, resid ? PP_EPI_RESID : PP_EPI_STORE, da, a16, dw, dws, das, m, n, k, dout, n, nullptr));
+  if (engine == PP_GEMM_TC) PP_TRY(pp_op_status(nullptr));
+  PP_CUDA(cudaMemcpy(out, dout, mn * sizeof(float), cudaMemcpyDeviceToHost));
+  return PP_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* pp_status_str(int s) {
@@ -1662,6 +1737,43 @@ int pp_op_status(void* stream) {
   PP_CUDA(cudaStreamSynchronize(st));
   set_err("a bounded device wait of a single-step GEMM gave up");
   return PP_ERR_DEVICE_TIMEOUT;
+}
+
+
+// ---------------------------------------------------------------- host-buffer checks
+int pp_debug_quantize(const float* x, int32_t rows, int32_t k, int8_t* q, float* a_scale) {
+  if (!x || !q || !a_scale || rows <= 0 || k <= 0 || k % 4) {
+    set_err("bad pp_debug_quantize arguments");
+    return PP_ERR_ARG;
+  }
+  const size_t n = (size_t)rows * k;
+  DeviceScratch d;
+  float *dx = nullptr, *ds = nullptr;
+  int8_t* dq = nullptr;
+  PP_TRY(d.upload(&dx, x, n));
+  PP_TRY(d.alloc(&dq, n));
+  PP_TRY(d.alloc(&ds, (size_t)rows));
+  PP_TRY(pp_op_quantize(dx, rows, k, dq, nullptr, ds, nullptr));
+  PP_CUDA(cudaMemcpy(q, dq, n, cudaMemcpyDeviceToHost));
+  PP_CUDA(cudaMemcpy(a_scale, ds, (size_t)rows * sizeof(float), cudaMemcpyDeviceToHost));
+  return PP_OK;
+}
+
+int pp_debug_gemm_i8(const int8_t* a, const int8_t* w, int32_t m, int32_t n, int32_t k, int32_t* acc) {
+  if (!acc) {
+    set_err("null acc");
+    return PP_ERR_ARG;
+  }
+  return debug_gemm(a, w, nullptr, nullptr, nullptr, m, n, k, acc, nullptr);
+}
+
+int pp_debug_gemm_epilogue(const int8_t* a, const int8_t* w, const float* w_scale, const float* a_scale,
+                           const float* resid, int32_t m, int32_t n, int32_t k, float* out) {
+  if (!out) {
+    set_err("null out");
+    return PP_ERR_ARG;
+  }
+  return debug_gemm(a, w, w_scale, a_scale, resid, m, n, k, nullptr, out);
 }
 
 int pp_debug_op_stall(int32_t wait_us) {

@@ -31,6 +31,8 @@ cudaError_t launch_embed(const int32_t* tok, int n, const float* emb, int vocab,
 cudaError_t launch_norm_quant(const float* x, int ldx, const float* g, int rows, int k, float eps, float* y,
                               int8_t* q8, __half* q16, float* a_scale, cudaStream_t s, bool pdl = true);
 cudaError_t launch_rope_table(int max_pos, int hd, float theta, float* table, cudaStream_t s);
+// a [n] int8 -> out [n] fp16, exact.
+cudaError_t launch_widen_i8(const int8_t* a, long long n, __half* out, cudaStream_t s);
 // paired: the q and k head columns of qkv are in pair order (dims j and j + hd/2 at
 // columns 2j and 2j + 1 of the head), as the model's packed QKV weights produce them.
 cudaError_t launch_rope_kv(const float* qkv, int rows, int start_pos, int H, int Hkv, int hd, const float* table,

@@ -82,6 +82,17 @@ def test_host_side_validation_needs_no_device(libpp):
     assert libpp.pp_prefill(None, None, 4, 0, 8, None) == pp.PP_ERR_ARG
     assert libpp.pp_op_quantize(None, 1, 4, None, None, None, None) == pp.PP_ERR_ARG
     assert libpp.pp_op_gemm_acc(pp.PP_GEMM_MMA, None, None, None, 4, 32, 60, None, None) == pp.PP_ERR_ARG
+    # the host-buffer checks validate before allocating or copying anything
+    x = np.zeros((2, 6), np.float32)
+    q, s = np.zeros((2, 6), np.int8), np.zeros(2, np.float32)
+    assert libpp.pp_debug_quantize(x.ctypes.data, 2, 6, q.ctypes.data, s.ctypes.data) == pp.PP_ERR_ARG  # k % 4
+    a, w, acc = np.zeros((4, 64), np.int8), np.zeros((48, 64), np.int8), np.zeros((4, 48), np.int32)
+    assert libpp.pp_debug_gemm_i8(a.ctypes.data, w.ctypes.data, 4, 48, 64, acc.ctypes.data) == pp.PP_ERR_ARG  # n % 32
+    assert libpp.pp_debug_gemm_i8(a.ctypes.data, w.ctypes.data, 4, 32, 60, acc.ctypes.data) == pp.PP_ERR_ARG  # k % 64
+    assert libpp.pp_debug_gemm_i8(a.ctypes.data, w.ctypes.data, 4, 32, 64, None) == pp.PP_ERR_ARG
+    out = np.zeros((4, 32), np.float32)
+    assert libpp.pp_debug_gemm_epilogue(a.ctypes.data, w.ctypes.data, None, None, None, 4, 32, 64,
+                                        out.ctypes.data) == pp.PP_ERR_ARG  # scales missing
     bad = pp.make_config(100, 1, 4, 4, 64, 256, 10)  # dim % 64 != 0
     h = ctypes.c_void_p()
     assert libpp.pp_model_load(ctypes.byref(bad), None, ctypes.byref(h)) == pp.PP_ERR_ARG
