@@ -549,6 +549,14 @@ def run_ours(args, cfg, world, rank, local, pg):
     t_e2e = time.perf_counter() - t0
     t_e2e = max_over_ranks(pg, t_e2e)
     assert np.array_equal(host_logits.view(np.uint32), logits.view(np.uint32)), "host and device paths differ"
+    if args.profile_step:
+        # one more step, after everything timed, between cudaProfilerStart and cudaProfilerStop: the launch
+        # list of exactly one step under `ncu --profile-from-start off`
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
 
     value = replica_tok_per_s(world, P, args.steps, ms_max / 1000.0)
     e2e_value = replica_tok_per_s(world, P, args.steps, t_e2e)
@@ -864,6 +872,9 @@ def main(argv=None):
                     help="1 (default): consecutive chunks on eight streams (pp_set_chunk_overlap); 0: serial")
     ap.add_argument("--graphs", type=int, default=1,
                     help="1 (default): each prefill call replayed from a CUDA graph after its first (pp_set_graphs)")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="after the timed steps, run one more step between cudaProfilerStart and cudaProfilerStop "
+                         "(for ncu --profile-from-start off)")
     ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention | quant | norm_quant")
     ap.add_argument("--m", type=int, default=512)
     ap.add_argument("--n", type=int, default=28672)
