@@ -61,12 +61,15 @@ def logits_close(gpu: np.ndarray, ref: np.ndarray, tol: float = 1e-2):
     return err <= tol * std, err / std, int(np.argmax(gpu)) == top_ref, gap / std
 
 
-def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3, calls=None):
+def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3, calls=None, layers=None):
     """Verify a GPU prefill layer by layer against the oracle.
 
     calls: the prefill calls that cover toks, as (start_pos, n, chunk) in
     position order (default: one call of every token from position 0); later
     calls continue the K/V cache of earlier ones, on both sides.
+    layers: the layers the oracle checks (default: all). Each checked layer
+    runs on the GPU's own input rows, so any subset is a valid check of those
+    layers while the GPU runs the whole model.
 
     The GPU runs with its trace on (residual stream at every layer boundary,
     int8 codes and scales at every quantisation point). For each layer the
@@ -111,9 +114,10 @@ def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3, calls=None):
     om = oracle.OracleModel(model, max_seq=P)
     widths = (c.dim, c.n_heads * c.head_dim, c.dim, c.ffn)
     report = []
+    checked = list(range(c.n_layers)) if layers is None else sorted(layers)
     for start, n, _ in calls:
         rows = slice(start, start + n)
-        for L in range(c.n_layers):
+        for L in checked:
             y, st = om.layer_forced(L, X[L][rows], codes[L][:, rows], scales[L][:, rows], start)
             assert np.array_equal(bits(y), bits(X[L + 1][rows])), \
                 f"layer {L}, positions {start}..: residual rows differ with equal codes"
@@ -125,7 +129,7 @@ def layerwise_forced(model, g, toks, chunk, margin_tol=4e-3, calls=None):
                 if st["scale_mismatches"][pt]:
                     assert st["max_scale_rel"][pt] <= 1e-5, (L, pt, st)
             report.append(st)
-    for L in range(c.n_layers):
+    for L in checked:
         for which in (0, 1):
             ref = om.kv(L, which)[:P]
             got = g.kv(L, which, 0, P)
