@@ -253,7 +253,7 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 
 template <int EPI, int NT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT, const TcParams p) {
+    k_gemm_tw(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT, const TcParams p) {
   using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ppdev::smem_u32(smem_raw);
@@ -673,8 +673,8 @@ int max_clusters() {
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.numAttrs = 0;  // the kernel declares its cluster shape
     int c = 0;
-    cudaFuncSetAttribute(k_gemm_tc<EPI_STORE, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (cudaOccupancyMaxActiveClusters(&c, k_gemm_tc<EPI_STORE, 128>, &cfg) != cudaSuccess || c <= 0) {
+    cudaFuncSetAttribute(k_gemm_tw<EPI_STORE, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (cudaOccupancyMaxActiveClusters(&c, k_gemm_tw<EPI_STORE, 128>, &cfg) != cudaSuccess || c <= 0) {
       cudaGetLastError();
       int dev = 0, sms = 0;
       cudaGetDevice(&dev);
@@ -692,11 +692,11 @@ cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& mt, const TcParam
   using C = Cfg<NT>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tw<EPI, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl_if(pdl, k_gemm_tc<EPI, NT>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, mw, mt,
+  return launch_pdl_if(pdl, k_gemm_tw<EPI, NT>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, mw, mt,
                        p);
 }
 

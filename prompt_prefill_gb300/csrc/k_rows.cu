@@ -276,8 +276,12 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // Output projection of the last position ("Single-pass prefill": logits for
-// the last position only). One warp per vocabulary row; the int32 dot product
-// is exact, so the lane split does not matter.
+// the last position only). Each warp takes kLmRows vocabulary rows at a time and
+// walks their k range together, so the loads of all of them are in flight at
+// once; the int32 dot products are exact, so neither the lane split nor the
+// row grouping changes a result.
+constexpr int kLmRows = 4;
+
 __global__ void __launch_bounds__(kRowThreads)
     k_lm_head(const int8_t* __restrict__ q8, const float* __restrict__ a_scale, const int8_t* __restrict__ w,
               const float* __restrict__ ws, int vocab, int dim, float* __restrict__ logits) {
@@ -291,20 +295,35 @@ __global__ void __launch_bounds__(kRowThreads)
   const int lane = threadIdx.x & 31;
   const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const int n_warps = (gridDim.x * kRowThreads) >> 5;
-  for (int v = warp; v < vocab; v += n_warps) {
-    const int4* wr = reinterpret_cast<const int4*>(w + (size_t)v * dim);
-    int acc = 0;
-#pragma unroll 4
-    for (int c = lane; c < n16; c += 32) {
-      const int4 a = __ldg(wr + c);
-      const int4 b = qs[c];
-      acc = __dp4a(a.x, b.x, acc);
-      acc = __dp4a(a.y, b.y, acc);
-      acc = __dp4a(a.z, b.z, acc);
-      acc = __dp4a(a.w, b.w, acc);
+  const int4* w4 = reinterpret_cast<const int4*>(w);
+  for (int v0 = warp * kLmRows; v0 < vocab; v0 += n_warps * kLmRows) {
+    int acc[kLmRows];
+    const int4* wr[kLmRows];
+#pragma unroll
+    for (int r = 0; r < kLmRows; ++r) {
+      acc[r] = 0;
+      wr[r] = w4 + (size_t)min(v0 + r, vocab - 1) * n16;  // rows past the end repeat the last; never stored
     }
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) logits[v] = ppdev::dequant(acc, ws[v], as);
+#pragma unroll 2
+    for (int c = lane; c < n16; c += 32) {
+      const int4 b = qs[c];
+      int4 a[kLmRows];
+#pragma unroll
+      for (int r = 0; r < kLmRows; ++r) a[r] = __ldg(wr[r] + c);
+#pragma unroll
+      for (int r = 0; r < kLmRows; ++r) {
+        acc[r] = __dp4a(a[r].x, b.x, acc[r]);
+        acc[r] = __dp4a(a[r].y, b.y, acc[r]);
+        acc[r] = __dp4a(a[r].z, b.z, acc[r]);
+        acc[r] = __dp4a(a[r].w, b.w, acc[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kLmRows; ++r) {
+      int v = acc[r];
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && v0 + r < vocab) logits[v0 + r] = ppdev::dequant(v, ws[v0 + r], as);
+    }
   }
 }
 

@@ -231,7 +231,7 @@ def test_attention_row_result_independent_of_chunk(torch, rows, start):
     assert np.array_equal(bits(host(whole)), bits(host(single)))
 
 
-@pytest.mark.parametrize("vocab,dim", [(1024, 256), (5000, 4096)])
+@pytest.mark.parametrize("vocab,dim", [(1024, 256), (5000, 4096), (128257, 2048)])  # last: a ragged group of rows
 def test_lm_head_bit_exact(torch, vocab, dim):
     x = synth.normal_f32(71, 1, (1, dim), 0.0, 1.0)
     q8, s = oracle.quantize_rows(x)
