@@ -871,7 +871,7 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the 350M, 1B and streamed measurements that follow the 8B line")
     ap.add_argument("--overlap", type=int, default=1,
-                    help="1 (default): consecutive chunks on eight streams (pp_set_chunk_overlap); 0: serial")
+                    help="1 (default): consecutive chunks on their own streams, up to 32 (pp_set_chunk_overlap); 0: serial")
     ap.add_argument("--graphs", type=int, default=1,
                     help="1 (default): each prefill call replayed from a CUDA graph after its first (pp_set_graphs)")
     ap.add_argument("--profile-step", action="store_true",

@@ -208,7 +208,8 @@ int pp_reset_stats(pp_model* m);
 int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
 
 /* Chunk overlap (1 on, 0 off; off after pp_model_load). The chunks of a call
- * rotate over eight streams, each with its own scratch set; a chunk waits, layer
+ * rotate over min(32, chunks of the call) streams, each with its own scratch
+ * set; a chunk waits, layer
  * by layer, only for the earlier chunks' K/V rows of that layer before its
  * attention reads them ("Single-pass prefill": K/V history written position
  * by position), so one chunk's kernels can use the SMs the others leave idle.
@@ -216,11 +217,13 @@ int pp_set_profile_kernel(pp_model* m, int32_t kernel_class);
  * through their layers concurrently. Layer-outer order, resident or streamed:
  * the chunks of each layer run concurrently (streamed: every stream waits for
  * the layer's copy, and the ring slot is released after all of them). Results
- * are bit-identical to the serial order. The first call that turns it on
- * allocates seven more scratch sets and streams (PP_ERR_OOM if that fails)
- * after waiting for the model's work. Ignored while the per-layer profile is
- * on, for calls of a single chunk, and for streamed weights in chunk-outer
- * order. */
+ * are bit-identical to the serial order. This call allocates nothing: the
+ * first prefill call that needs more streams than exist so far allocates the
+ * missing scratch sets (each sized for max_chunk rows), streams and events
+ * after waiting for the model's work, before it launches anything (PP_ERR_OOM
+ * if that fails; what was made stays for later calls). Ignored while the
+ * per-layer profile is on, for calls of a single chunk, and for streamed
+ * weights in chunk-outer order. */
 int pp_set_chunk_overlap(pp_model* m, int32_t enable);
 
 /* CUDA graphs (1 on, 0 off; off after pp_model_load). With graphs on, the

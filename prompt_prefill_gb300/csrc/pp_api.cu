@@ -201,7 +201,7 @@ struct pp_model {
   TcWorkspace tcws;  // stream-K partial tiles and counters of the projection GEMMs
   float* attn_part = nullptr;  // per-key-range partial attention state of one chunk
   size_t attn_part_bytes = 0;
-  // chunk overlap (pp_set_chunk_overlap): consecutive chunks rotate over
+  // chunk overlap (pp_set_chunk_overlap): consecutive chunks rotate over up to
   // kOverlap streams (the compute stream and ostream[]), each with its own
   // scratch set (the fields above hold the active one, sets[] all of them);
   // chunk k waits for chunk k-1's K/V rows of a layer (qkv_ev) before its
@@ -216,11 +216,14 @@ struct pp_model {
     CUtensorMap amap[3];
     CUtensorMap amap_tw[3][3];
   };
-  static constexpr int kOverlap = 8;
+  // Up to kOverlap chunks in flight, one stream and scratch set each; a call uses
+  // min(kOverlap, its chunks). Measured on the 350M workload (24 chunks of 32):
+  // 8 / 16 / 24 / 32 streams gave 10.4 / 8.6 / 6.9 / 6.9 ms per call.
+  static constexpr int kOverlap = 32;
   bool overlap = false;
   bool gemm_wide = false;  // the current call overlaps chunks: widest GEMM tiles, no stream-K
-  bool sets_ready = false;
-  int sets_alloc = 1;  // scratch sets fully allocated (set 0 at load)
+  int sets_alloc = 1;      // scratch sets fully allocated (set 0 at load)
+  int streams_ready = 1;   // overlap streams (set 0: the model's stream) with their K/V events
   int active_set = 0;
   Scratch sets[kOverlap]{};
   cudaStream_t ostream[kOverlap - 1] = {};
@@ -862,6 +865,36 @@ int head(pp_model* m, cudaStream_t cs, const float* xlast, float* d_logits) {
   return PP_OK;
 }
 
+// Streams a call with chunk overlap uses: one per chunk, at most kOverlap.
+int overlap_streams(int n, int chunk) { return std::min(pp_model::kOverlap, (n + chunk - 1) / chunk); }
+
+// Scratch sets, streams and K/V events for `ns` chunks in flight. Runs before
+// a call (never inside a graph capture). A step that fails leaves what it made
+// in place (released with the model); a later call resumes from there.
+int ensure_overlap(pp_model* m, int ns) {
+  if (ns <= m->sets_alloc && ns <= m->streams_ready) return PP_OK;
+  PP_TRY(sync_model(m));
+  for (int j = m->sets_alloc; j < ns; ++j) {
+    use_scratch(m, j);  // the set is (re)allocated into its fields
+    const int rc = alloc_scratch(m, false);
+    use_scratch(m, 0);
+    if (rc != PP_OK) return rc;
+    m->sets_alloc = j + 1;
+  }
+  for (int j = m->streams_ready; j < ns; ++j) {
+    if (!m->ostream[j - 1]) PP_CUDA(cudaStreamCreateWithFlags(&m->ostream[j - 1], cudaStreamNonBlocking));
+    m->streams_ready = j + 1;
+  }
+  for (int p = 0; p < ns; ++p)
+    while ((int)m->qkv_ev[p].size() < m->cfg.n_layers) {
+      cudaEvent_t e;
+      PP_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+      m->qkv_ev[p].push_back(e);
+    }
+  PP_CUDA(cudaStreamSynchronize(m->stream));  // the new sets' initial clears
+  return PP_OK;
+}
+
 int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
                  cudaStream_t st) {
   const pp_config& c = m->cfg;
@@ -931,8 +964,12 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     // inputs are its own), so chunk k's layer l can fill the SMs the others
     // leave idle between their kernels. Chunk k-NS ran on the same stream: its
     // scratch set is free in stream order.
-    constexpr int NS = pp_model::kOverlap;
-    cudaStream_t S[NS];
+    const int NS = overlap_streams(n, chunk);
+    if (NS > m->sets_alloc || NS > m->streams_ready) {
+      set_err("chunk overlap needs %d scratch sets", NS);
+      return PP_ERR_CUDA;
+    }
+    cudaStream_t S[pp_model::kOverlap];
     S[0] = cs;
     cudaEvent_t e;
     PP_TRY(ev_get(m, &e));
@@ -1011,8 +1048,12 @@ int prefill_impl(pp_model* m, const int32_t* d_tok, int n, int start_pos, int ch
     // streamed weights every stream waits for the layer's copy and the ring
     // slot is freed only after every stream's work on the layer.
     const bool ovl = m->overlap && !m->layer_prof && n > chunk;
-    constexpr int NS = pp_model::kOverlap;
-    cudaStream_t S[NS];
+    const int NS = ovl ? overlap_streams(n, chunk) : 1;
+    if (NS > m->sets_alloc || NS > m->streams_ready) {
+      set_err("chunk overlap needs %d scratch sets", NS);
+      return PP_ERR_CUDA;
+    }
+    cudaStream_t S[pp_model::kOverlap];
     S[0] = cs;
     for (int i = 1; i < NS; ++i) S[i] = ovl ? m->ostream[i - 1] : cs;
     auto fan = [&](bool out) -> int {  // out: the others wait for cs; in: cs waits for the others
@@ -1124,6 +1165,9 @@ void graphs_clear(pp_model* m) {
 int prefill_call(pp_model* m, const int32_t* d_tok, int n, int start_pos, int chunk, float* d_logits,
                  cudaStream_t st) {
   const pp_config& c = m->cfg;
+  const bool layer_outer = c.loop_order == PP_LOOP_LAYER_OUTER;
+  if (m->overlap && !m->layer_prof && n > chunk && (layer_outer || c.mode != PP_MODE_STREAMED))
+    PP_TRY(ensure_overlap(m, overlap_streams(n, chunk)));
   const bool use_graph = m->graphs && c.mode == PP_MODE_RESIDENT && !c.kv_grow && c.profile_kernel == PP_KERNEL_NONE &&
                          !m->trace && !m->layer_prof;
   if (!use_graph) return prefill_impl(m, d_tok, n, start_pos, chunk, d_logits, st);
@@ -1422,29 +1466,7 @@ int pp_set_chunk_overlap(pp_model* m, int32_t enable) {
     set_err("bad pp_set_chunk_overlap arguments");
     return PP_ERR_ARG;
   }
-  if (enable && !m->sets_ready) {
-    // A call that failed part of the way leaves what it made in place (released
-    // with the model); a later call resumes from there.
-    PP_TRY(sync_model(m));
-    for (int j = m->sets_alloc; j < pp_model::kOverlap; ++j) {
-      use_scratch(m, j);  // the set is (re)allocated into its fields
-      const int rc = alloc_scratch(m, false);
-      use_scratch(m, 0);
-      if (rc != PP_OK) return rc;
-      m->sets_alloc = j + 1;
-    }
-    for (int j = 1; j < pp_model::kOverlap; ++j)
-      if (!m->ostream[j - 1]) PP_CUDA(cudaStreamCreateWithFlags(&m->ostream[j - 1], cudaStreamNonBlocking));
-    for (int p = 0; p < pp_model::kOverlap; ++p)
-      while ((int)m->qkv_ev[p].size() < m->cfg.n_layers) {
-        cudaEvent_t e;
-        PP_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
-        m->qkv_ev[p].push_back(e);
-      }
-    PP_CUDA(cudaStreamSynchronize(m->stream));  // the new sets' initial clears
-    m->sets_ready = true;
-  }
-  m->overlap = enable != 0;
+  m->overlap = enable != 0;  // streams and scratch sets are made by the first call that needs them
   return PP_OK;
 }
 
