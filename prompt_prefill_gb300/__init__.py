@@ -216,11 +216,14 @@ def pp_model_free(h: int):
     lib().pp_model_free(h)
 
 
-def pp_prefill(h: int, tokens, start_pos: int, chunk: int, vocab: int) -> np.ndarray:
+def pp_prefill(h: int, tokens, start_pos: int, chunk: int, vocab: int, out: np.ndarray | None = None) -> np.ndarray:
+    """Host-buffer prefill; `out` (f32 [vocab], contiguous, e.g. in pinned memory) receives the logits."""
     t = np.ascontiguousarray(tokens, dtype=np.int32)
-    logits = np.empty((vocab,), np.float32)
-    _check(lib().pp_prefill(h, _ptr(t), t.size, start_pos, chunk, _ptr(logits)), "pp_prefill")
-    return logits
+    if out is None:
+        out = np.empty((vocab,), np.float32)
+    assert out.dtype == np.float32 and out.shape == (vocab,) and out.flags["C_CONTIGUOUS"]
+    _check(lib().pp_prefill(h, _ptr(t), t.size, start_pos, chunk, _ptr(out)), "pp_prefill")
+    return out
 
 
 def pp_prefill_rc(h: int, tokens, start_pos: int, chunk: int, vocab: int) -> int:
@@ -457,9 +460,9 @@ class PrefillModel:
         except Exception:
             pass
 
-    def prefill(self, tokens, start_pos=0, chunk=None):
+    def prefill(self, tokens, start_pos=0, chunk=None, out=None):
         t = np.ascontiguousarray(tokens, dtype=np.int32)
-        return pp_prefill(self.h, t, start_pos, chunk or self.cfg.max_chunk, self.vocab)
+        return pp_prefill(self.h, t, start_pos, chunk or self.cfg.max_chunk, self.vocab, out)
 
     def prefill_device(self, d_tokens, n, start_pos, chunk, d_logits, stream=None):
         pp_prefill_device(self.h, d_tokens, n, start_pos, chunk, d_logits, stream)
