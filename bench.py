@@ -828,7 +828,7 @@ def run_op(args):
             pp.pp_op_gemm(engine, pp.PP_EPI_STORE, a, a16, w, ws, as_, m, n, k, out, n)
         work, unit, bound = 2.0 * m * n * k, "TFLOP/s", "tensor"
     elif args.op == "attention":
-        H, Hkv, hd = 32, 8, 128
+        H, Hkv, hd = args.heads, args.kv_heads, args.hd
         start = args.start
         q = torch.randn((m, H, hd), device="cuda")
         kc = torch.randn((start + m, Hkv, hd), device="cuda")
@@ -884,6 +884,9 @@ def main(argv=None):
                     help="after the timed steps, run one more step between cudaProfilerStart and cudaProfilerStop "
                          "(for ncu --profile-from-start off)")
     ap.add_argument("--op", default=None, help="time one kernel alone: gemm | attention | quant | norm_quant")
+    ap.add_argument("--heads", type=int, default=32, help="--op attention: query heads")
+    ap.add_argument("--kv-heads", type=int, default=8, help="--op attention: KV heads")
+    ap.add_argument("--hd", type=int, default=128, help="--op attention: head dim (64 or 128)")
     ap.add_argument("--m", type=int, default=512)
     ap.add_argument("--n", type=int, default=28672)
     ap.add_argument("--k", type=int, default=4096)
