@@ -310,6 +310,21 @@ def time_calls(stream, fn, steps: int, warmup: int) -> float:
     return e0.elapsed_time(e1) / steps
 
 
+def time_calls_each(stream, fn, calls: int) -> list:
+    """Milliseconds of each of `calls` calls of fn() (CUDA events around every call on `stream`)."""
+    import torch
+
+    out = []
+    for _ in range(calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
 def profile_classes(g, step, steps_dominant: int = 1):
     """Per kernel class: summed launch time of one step with every launch of the class bracketed by CUDA
     events on its stream (chunks in serial order, so no other kernel runs inside a bracket). The
@@ -452,7 +467,9 @@ def run_streamed_config(args, model, cfg8) -> dict:
     cfg = synth.CONFIGS["8b-streamed"]
     chunk = 512
     bw = h2d_bandwidth_gbs()
-    steps, warm = max(1, min(args.steps, 3)), 3
+    # the host link is shared with the machine's other work: every call is timed on its own and the median of
+    # five reported (with the fastest and slowest), so one disturbed copy does not move the figure
+    steps, warm = 5, 3
     out = {"h2d_gbs_measured": bw, "ring_slots": 2, "chunk": chunk,
            "weights": "the resident workload's 8B-shaped weights, held in pinned host memory by the library"}
     for order, tag in ((pp.PP_LOOP_CHUNK_OUTER, "chunk_outer"), (pp.PP_LOOP_LAYER_OUTER, "layer_outer")):
@@ -468,12 +485,14 @@ def run_streamed_config(args, model, cfg8) -> dict:
                 g.prefill_device(d_tok, P, 0, chunk, d_logits, stream)
             torch.cuda.synchronize()
             g.reset_stats()
-            ms = time_calls(stream, lambda: g.prefill_device(d_tok, P, 0, chunk, d_logits, stream), steps, 0)
+            each = sorted(time_calls_each(stream, lambda: g.prefill_device(d_tok, P, 0, chunk, d_logits, stream), steps))
+            ms = each[len(each) // 2]
             st = g.stats()
             h2d = st["h2d_bytes"] / steps
             visits = (1 if order == pp.PP_LOOP_LAYER_OUTER else -(-P // chunk)) * cfg8.n_layers
             layer_block = h2d / visits  # device-resident ids: the layer copies are the only host-to-device bytes
-            res[str(P)] = {"tok_per_s": P / (ms / 1000), "ms": ms, "h2d_bytes_per_prompt": h2d,
+            res[str(P)] = {"tok_per_s": P / (ms / 1000), "ms": ms, "ms_min_max": [each[0], each[-1]],
+                           "h2d_bytes_per_prompt": h2d,
                            "h2d_bytes_naive_per_prompt": layer_block * cfg8.n_layers * P,
                            "prefetch_hits": st["prefetch_hits"] // steps, "prefetch_misses": st["prefetch_misses"] // steps,
                            "h2d_bound_tok_per_s": P / (h2d / (bw * 1e9)), "frac_of_h2d_bound": (h2d / (bw * 1e9)) / (ms / 1000)}
