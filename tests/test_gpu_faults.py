@@ -128,3 +128,35 @@ def test_allocation_cap_gives_oom_without_damage():
         assert np.array_equal(bits(got), bits(ref))
     finally:
         pp.pp_debug_alloc_cap(0)
+
+
+def test_chunk_overlap_sets_are_made_on_demand_and_resume_after_oom():
+    # pp_set_chunk_overlap allocates nothing; a call of several chunks makes the scratch sets it needs first
+    # (here over the cap: PP_ERR_OOM before anything is launched), and a later call resumes from there
+    torch_cuda()
+    mod = synth.make_model(synth.CONFIGS["350m"])
+    c = mod.cfg
+    toks = synth.prompt(c, 200)  # 7 chunks of 32
+    ref_g = load(mod, max_seq=1024, max_chunk=32)
+    ref = ref_g.prefill(toks, 0, 32)
+    ref_kv = ref_g.kv(5, 1, 0, 200)
+    ref_g.kv_reset()
+    ref_one = ref_g.prefill(toks[:32], 0, 32)
+    ref_g.close()
+    g = load(mod, max_seq=1024, max_chunk=32)
+    try:
+        pp.pp_debug_alloc_cap(1)  # any further device allocation is over the cap
+        g.set_chunk_overlap(True)
+        one = g.prefill(toks[:32], 0, 32)  # a single chunk needs no second set
+        assert np.array_equal(bits(one), bits(ref_one))
+        g.kv_reset()
+        assert pp.pp_prefill_rc(g.h, toks, 0, 32, c.vocab) == pp.PP_ERR_OOM
+        pp.pp_debug_alloc_cap(0)
+        g.kv_reset()
+        got = g.prefill(toks, 0, 32)
+        assert np.array_equal(bits(got), bits(ref))
+        assert np.array_equal(bits(g.kv(5, 1, 0, 200)), bits(ref_kv))
+    finally:
+        pp.pp_debug_alloc_cap(0)
+        g.close()
+
