@@ -312,8 +312,9 @@ def test_head_dim_128_fused_rope_engines_and_oracle():
 
 def test_1b_chunk_overlap_bit_identical(one_b):
     # Chunks rotating over the overlap streams (each waits only for the previous chunk's K/V rows of a
-    # layer) give the serial path's bits: logits, K/V rows, ragged chunks (21 chunks of 100: more than
-    # streams) and a continuation call.
+    # layer) give the serial path's bits: logits, K/V rows, ragged chunks (21 chunks of 100), more chunks
+    # than streams (64 chunks of 32 on 32 streams: chunk k + 32 reuses chunk k's stream and scratch set),
+    # launch by launch and replayed from a graph, and a continuation call.
     m, g = one_b
     toks = synth.prompt(m.cfg)  # 2048 tokens
     g.kv_reset()
@@ -321,14 +322,20 @@ def test_1b_chunk_overlap_bit_identical(one_b):
     kv_ref = [g.kv(L, which, 0, len(toks)) for L in (0, m.cfg.n_layers - 1) for which in (0, 1)]
     g.set_chunk_overlap(True)
     try:
-        for chunk in (256, 512, 100):
+        for chunk in (256, 512, 100, 32):
             g.kv_reset()
             assert np.array_equal(bits(g.prefill(toks, 0, chunk)), bits(ref)), chunk
-        kv = [g.kv(L, which, 0, len(toks)) for L in (0, m.cfg.n_layers - 1) for which in (0, 1)]
-        for a, b in zip(kv, kv_ref):
-            assert np.array_equal(bits(a), bits(b))
+            kv = [g.kv(L, which, 0, len(toks)) for L in (0, m.cfg.n_layers - 1) for which in (0, 1)]
+            for a, b in zip(kv, kv_ref):
+                assert np.array_equal(bits(a), bits(b)), chunk
+        g.set_graphs(True)
+        for _ in range(2):  # capture, then replay
+            g.kv_reset()
+            assert np.array_equal(bits(g.prefill(toks, 0, 32)), bits(ref))
+        g.set_graphs(False)
         g.kv_reset()
         g.prefill(toks[:1000], 0, 256)
         assert np.array_equal(bits(g.prefill(toks[1000:], 1000, 256)), bits(ref))
     finally:
+        g.set_graphs(False)
         g.set_chunk_overlap(False)
