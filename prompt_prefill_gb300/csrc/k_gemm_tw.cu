@@ -41,38 +41,47 @@ constexpr int WM = 128;            // weight rows per CTA (256 per pair): the M 
 constexpr int BK = 64;             // k per stage
 constexpr int W_BYTES = WM * BK;   // int8 weights of one CTA per stage (8 KB, 64-byte swizzle)
 constexpr int A_COLS = BK / 2;     // TMEM columns of one converted stage (two fp16 per column)
-constexpr int STAGES = 8;          // pipeline stages (shared memory and TMEM weight slots)
 constexpr int N_CONV_WARPS = 4;    // warpgroup 1: int8 -> fp16 into TMEM, one thread per weight row
 constexpr int N_DRAIN_WARPS = 8;   // warpgroups 2-3: 2 per TMEM lane quarter, NT/2 token columns each
 constexpr int THREADS = 512;       // warpgroup 0: TMA, MMA, 2 idle
 constexpr int CONV_WARP0 = 4;
 constexpr int DRAIN_WARP0 = 8;
-// Register split (setmaxnreg): launched at 128 per thread (16 x 32 x 128 = 65536 in the
-// pool); warpgroup 0 drops to 48, the converters to 72 and the drain warpgroups rise to
-// 192 (up to 128 running sums and 64 accumulator columns in flight): 128 x 48 + 128 x 72 +
-// 256 x 192 = 64512 of 65536, and per SM sub-partition (48 + 72 + 192 + 192) x 32 = 16128.
-constexpr int REGS_ROLE = 48, REGS_CONV = 72, REGS_DRAIN = 192;
 constexpr int MAX_SEG_KB = 16;     // 16 x 64 = 1024 products per exact f32 segment
 constexpr int MIN_SK_KB = 64;      // NT = 128: stream-K only when each cluster owns >= 64 k-blocks
-// Every CTA allocates all 512 TMEM columns, so two of these CTAs must never share an SM
-// (a pair would wait on another pair's columns): each CTA asks for more than half of the
-// SM's shared memory.
+// A CTA of the full form (NT = 128) allocates all 512 TMEM columns, so two of them must
+// never share an SM (a pair would wait on another pair's columns): each asks for more than
+// half of the SM's shared memory.
 constexpr int MIN_SMEM = 120 * 1024;
 
 constexpr int BAR_BYTES = 512;      // mbarriers, the TMEM address slot and two flags
 
-// Per-token-tile constants.
+// Per-token-tile constants. NT = 128: 8 stages, all 512 TMEM columns, one CTA per SM,
+// registers launched at 128 per thread and split (setmaxnreg) 48 / 72 / 192 between
+// warpgroup 0, the converters and the drains (up to 128 running sums and 64 accumulator
+// columns in flight): 128 x 48 + 128 x 72 + 256 x 192 = 64512 of 65536. NT <= 64 (the lean
+// form): a launch is a latency chain (weights streamed once, few MMAs), so two CTAs share
+// an SM: 4 stages, 256 TMEM columns (two accumulators of NT plus four weight slots), no
+// shared-memory floor, registers launched at 64 and split 40 / 64 / 72 (128 x 40 + 128 x 64
+// + 256 x 72 = 31744 of the 32768 launched, half the file).
 template <int NT>
 struct Cfg {
+  static constexpr bool LEAN = NT <= 64;
+  static constexpr int STAGES = LEAN ? 4 : 8;            // pipeline stages (shared memory and TMEM weight slots)
+  static constexpr int TMEM_COLS = LEAN ? 256 : 512;
+  static constexpr int CTAS_PER_SM = LEAN ? 2 : 1;
+  static constexpr int R_LAUNCH = 65536 / (THREADS * CTAS_PER_SM);  // registers per thread at launch
+  static constexpr int R_ROLE = LEAN ? 40 : 48, R_CONV = LEAN ? 64 : 72, R_DRAIN = LEAN ? 72 : 192;
+  static_assert(R_ROLE <= R_LAUNCH && R_CONV <= R_LAUNCH && R_DRAIN >= R_LAUNCH, "dec / dec / inc");
+  static_assert(128 * R_ROLE + 128 * R_CONV + 256 * R_DRAIN <= R_LAUNCH * THREADS, "register split");
   static constexpr int TOK = NT / 2;                     // token rows per CTA
   static constexpr int T_BYTES = TOK * BK * 2;           // fp16 tokens of one CTA per stage
   static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;  // 16 / 12 / 10 KB
   static constexpr int COLS = NT / 2;                    // accumulator columns per drain warp
   static constexpr int TMEM_A0 = 2 * NT;                 // first column of the weight slots
-  static_assert(TMEM_A0 + STAGES * A_COLS <= 512, "TMEM: two accumulators and the weight slots");
+  static_assert(TMEM_A0 + STAGES * A_COLS <= TMEM_COLS, "TMEM: two accumulators and the weight slots");
   static_assert(STAGE_BYTES % 1024 == 0, "every stage keeps the 1024-byte swizzle atoms aligned");
   static constexpr int USED = STAGES * STAGE_BYTES + 1024 /*align*/ + BAR_BYTES + 2 * NT * 4 /*token scales*/;
-  static constexpr int SMEM_BYTES = USED > MIN_SMEM ? USED : MIN_SMEM;
+  static constexpr int SMEM_BYTES = (LEAN || USED > MIN_SMEM) ? USED : MIN_SMEM;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
@@ -252,26 +261,26 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 }
 
 template <int EPI, int NT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CTAS_PER_SM)
     k_gemm_tw(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT, const TcParams p) {
   using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ppdev::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + STAGES * C::STAGE_BYTES;
+  const uint32_t bars = base + C::STAGES * C::STAGE_BYTES;
   // full: one barrier per producer and stage (weights, tokens), so that a producer
   // that gives up can wait for exactly its own copies in flight
-  auto full_b = [&](int src, int s) { return bars + 8 * (src * STAGES + s); };
-  auto ready_b = [&](int s) { return bars + 8 * (2 * STAGES + s); };
-  auto empty_b = [&](int s) { return bars + 8 * (3 * STAGES + s); };
-  auto accf_b = [&](int b) { return bars + 8 * (4 * STAGES + b); };
-  auto acce_b = [&](int b) { return bars + 8 * (4 * STAGES + 2 + b); };
-  const uint32_t done_b = bars + 8 * (4 * STAGES + 4);
-  const uint32_t tmem_slot = bars + 8 * (4 * STAGES + 5);
-  static_assert(8 * (4 * STAGES + 6) + 8 <= BAR_BYTES, "barrier area");
+  auto full_b = [&](int src, int s) { return bars + 8 * (src * C::STAGES + s); };
+  auto ready_b = [&](int s) { return bars + 8 * (2 * C::STAGES + s); };
+  auto empty_b = [&](int s) { return bars + 8 * (3 * C::STAGES + s); };
+  auto accf_b = [&](int b) { return bars + 8 * (4 * C::STAGES + b); };
+  auto acce_b = [&](int b) { return bars + 8 * (4 * C::STAGES + 2 + b); };
+  const uint32_t done_b = bars + 8 * (4 * C::STAGES + 4);
+  const uint32_t tmem_slot = bars + 8 * (4 * C::STAGES + 5);
+  static_assert(8 * (4 * C::STAGES + 6) + 8 <= BAR_BYTES, "barrier area");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (tmem_slot + 8 - base));
-  float* const as_s = reinterpret_cast<float*>(gbase + STAGES * C::STAGE_BYTES + BAR_BYTES);  // [2][NT] token scales
+  float* const as_s = reinterpret_cast<float*>(gbase + C::STAGES * C::STAGE_BYTES + BAR_BYTES);  // [2][NT] token scales
   auto sW = [&](int s) { return base + s * C::STAGE_BYTES; };
   auto sT = [&](int s) { return base + s * C::STAGE_BYTES + W_BYTES; };
 
@@ -281,7 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int nkb = p.K / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       for (int src = 0; src < 2; ++src) mbar_init(full_b(src, s), 1);
       mbar_init(ready_b(s), 2 * N_CONV_WARPS);
       mbar_init(empty_b(s), 1);
@@ -296,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(512));
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(C::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   tc_fence_before();
@@ -320,20 +329,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0 || warp == 2) {
     // ---------------------------------------------------------------- TMA producers
     // One thread per operand stream: warp 0 the weights, warp 2 the tokens.
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_ROLE));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::R_ROLE));
     if (lane == 0) {
       const int src = warp == 0 ? 0 : 1;  // 0 weights, 1 tokens
       const uint32_t bytes = src == 0 ? W_BYTES : C::T_BYTES;
       int s = 0;
       uint32_t ph = 0;
-      int issued[STAGES] = {0};
+      int issued[C::STAGES] = {0};
       const Sched sc(p, cluster, n_clusters);
       int pre = 0;
-      for (int u = 0; src == 0 && p.early_w && u < sc.units() && pre < STAGES; ++u) {
+      for (int u = 0; src == 0 && p.early_w && u < sc.units() && pre < C::STAGES; ++u) {
         int t, kb0, kb1;
         sc.unit(u, t, kb0, kb1);
         const int w_row = (t / p.num_t_tiles) * 2 * WM + (int)rank * WM;
-        for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
+        for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
           mbar_expect_tx(full_b(0, pre), bytes);
           tma_load_2d(sW(pre), &tmW, kb * BK, w_row, full_b(0, pre));
           issued[pre] = 1;
@@ -357,21 +366,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               tma_load_2d(sT(s), &tmT, kb * BK, t_row, full_b(1, s));
             issued[s] = 1;
           }
-          if (++s == STAGES) { s = 0; ph ^= 1; }
+          if (++s == C::STAGES) { s = 0; ph ^= 1; }
         }
       }
       if (*abort_flag) {
         // let this stream's copies in flight land before the CTA's shared memory goes away
-        for (int i = 0; i < STAGES; ++i) {
-          const int st = (s + i) % STAGES;
-          const uint32_t sph = (s + i >= STAGES) ? ph ^ 1 : ph;
+        for (int i = 0; i < C::STAGES; ++i) {
+          const int st = (s + i) % C::STAGES;
+          const uint32_t sph = (s + i >= C::STAGES) ? ph ^ 1 : ph;
           if (issued[st]) mbar_wait(full_b(src, st), sph ^ 1, p.wait_cycles);
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (leader CTA)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_ROLE));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::R_ROLE));
     if (rank == 0 && lane == 0 && !p.hold_mma) {
       const uint32_t idesc = idesc_f16(2 * WM, NT);
       int s = 0;
@@ -397,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: 8 TMEM columns, 32 bytes of the swizzle atom
               mma_f16_pair_ta(d, a + 8 * k, db + (uint64_t)(2 * k), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
             mma_commit_pair(empty_b(s));
-            if (++s == STAGES) { s = 0; ph ^= 1; }
+            if (++s == C::STAGES) { s = 0; ph ^= 1; }
           }
           if (ok) mma_commit_pair(accf_b(buf));
         }
@@ -410,10 +419,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp < CONV_WARP0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_ROLE));  // warp 3: idle
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::R_ROLE));  // warp 3: idle
   } else if (warp < DRAIN_WARP0) {
     // ---------------------------------------------------------------- converters
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CONV));
+    if (C::R_CONV < C::R_LAUNCH) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::R_CONV));
     const int row = threadIdx.x - 32 * CONV_WARP0;  // this thread's weight row of the CTA, = its TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + C::TMEM_A0;
     const uint32_t swz = (uint32_t)((row >> 1) & 3);  // 64-byte swizzle of the TMA tile: chunk c at c ^ swz
@@ -446,11 +455,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(ready_b(s), 0);
-      if (++s == STAGES) { s = 0; ph ^= 1; }
+      if (++s == C::STAGES) { s = 0; ph ^= 1; }
     }
   } else {
     // ---------------------------------------------------------------- drains + epilogue
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_DRAIN));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::R_DRAIN));
     constexpr int COLS = C::COLS;
     const int et = threadIdx.x - 32 * DRAIN_WARP0;  // 0..255
     const int quarter = warp & 3;                   // TMEM lanes (weight rows) 32*quarter .. +31
@@ -646,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
   }
 }
 
@@ -694,6 +703,11 @@ cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& mt, const TcParam
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tw<EPI, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // the register split (setmaxnreg) assumes the launch allocation R_LAUNCH per thread: a drain's
+    // increase would wait forever on a smaller pool, so refuse to launch on any other count
+    cudaFuncAttributes fa{};
+    if ((e = cudaFuncGetAttributes(&fa, k_gemm_tw<EPI, NT>)) != cudaSuccess) return e;
+    if (fa.numRegs != C::R_LAUNCH) return cudaErrorInvalidConfiguration;
     attr = true;
   }
   return launch_pdl_if(pdl, k_gemm_tw<EPI, NT>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, mw, mt,
