@@ -47,7 +47,7 @@ constexpr int THREADS = 512;       // warpgroup 0: TMA, MMA, 2 idle
 constexpr int CONV_WARP0 = 4;
 constexpr int DRAIN_WARP0 = 8;
 constexpr int MAX_SEG_KB = 16;     // 16 x 64 = 1024 products per exact f32 segment
-constexpr int MIN_SK_KB = 64;      // NT = 128: stream-K only when each cluster owns >= 64 k-blocks
+constexpr int MIN_SK_KB = 32;      // NT = 128: stream-K gives each cluster >= 32 k-blocks
 // A CTA of the full form (NT = 128) allocates all 512 TMEM columns, so two of them must
 // never share an SM (a pair would wait on another pair's columns): each asks for more than
 // half of the SM's shared memory.
@@ -671,28 +671,47 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// Co-resident CTA pairs (one pair per 2 SMs).
-int max_clusters() {
+// Co-resident CTA pairs of the NT form. The cluster occupancy query counts one pair per
+// two SMs for either form; the lean form (NT <= 64) fits two CTAs on an SM, so its count
+// is that times the CTAs an SM holds (measured: two lean pairs per two SMs run side by
+// side, 64 x 28672 x 4096 in 38 instead of 60 us).
+template <int NT>
+int max_clusters_t() {
   static int n = 0;
   if (!n) {
-    using C = Cfg<128>;
+    using C = Cfg<NT>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.numAttrs = 0;  // the kernel declares its cluster shape
-    int c = 0;
-    cudaFuncSetAttribute(k_gemm_tw<EPI_STORE, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (cudaOccupancyMaxActiveClusters(&c, k_gemm_tw<EPI_STORE, 128>, &cfg) != cudaSuccess || c <= 0) {
+    int c = 0, dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(k_gemm_tw<EPI_STORE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (cudaOccupancyMaxActiveClusters(&c, k_gemm_tw<EPI_STORE, NT>, &cfg) != cudaSuccess || c <= 0) {
       cudaGetLastError();
-      int dev = 0, sms = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       c = sms / 2;
     }
-    n = c;
+    // CTAs of this form an SM holds, from its registers and shared memory (the per-SM
+    // occupancy query does not take kernels with a compile-time cluster shape)
+    cudaFuncAttributes fa{};
+    int regs_sm = 0, smem_sm = 0, smem_reserved = 0;
+    cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (cudaFuncGetAttributes(&fa, k_gemm_tw<EPI_STORE, NT>) == cudaSuccess)
+      for (per_sm = C::CTAS_PER_SM; per_sm > 1; --per_sm)
+        if ((long long)fa.numRegs * THREADS * per_sm <= regs_sm &&
+            (long long)(C::SMEM_BYTES + fa.sharedSizeBytes + smem_reserved) * per_sm <= smem_sm)
+          break;
+    cudaGetLastError();
+    n = std::max(1, c * std::max(1, per_sm));
   }
   return n;
+}
+int max_clusters(int nt) {
+  return nt == 128 ? max_clusters_t<128>() : (nt == 64 ? max_clusters_t<64>() : max_clusters_t<32>());
 }
 
 template <int EPI, int NT>
@@ -769,18 +788,19 @@ Plan plan(int m, int n, int k, bool wide) {
   const int nkb = k / BK;
   pl.num_t_tiles = (m + pl.nt - 1) / pl.nt;
   pl.num_tiles = pl.num_t_tiles * ((n + 2 * WM - 1) / (2 * WM));
-  const int mc = max_clusters();
+  const int mc = max_clusters(pl.nt);
   if (wide || pl.num_tiles >= mc) {
     pl.clusters = std::min(pl.num_tiles, mc);
     return pl;
   }
-  // Fewer tiles than CTA pairs: split the (tile, k-block) space evenly when every
-  // pair gets enough k-blocks to amortise the partial-tile exchange (whose cost
-  // grows with the tile: MIN_SK_KB at NT = 128, one exact segment at NT <= 64).
+  // Fewer tiles than CTA pairs: split the (tile, k-block) space evenly, each pair
+  // taking at least min_kb k-blocks to amortise the partial-tile exchange (whose cost
+  // grows with the tile: MIN_SK_KB at NT = 128, one exact segment at NT <= 64), and
+  // whole tiles when that leaves a pair all of K.
   const long long total = (long long)pl.num_tiles * nkb;
   const int min_kb = pl.nt == 128 ? MIN_SK_KB : MAX_SEG_KB;
-  const int ipc = std::max((int)((total + mc - 1) / mc), MAX_SEG_KB);  // at least one exact segment per cluster
-  if (ipc < min_kb || ipc >= nkb) {
+  const int ipc = std::max((int)((total + mc - 1) / mc), std::max(MAX_SEG_KB, min_kb));
+  if (ipc >= nkb) {
     pl.clusters = std::min(pl.num_tiles, mc);
     return pl;
   }
@@ -829,7 +849,7 @@ cudaError_t launch_gemm_tw(int epi, const CUtensorMap& mt, const CUtensorMap& mw
     p.part = wsp.part;
     p.cnt = wsp.cnt;
   } else {
-    pl.clusters = std::min(pl.num_tiles, max_clusters());  // no workspace: whole tiles
+    pl.clusters = std::min(pl.num_tiles, max_clusters(pl.nt));  // no workspace: whole tiles
   }
   switch (epi) {
     case EPI_STORE: return launch_nt<EPI_STORE>(nt, mw, mt, p, pl.clusters, s, pdl);
