@@ -40,12 +40,15 @@ TC_SHAPES = [(1, 256, 64), (8, 768, 256), (37, 256, 768), (130, 512, 320), (200,
 # Both tcgen05 kernels and every tile: chunks of at most 128 rows run 256
 # weight rows x 32 / 64 / 128 tokens (weights in tensor memory), longer chunks
 # 256 tokens x 256 / 192 / 128 weight rows; with whole tiles and with stream-K
-# partial tiles (few tiles and long k on 76 CTA pairs): the 350M down projection
-# at a 32-row chunk, a 64-row chunk over k = 8192, the 8B down projection at
-# 512 rows, and a ragged 300-row chunk with k not a multiple of the 1024-k
-# segment.
+# partial tiles (fewer tiles than CTA pairs and long k; a GB300 holds 76 pairs
+# of the full forms and 152 of the lean short-chunk form): the 350M down
+# projection at a 32-row chunk, a 64-row chunk over k = 8192, the 8B down
+# projection at 512 rows, a ragged 300-row chunk with k not a multiple of the
+# 1024-k segment, a 100-row chunk split 32 k-blocks per pair, and a 24-row
+# chunk over 96 weight tiles whose K is split into runs of 29 k-blocks (not a
+# whole number of segments) across ~150 lean pairs.
 WIDTH_SHAPES = [(16, 19456, 128), (40, 14592, 192), (290, 512, 1024), (32, 1024, 4096), (64, 2048, 8192),
-                (512, 4096, 14336), (512, 28672, 4096), (300, 4096, 2880), (100, 4096, 4096)]
+                (512, 4096, 14336), (512, 28672, 4096), (300, 4096, 2880), (100, 4096, 4096), (24, 24576, 2880)]
 
 
 @pytest.mark.parametrize("m,n,k", TC_SHAPES)
@@ -92,6 +95,13 @@ def test_tc_and_mma_engines_agree_at_8b_shapes(torch):
         rng = np.random.default_rng(n)
         for t, r in zip(rng.integers(0, m, 64), rng.integers(0, n, 64)):
             assert tc[t, r] == oracle.dot_i8(a[t], w[r])
+
+
+def test_short_chunk_shapes_plan_stream_k(torch):
+    # the stream-K cases above are stream-K on this device (the plan depends on its SM count)
+    for m, n, k in ((32, 1024, 4096), (64, 2048, 8192), (100, 4096, 4096), (24, 24576, 2880)):
+        part, counters = pp.pp_op_gemm_noalloc_need(m, n, k)
+        assert part > 0 and counters > 0, (m, n, k)
 
 
 @pytest.mark.parametrize("m,n,k", WIDTH_SHAPES)
