@@ -52,10 +52,15 @@ constexpr int MIN_SK_KB = 32;      // NT = 128: stream-K gives each cluster >= 3
 // never share an SM (a pair would wait on another pair's columns): each asks for more than
 // half of the SM's shared memory.
 constexpr int MIN_SMEM = 120 * 1024;
+constexpr int SMEM_SM = 233472;     // shared memory of an SM, 1 KB of it reserved per resident CTA
 
-constexpr int BAR_BYTES = 512;      // mbarriers, the TMEM address slot and two flags
+constexpr int BAR_BYTES = 1024;     // mbarriers, the TMEM address slot and two flags
 
-// Per-token-tile constants. NT = 128: 8 stages, all 512 TMEM columns, one CTA per SM,
+// Per-token-tile constants. The int8 weights stream through a ring of W_STAGES shared-memory
+// stages that the converters free as soon as they have read them (not when the MMA is done
+// with the k-block, as the tokens and the converted weights in their TMEM slots are); a
+// deeper weight ring (12-16 stages, all the shared memory) measured no faster.
+// NT = 128: 8 stages, all 512 TMEM columns, one CTA per SM,
 // registers launched at 128 per thread and split (setmaxnreg) 48 / 72 / 192 between
 // warpgroup 0, the converters and the drains (up to 128 running sums and 64 accumulator
 // columns in flight): 128 x 48 + 128 x 72 + 256 x 192 = 64512 of 65536. NT <= 64 (the lean
@@ -66,7 +71,8 @@ constexpr int BAR_BYTES = 512;      // mbarriers, the TMEM address slot and two 
 template <int NT>
 struct Cfg {
   static constexpr bool LEAN = NT <= 64;
-  static constexpr int STAGES = LEAN ? 4 : 8;            // pipeline stages (shared memory and TMEM weight slots)
+  static constexpr int STAGES = LEAN ? 4 : 8;            // token stages and TMEM weight slots
+  static constexpr int W_STAGES = STAGES;                // int8 weight stages
   static constexpr int TMEM_COLS = LEAN ? 256 : 512;
   static constexpr int CTAS_PER_SM = LEAN ? 2 : 1;
   static constexpr int R_LAUNCH = 65536 / (THREADS * CTAS_PER_SM);  // registers per thread at launch
@@ -75,14 +81,15 @@ struct Cfg {
   static_assert(128 * R_ROLE + 128 * R_CONV + 256 * R_DRAIN <= R_LAUNCH * THREADS, "register split");
   static constexpr int TOK = NT / 2;                     // token rows per CTA
   static constexpr int T_BYTES = TOK * BK * 2;           // fp16 tokens of one CTA per stage
-  static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;  // 16 / 12 / 10 KB
+  static constexpr int W_RING = W_STAGES * W_BYTES, T_RING = STAGES * T_BYTES;
   static constexpr int COLS = NT / 2;                    // accumulator columns per drain warp
   static constexpr int TMEM_A0 = 2 * NT;                 // first column of the weight slots
   static_assert(TMEM_A0 + STAGES * A_COLS <= TMEM_COLS, "TMEM: two accumulators and the weight slots");
-  static_assert(STAGE_BYTES % 1024 == 0, "every stage keeps the 1024-byte swizzle atoms aligned");
-  static constexpr int USED = STAGES * STAGE_BYTES + 1024 /*align*/ + BAR_BYTES + 2 * NT * 4 /*token scales*/;
+  static_assert(W_BYTES % 1024 == 0 && T_BYTES % 1024 == 0, "every stage keeps the 1024-byte swizzle atoms aligned");
+  static constexpr int USED = W_RING + T_RING + 1024 /*align*/ + BAR_BYTES + 2 * NT * 4 /*token scales*/;
   static constexpr int SMEM_BYTES = (LEAN || USED > MIN_SMEM) ? USED : MIN_SMEM;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(CTAS_PER_SM * (SMEM_BYTES + 1024) <= SMEM_SM, "CTAs per SM by shared memory");
 };
 
 struct TcParams {
@@ -151,6 +158,9 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t a, uint32_t rank) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_local(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   uint32_t ok;
@@ -268,21 +278,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
   const uint32_t raw = ppdev::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + C::STAGES * C::STAGE_BYTES;
-  // full: one barrier per producer and stage (weights, tokens), so that a producer
-  // that gives up can wait for exactly its own copies in flight
-  auto full_b = [&](int src, int s) { return bars + 8 * (src * C::STAGES + s); };
-  auto ready_b = [&](int s) { return bars + 8 * (2 * C::STAGES + s); };
-  auto empty_b = [&](int s) { return bars + 8 * (3 * C::STAGES + s); };
-  auto accf_b = [&](int b) { return bars + 8 * (4 * C::STAGES + b); };
-  auto acce_b = [&](int b) { return bars + 8 * (4 * C::STAGES + 2 + b); };
-  const uint32_t done_b = bars + 8 * (4 * C::STAGES + 4);
-  const uint32_t tmem_slot = bars + 8 * (4 * C::STAGES + 5);
-  static_assert(8 * (4 * C::STAGES + 6) + 8 <= BAR_BYTES, "barrier area");
+  const uint32_t bars = base + C::W_RING + C::T_RING;
+  // full: one barrier per producer and stage (weight stage, token stage), so that a
+  // producer that gives up can wait for exactly its own copies in flight; wfree: the
+  // converters have read a weight stage; ready / empty: a token stage and its TMEM slot
+  // are loaded and converted / read by the MMA.
+  constexpr int WS = C::W_STAGES, TS = C::STAGES, NB0 = 2 * WS + 3 * TS;
+  auto full_b = [&](int src, int s) { return bars + 8 * (src == 0 ? s : WS + s); };
+  auto ready_b = [&](int s) { return bars + 8 * (WS + TS + s); };
+  auto empty_b = [&](int s) { return bars + 8 * (WS + 2 * TS + s); };
+  auto wfree_b = [&](int s) { return bars + 8 * (WS + 3 * TS + s); };
+  auto accf_b = [&](int b) { return bars + 8 * (NB0 + b); };
+  auto acce_b = [&](int b) { return bars + 8 * (NB0 + 2 + b); };
+  const uint32_t done_b = bars + 8 * (NB0 + 4);
+  const uint32_t tmem_slot = bars + 8 * (NB0 + 5);
+  static_assert(8 * (NB0 + 6) + 8 <= BAR_BYTES, "barrier area");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (tmem_slot + 8 - base));
-  float* const as_s = reinterpret_cast<float*>(gbase + C::STAGES * C::STAGE_BYTES + BAR_BYTES);  // [2][NT] token scales
-  auto sW = [&](int s) { return base + s * C::STAGE_BYTES; };
-  auto sT = [&](int s) { return base + s * C::STAGE_BYTES + W_BYTES; };
+  float* const as_s = reinterpret_cast<float*>(gbase + C::W_RING + C::T_RING + BAR_BYTES);  // [2][NT] token scales
+  auto sW = [&](int s) { return base + s * W_BYTES; };
+  auto sT = [&](int s) { return base + C::W_RING + s * C::T_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cta_rank();
@@ -290,8 +304,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
   const int nkb = p.K / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      for (int src = 0; src < 2; ++src) mbar_init(full_b(src, s), 1);
+    for (int s = 0; s < WS; ++s) {
+      mbar_init(full_b(0, s), 1);
+      mbar_init(wfree_b(s), N_CONV_WARPS);  // this CTA's converter warps
+    }
+    for (int s = 0; s < TS; ++s) {
+      mbar_init(full_b(1, s), 1);
       mbar_init(ready_b(s), 2 * N_CONV_WARPS);
       mbar_init(empty_b(s), 1);
     }
@@ -333,16 +351,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
     if (lane == 0) {
       const int src = warp == 0 ? 0 : 1;  // 0 weights, 1 tokens
       const uint32_t bytes = src == 0 ? W_BYTES : C::T_BYTES;
+      const int RS = src == 0 ? WS : TS;  // this stream's ring
       int s = 0;
       uint32_t ph = 0;
-      int issued[C::STAGES] = {0};
+      int issued[WS > TS ? WS : TS] = {0};
       const Sched sc(p, cluster, n_clusters);
       int pre = 0;
-      for (int u = 0; src == 0 && p.early_w && u < sc.units() && pre < C::STAGES; ++u) {
+      for (int u = 0; src == 0 && p.early_w && u < sc.units() && pre < WS; ++u) {
         int t, kb0, kb1;
         sc.unit(u, t, kb0, kb1);
         const int w_row = (t / p.num_t_tiles) * 2 * WM + (int)rank * WM;
-        for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+        for (int kb = kb0; kb < kb1 && pre < WS; ++kb, ++pre) {
           mbar_expect_tx(full_b(0, pre), bytes);
           tma_load_2d(sW(pre), &tmW, kb * BK, w_row, full_b(0, pre));
           issued[pre] = 1;
@@ -358,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
         const int t_row = (t % p.num_t_tiles) * NT + (int)rank * C::TOK;
         for (int kb = kb0; kb < kb1; ++kb, ++g) {
           if (g >= pre) {
-            if (!mbar_wait(empty_b(s), ph ^ 1, p.wait_cycles)) { fail(); break; }
+            if (!mbar_wait(src == 0 ? wfree_b(s) : empty_b(s), ph ^ 1, p.wait_cycles)) { fail(); break; }
             mbar_expect_tx(full_b(src, s), bytes);
             if (src == 0)
               tma_load_2d(sW(s), &tmW, kb * BK, w_row, full_b(0, s));
@@ -366,14 +385,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
               tma_load_2d(sT(s), &tmT, kb * BK, t_row, full_b(1, s));
             issued[s] = 1;
           }
-          if (++s == C::STAGES) { s = 0; ph ^= 1; }
+          if (++s == RS) { s = 0; ph ^= 1; }
         }
       }
       if (*abort_flag) {
         // let this stream's copies in flight land before the CTA's shared memory goes away
-        for (int i = 0; i < C::STAGES; ++i) {
-          const int st = (s + i) % C::STAGES;
-          const uint32_t sph = (s + i >= C::STAGES) ? ph ^ 1 : ph;
+        for (int i = 0; i < RS; ++i) {
+          const int st = (s + i) % RS;
+          const uint32_t sph = (s + i >= RS) ? ph ^ 1 : ph;
           if (issued[st]) mbar_wait(full_b(src, st), sph ^ 1, p.wait_cycles);
         }
       }
@@ -433,14 +452,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
       sc.unit(u, t, a, b);
       total_kb += b - a;
     }
-    int s = 0;
-    uint32_t ph = 0;
+    int s = 0, sw = 0;  // token stage / TMEM slot, weight stage
+    uint32_t ph = 0, phw = 0;
     for (int kb = 0; kb < total_kb; ++kb) {
-      // this stage's weights, and its tokens (the MMA reads them once the converters arrive)
-      bool landed = !*abort_flag;
-      for (int src = 0; src < 2 && landed; ++src) landed = mbar_wait(full_b(src, s), ph, p.wait_cycles);
+      // this k-block's weights, and its tokens (the MMA reads them once the converters
+      // arrive; their load was issued after the MMA had freed TMEM slot s)
+      bool landed = !*abort_flag && mbar_wait(full_b(0, sw), phw, p.wait_cycles);
+      landed = landed && mbar_wait(full_b(1, s), ph, p.wait_cycles);
       if (!landed) { fail(); break; }
-      const uint8_t* wr = gbase + (sW(s) - base) + row * 64;
+      const uint8_t* wr = gbase + (sW(sw) - base) + row * 64;
       uint32_t f[32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // k = 16c .. 16c + 15
@@ -450,12 +470,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, Cfg<NT>::CT
         i8x4_to_f16x4(w.z, f[8 * c + 4], f[8 * c + 5]);
         i8x4_to_f16x4(w.w, f[8 * c + 6], f[8 * c + 7]);
       }
+      // every lane has read its row of the weight stage; order those generic-proxy reads
+      // before the TMA (async proxy) write that refills the stage once it is free (without
+      // this fence, with the weight ring running 12-16 stages ahead, a refill was seen to
+      // overtake the reads under concurrent launches)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(wfree_b(sw));
+      if (++sw == WS) { sw = 0; phw ^= 1; }
       tmem_st32(lane_addr + s * A_COLS, f);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(ready_b(s), 0);
-      if (++s == C::STAGES) { s = 0; ph ^= 1; }
+      if (++s == TS) { s = 0; ph ^= 1; }
     }
   } else {
     // ---------------------------------------------------------------- drains + epilogue
