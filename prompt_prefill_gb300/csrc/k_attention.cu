@@ -363,12 +363,11 @@ template <int HD>
 cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows, int start_pos, int H, int Hkv,
                      float* o, float* part, size_t part_bytes, cudaStream_t s, bool pdl) {
   constexpr int smem = (ROWS * HD + 2 * KB * HD + KB * PS) * (int)sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attention<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(k_attention<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (e != cudaSuccess) return e;
   const int G = H / Hkv;
   const int bq = ROWS / G;
   const int n_tiles = (rows + bq - 1) / bq;
@@ -376,8 +375,8 @@ cudaError_t launch_t(const float* q, const float* kc, const float* vc, int rows,
   if (n_ranges > 1 && (!part || part_bytes < attention_workspace_bytes(rows, start_pos, H, Hkv, HD)))
     return cudaErrorInvalidValue;
   const float qscale = (float)(1.4426950408889634 / sqrt((double)HD));
-  cudaError_t e = launch_pdl_if(pdl, k_attention<HD>, dim3(n_tiles * Hkv * n_ranges), dim3(THREADS), (size_t)smem, s,
-                                q, kc, vc, rows, start_pos, H, Hkv, o, qscale, part, n_ranges);
+  e = launch_pdl_if(pdl, k_attention<HD>, dim3(n_tiles * Hkv * n_ranges), dim3(THREADS), (size_t)smem, s, q, kc, vc,
+                    rows, start_pos, H, Hkv, o, qscale, part, n_ranges);
   if (e == cudaSuccess && n_ranges > 1)
     e = launch_pdl(k_attention_merge<HD>, dim3(n_tiles * Hkv * (ROWS * HD / 4 / 256)), dim3(256), 0, s, rows,
                    start_pos, H, Hkv, o, (const float*)part, n_ranges);

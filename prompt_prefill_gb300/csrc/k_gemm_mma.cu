@@ -151,12 +151,11 @@ __global__ void __launch_bounds__(THREADS) k_gemm_mma(const int8_t* __restrict__
 template <int EPI>
 cudaError_t launch_t(const int8_t* a8, const int8_t* w, const float* ws, const float* as, int m, int n, int k,
                      float* out, int ldo, int32_t* acc, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mma<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(k_gemm_mma<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid((n + BN - 1) / BN, (m + BM - 1) / BM);
   k_gemm_mma<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(a8, w, ws, as, m, n, k, out, ldo, acc);
   return cudaGetLastError();

@@ -707,8 +707,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // Co-resident CTA pairs of the widest configuration (one pair per 2 SMs).
 int max_clusters() {
-  static int n = 0;
-  if (!n) {
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device(cache, [] {
     using C = Cfg<256>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
@@ -724,21 +724,19 @@ int max_clusters() {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       c = sms / 2;
     }
-    n = c;
-  }
-  return n;
+    return c;
+  });
 }
 
 template <int EPI, int BN>
 cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mw, const TcParams& p, int clusters, cudaStream_t s,
                      bool pdl) {
   using C = Cfg<BN>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(k_gemm_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl_if(pdl, k_gemm_tc<EPI, BN>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, ma, mw, p);
 }
 

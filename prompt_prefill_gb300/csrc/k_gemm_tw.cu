@@ -705,8 +705,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // side, 64 x 28672 x 4096 in 38 instead of 60 us).
 template <int NT>
 int max_clusters_t() {
-  static int n = 0;
-  if (!n) {
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device(cache, [] {
     using C = Cfg<NT>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
@@ -734,9 +734,8 @@ int max_clusters_t() {
             (long long)(C::SMEM_BYTES + fa.sharedSizeBytes + smem_reserved) * per_sm <= smem_sm)
           break;
     cudaGetLastError();
-    n = std::max(1, c * std::max(1, per_sm));
-  }
-  return n;
+    return std::max(1, c * std::max(1, per_sm));
+  });
 }
 int max_clusters(int nt) {
   return nt == 128 ? max_clusters_t<128>() : (nt == 64 ? max_clusters_t<64>() : max_clusters_t<32>());
@@ -746,17 +745,17 @@ template <int EPI, int NT>
 cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& mt, const TcParams& p, int clusters, cudaStream_t s,
                      bool pdl) {
   using C = Cfg<NT>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tw<EPI, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+  static std::atomic<uint64_t> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    cudaError_t r = cudaFuncSetAttribute(k_gemm_tw<EPI, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (r != cudaSuccess) return r;
     // the register split (setmaxnreg) assumes the launch allocation R_LAUNCH per thread: a drain's
     // increase would wait forever on a smaller pool, so refuse to launch on any other count
     cudaFuncAttributes fa{};
-    if ((e = cudaFuncGetAttributes(&fa, k_gemm_tw<EPI, NT>)) != cudaSuccess) return e;
-    if (fa.numRegs != C::R_LAUNCH) return cudaErrorInvalidConfiguration;
-    attr = true;
-  }
+    if ((r = cudaFuncGetAttributes(&fa, k_gemm_tw<EPI, NT>)) != cudaSuccess) return r;
+    return fa.numRegs == C::R_LAUNCH ? cudaSuccess : cudaErrorInvalidConfiguration;
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl_if(pdl, k_gemm_tw<EPI, NT>, dim3(2 * clusters), dim3(THREADS), (size_t)C::SMEM_BYTES, s, mw, mt,
                        p);
 }

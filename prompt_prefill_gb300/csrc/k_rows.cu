@@ -335,14 +335,13 @@ __global__ void k_widen_i8(const int8_t* __restrict__ a, long long n, __half* __
 }
 
 int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device(cache, [] {
+    int dev = 0, n = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+    return n > 0 ? n : 148;
+  });
 }
 
 }  // namespace

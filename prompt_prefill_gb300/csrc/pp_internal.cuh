@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include <cstdint>
@@ -13,6 +14,36 @@
 #include "pp.h"
 
 namespace pp {
+
+// Host-side facts kept per device (a kernel's shared-memory attribute set, occupancy
+// counts): one slot per device ordinal below kMaxDevices, recomputed on every call above.
+constexpr int kMaxDevices = 64;
+
+// Runs `set` (returning cudaError_t) on the current device until it has succeeded once there.
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < kMaxDevices ? (uint64_t)1 << dev : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// The positive int `get()` computes for the current device, computed once per device.
+template <typename F>
+int per_device(std::atomic<int> (&cache)[kMaxDevices], F&& get) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return get();
+  int v = cache[dev].load(std::memory_order_acquire);
+  if (v <= 0) {
+    v = get();
+    cache[dev].store(v, std::memory_order_release);
+  }
+  return v;
+}
 
 // Epilogue selector of the GEMM kernels (PP_EPI_* plus the raw int32 form).
 // EPI_ROPE (tcgen05 engine only): RoPE + K/V write of a QKV projection whose q and k
